@@ -1,0 +1,166 @@
+/*
+ * sgq.h -- fused pre-GEMM activation epilogue for NVIDIA GB300 (sm_103a).
+ *
+ * Two operations, each one CUDA kernel launch on the caller's stream:
+ *
+ *   rmsnorm_add_quant  residual add + RMSNorm + FP8 activation quantisation
+ *                      (+ optional bf16 copy of the normed rows)
+ *   swiglu_quant       fp32 SwiGLU (OAI clamped, or SiLU-and-mul)
+ *                      + the same quantisation
+ *
+ * The operations follow these pages:
+ *   [P1] "[ROCm][MiniMax-M3.1] Fuse MXFP8 quant into the add+RMSNorm and
+ *        SwiGLU epilogues" (vllm PR 65478): "Purpose" (the two fusions),
+ *        "Test Plan / Correctness" (bit-identical norm, fp32-direct SwiGLU),
+ *        review "Scale layout / scheme contract" (row-major, unswizzled
+ *        [M, N/32] E8M0 scales).
+ *   [P2] "[Perf] [AMD] qwen3: Fuse the 1x128 FP8 input quant into RMSNorm
+ *        and SiLU-and-mul" (sglang PR 48043): "Modifications" (1x128 group
+ *        FP8; SiLU-and-mul rounded like the unfused op; bf16 inputs only).
+ *   [P4] "[ROCm] Fuse per-token activation quant into RMSNorm" (sglang PR
+ *        34502): "Change" (per-token FP8, [m, 1] scale).
+ *
+ * Conventions shared by both entry points
+ *   - All pointers are DEVICE pointers owned by the caller. The library
+ *     allocates nothing, keeps no state between calls, never synchronises and
+ *     launches nothing but its one kernel, so calls may be captured into CUDA
+ *     graphs.
+ *   - All tensors are contiguous and row-major. Inputs are bfloat16. Quantised
+ *     values are OCP E4M3 ("e4m3fn") bytes.
+ *   - Scale layouts: MXFP8 -> uint8 E8M0 codes [M, W/32] (value 2^(code-127));
+ *     1x128 block -> float32 [M, W/128]; per-token -> float32 [M, 1].
+ *   - Alignment: every tensor pointer must be 16-byte aligned, except a
+ *     float32 scale pointer (4 bytes) and an E8M0 scale pointer (1 byte).
+ *   - Width rules: MXFP8 needs W % 32 == 0, 1x128 needs W % 128 == 0,
+ *     per-token needs W % 8 == 0; W <= SGQ_MAX_WIDTH.
+ *   - Outputs may not overlap inputs or each other, except that residual_out
+ *     may equal residual_in exactly (in-place update).
+ *   - M == 0 returns SGQ_OK without a launch (pointers are not inspected).
+ *   - Errors: arguments are checked on the host before anything is launched;
+ *     a rejected call leaves every buffer untouched. SGQ_ERR_LAUNCH reports a
+ *     failed launch (cudaGetLastError after the launch).
+ *   - Non-finite inputs (inf, NaN) are outside the contract: the kernels do
+ *     not fault on them, but their outputs are unspecified.
+ */
+#ifndef SGQ_H
+#define SGQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SGQ_ABI_VERSION 1
+#define SGQ_MAX_WIDTH 32768
+
+/* Quantisation format of the output activation. */
+typedef enum sgq_format {
+    SGQ_FMT_MXFP8 = 0,          /* E4M3 + one E8M0 scale per 1x32 block [P1] */
+    SGQ_FMT_FP8_BLOCK128 = 1,   /* E4M3 + one fp32 scale amax/448 per 1x128 block [P2] */
+    SGQ_FMT_FP8_PER_TOKEN = 2   /* E4M3 + one fp32 scale amax/448 per row [P4] */
+} sgq_format_t;
+
+/* Activation of swiglu_quant. */
+typedef enum sgq_act {
+    SGQ_ACT_SWIGLU_OAI = 0,     /* min(g,L) * sigmoid(alpha*min(g,L)) * (clamp(u,-L,L) + beta) [P1] */
+    SGQ_ACT_SILU_MUL = 1        /* g * sigmoid(g) * u [P2] */
+} sgq_act_t;
+
+/* Flags. */
+#define SGQ_F_GEMMA_WEIGHT    (1u << 0) /* norm: scale by (1 + w) (Gemma) instead of w */
+#define SGQ_F_QUANT_FROM_FP32 (1u << 1) /* quantise the fp32 value, not its bf16 rounding */
+#define SGQ_F_ACT_ROUND_BF16  (1u << 2) /* SiLU-and-mul: round silu(g) to bf16 before the product */
+
+typedef enum sgq_status {
+    SGQ_OK = 0,
+    SGQ_ERR_INVALID_ARG = 1,    /* NULL required pointer, bad enum/flag, negative size, overlap */
+    SGQ_ERR_UNSUPPORTED = 2,    /* width not a multiple of the group, or above SGQ_MAX_WIDTH */
+    SGQ_ERR_MISALIGNED = 3,     /* a pointer breaks the alignment rule above */
+    SGQ_ERR_LAUNCH = 4          /* the CUDA launch failed */
+} sgq_status_t;
+
+/* A cudaStream_t (NULL selects the legacy default stream). */
+typedef void* sgq_stream_t;
+
+/*
+ * Residual add + RMSNorm + FP8 quantisation, one pass per row ([P1] "Purpose",
+ * commit 1; [P2] "Modifications"; [P4] "Change"). For each row i:
+ *
+ *   h   = x[i] + residual_in[i]            (fp32; h = x[i] if residual_in is NULL)
+ *   residual_out[i] = bf16(h)              (if residual_out is not NULL)
+ *   inv = 1 / sqrt(sum_j h_j^2 / H + eps)
+ *   y   = h * inv * (1 + w)  with SGQ_F_GEMMA_WEIGHT, else h * inv * w
+ *   normed_out[i] = bf16(y)                (if normed_out is not NULL)
+ *   src = y with SGQ_F_QUANT_FROM_FP32, else bf16(y)
+ *   q_out[i], scale_out[i] = quantise(src) in format fmt
+ *
+ * Quantisation of one group (32, 128 or H elements) with amax = max |src|:
+ *   MXFP8: e = clamp(floor(log2(amax)) - 8, -127, 127) (amax = 0 -> -127);
+ *          scale code = e + 127; q = E4M3_rn_satfinite(src * 2^-e).
+ *   FP8:   s = fp32(amax / 448); q = E4M3_rn_satfinite(fp32(src / s));
+ *          s = 0 gives q = 0.
+ *
+ * Arguments:
+ *   fmt           sgq_format_t
+ *   flags         SGQ_F_GEMMA_WEIGHT | SGQ_F_QUANT_FROM_FP32 (others rejected)
+ *   M, H          rows and hidden width
+ *   eps           >= 0, finite
+ *   x             [M, H] bf16, read
+ *   residual_in   [M, H] bf16, read, or NULL
+ *   residual_out  [M, H] bf16, written, or NULL; must be NULL when residual_in
+ *                 is NULL; may equal residual_in
+ *   weight        [H] bf16, read
+ *   q_out         [M, H] E4M3, written
+ *   scale_out     scales in the layout of fmt, written
+ *   normed_out    [M, H] bf16, written, or NULL
+ *   stream        the stream to launch on
+ */
+int rmsnorm_add_quant(int fmt, uint32_t flags, int64_t M, int64_t H, float eps,
+                      const void* x, const void* residual_in, void* residual_out,
+                      const void* weight, void* q_out, void* scale_out, void* normed_out,
+                      sgq_stream_t stream);
+
+/*
+ * SwiGLU + FP8 quantisation, one pass per row ([P1] "Purpose", commit 2 and
+ * "Test Plan / Correctness"; [P2] "Modifications"). gate_up is [M, 2I] bf16:
+ * gate g = columns [0, I), up u = columns [I, 2I). For each element:
+ *
+ *   OAI:  g' = min(g, limit); u' = min(max(u, -limit), limit);
+ *         a = g' * sigmoid(alpha * g') * (u' + beta)       (fp32)
+ *   SiLU: a = silu(g) * u, silu(g) = g * sigmoid(g)       (fp32); with
+ *         SGQ_F_ACT_ROUND_BF16 silu(g) is rounded to bf16 before the product
+ *   src = a with SGQ_F_QUANT_FROM_FP32, else bf16(a)
+ *   q_out, scale_out = quantise(src) as for rmsnorm_add_quant.
+ *
+ * [P1]'s fused OAI SwiGLU quantises the fp32 value (SGQ_F_QUANT_FROM_FP32);
+ * [P2]'s SiLU-and-mul rounds like the unfused op (SGQ_F_ACT_ROUND_BF16 and
+ * no SGQ_F_QUANT_FROM_FP32).
+ *
+ * Arguments:
+ *   fmt, act      sgq_format_t, sgq_act_t
+ *   flags         SGQ_F_QUANT_FROM_FP32, and SGQ_F_ACT_ROUND_BF16 with
+ *                 SGQ_ACT_SILU_MUL only (others rejected)
+ *   M, I          rows and intermediate width (the output width)
+ *   alpha, beta, limit  OAI parameters (finite alpha and beta, limit > 0,
+ *                 may be +inf); ignored for SiLU-and-mul
+ *   gate_up       [M, 2I] bf16, read
+ *   q_out         [M, I] E4M3, written
+ *   scale_out     scales in the layout of fmt, written
+ *   stream        the stream to launch on
+ */
+int swiglu_quant(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float alpha,
+                 float beta, float limit, const void* gate_up, void* q_out, void* scale_out,
+                 sgq_stream_t stream);
+
+/* A static, human-readable name of a status code. */
+const char* sgq_status_string(int status);
+
+/* SGQ_ABI_VERSION of the loaded library. */
+int sgq_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGQ_H */

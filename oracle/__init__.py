@@ -1,0 +1,147 @@
+"""CPU oracle of the fused norm / SwiGLU + FP8 quantisation ops.
+
+TEST INFRASTRUCTURE ONLY: the tests, `__graft_entry__.smoke()` and the
+benchmark's CPU-baseline leg use it; the library's product path never imports
+it. It wraps `sgq_oracle.c` (plain fp64 C, scalar loops) through ctypes and
+takes and returns numpy arrays. Inputs are raw bf16 bit patterns (uint16).
+
+Every function computes the definitions stated in `sgq_oracle.c`. Parity pins
+(closed forms, brute force and the pages' printed statistics) are in
+tests/test_oracle_*.py.
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import numpy as np
+
+from .build import build_oracle
+
+FORMATS = {"mxfp8": 0, "block128": 1, "per_token": 2}
+ACTS = {"swiglu_oai": 0, "silu_mul": 1}
+F_GEMMA, F_FROM_FP32, F_ACT_ROUND_BF16 = 1, 2, 4
+AMB_SRC, AMB_CODE = 1, 2
+REL_WINDOW = 2.0 ** -20
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    global _lib
+    if _lib is None:
+        L = C.CDLL(build_oracle())
+        L.ora_bf16_decode.restype = C.c_double
+        L.ora_bf16_decode.argtypes = [C.c_uint16]
+        L.ora_bf16_round.restype = C.c_uint16
+        L.ora_bf16_round.argtypes = [C.c_double]
+        L.ora_e4m3_decode.restype = C.c_double
+        L.ora_e4m3_decode.argtypes = [C.c_uint8]
+        L.ora_e4m3_encode.restype = C.c_uint8
+        L.ora_e4m3_encode.argtypes = [C.c_double]
+        L.ora_mx_scale_exp.restype = C.c_int
+        L.ora_mx_scale_exp.argtypes = [C.c_double]
+        p = C.c_void_p
+        L.ora_rmsnorm_add_quant.restype = C.c_int
+        L.ora_rmsnorm_add_quant.argtypes = [C.c_int, C.c_uint, C.c_long, C.c_long, C.c_float,
+                                            p, p, p, p, p, p, p, p, p, p, p, C.c_double]
+        L.ora_swiglu_quant.restype = C.c_int
+        L.ora_swiglu_quant.argtypes = [C.c_int, C.c_int, C.c_uint, C.c_long, C.c_long, C.c_float,
+                                       C.c_float, C.c_float, p, p, p, p, p, p, p, C.c_double]
+        _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(C.c_void_p)
+
+
+def bf16_decode(b: int) -> float:
+    return lib().ora_bf16_decode(int(b) & 0xFFFF)
+
+
+def bf16_round(v: float) -> int:
+    return int(lib().ora_bf16_round(float(v)))
+
+
+def e4m3_decode(c: int) -> float:
+    return lib().ora_e4m3_decode(int(c) & 0xFF)
+
+
+def e4m3_encode(v: float) -> int:
+    return int(lib().ora_e4m3_encode(float(v)))
+
+
+def mx_scale_exp(amax: float) -> int:
+    return int(lib().ora_mx_scale_exp(float(amax)))
+
+
+def _group(fmt: str, width: int) -> int:
+    return {"mxfp8": 32, "block128": 128, "per_token": width}[fmt]
+
+
+def _scale_array(fmt: str, M: int, width: int) -> np.ndarray:
+    ng = width // _group(fmt, width)
+    return np.zeros((M, ng), dtype=np.uint8 if fmt == "mxfp8" else np.float32)
+
+
+def _u16(a, shape):
+    a = np.ascontiguousarray(a, dtype=np.uint16)
+    assert a.shape == shape, (a.shape, shape)
+    return a
+
+
+def rmsnorm_add_quant(fmt: str, x: np.ndarray, r: np.ndarray | None, w: np.ndarray, *,
+                      eps: float, gemma: bool, from_fp32: bool, normed: bool = True,
+                      diagnostics: bool = True, rel: float = REL_WINDOW) -> dict:
+    """Residual add + RMSNorm + FP8 quantisation of rows x [M,H] (bf16 bits).
+
+    Returns q (uint8 [M,H]), scale ([M,G] uint8 E8M0 codes or float32),
+    residual (uint16 bits or None), normed (uint16 bits or None) and, with
+    diagnostics, y (fp64 normed values), t (fp64 E4M3 arguments), amb and gamb.
+    """
+    M, H = x.shape
+    x = _u16(x, (M, H))
+    r = None if r is None else _u16(r, (M, H))
+    w = _u16(w, (H,))
+    q = np.zeros((M, H), np.uint8)
+    s = _scale_array(fmt, M, H)
+    r_out = np.zeros((M, H), np.uint16) if r is not None else None
+    n_out = np.zeros((M, H), np.uint16) if normed else None
+    y = t = amb = gamb = None
+    if diagnostics:
+        y, t = np.zeros((M, H)), np.zeros((M, H))
+        amb, gamb = np.zeros((M, H), np.uint8), np.zeros(s.shape, np.uint8)
+    flags = (F_GEMMA if gemma else 0) | (F_FROM_FP32 if from_fp32 else 0)
+    rc = lib().ora_rmsnorm_add_quant(FORMATS[fmt], flags, M, H, float(eps), _ptr(x), _ptr(r), _ptr(w),
+                                     _ptr(r_out), _ptr(n_out), _ptr(q), _ptr(s), _ptr(y), _ptr(t),
+                                     _ptr(amb), _ptr(gamb), rel)
+    if rc != 0:
+        raise ValueError(f"oracle rejected arguments (fmt={fmt}, M={M}, H={H})")
+    return {"q": q, "scale": s, "residual": r_out, "normed": n_out, "y": y, "t": t,
+            "amb": amb, "gamb": gamb}
+
+
+def swiglu_quant(fmt: str, act: str, gate_up: np.ndarray, *, from_fp32: bool,
+                 round_act_bf16: bool = False, alpha: float = 1.702, beta: float = 1.0,
+                 limit: float = 7.0, diagnostics: bool = True, rel: float = REL_WINDOW) -> dict:
+    """SwiGLU (OAI clamped or SiLU-and-mul) + FP8 quantisation of gate_up [M, 2I] (bf16 bits).
+
+    Returns q (uint8 [M,I]), scale, and with diagnostics a (fp64 activation),
+    t, amb and gamb.
+    """
+    M, I2 = gate_up.shape
+    I = I2 // 2
+    gu = _u16(gate_up, (M, I2))
+    q = np.zeros((M, I), np.uint8)
+    s = _scale_array(fmt, M, I)
+    a = t = amb = gamb = None
+    if diagnostics:
+        a, t = np.zeros((M, I)), np.zeros((M, I))
+        amb, gamb = np.zeros((M, I), np.uint8), np.zeros(s.shape, np.uint8)
+    flags = (F_FROM_FP32 if from_fp32 else 0) | (F_ACT_ROUND_BF16 if round_act_bf16 else 0)
+    rc = lib().ora_swiglu_quant(FORMATS[fmt], ACTS[act], flags, M, I, float(alpha), float(beta),
+                                float(limit), _ptr(gu), _ptr(q), _ptr(s), _ptr(a), _ptr(t),
+                                _ptr(amb), _ptr(gamb), rel)
+    if rc != 0:
+        raise ValueError(f"oracle rejected arguments (fmt={fmt}, act={act}, M={M}, I={I})")
+    return {"q": q, "scale": s, "a": a, "t": t, "amb": amb, "gamb": gamb}

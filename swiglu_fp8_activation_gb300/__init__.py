@@ -1,0 +1,19 @@
+"""Fused pre-GEMM activation epilogue for NVIDIA GB300 (sm_103a).
+
+Two fused ops behind a C ABI (`libsgq.so`, declared in include/sgq.h):
+
+* `rmsnorm_add_quant`: residual add + RMSNorm (Gemma `(1+w)` or plain `w`)
+  + FP8 activation quantisation, with an optional bf16 copy of the normed rows.
+* `swiglu_quant`: fp32 SwiGLU (OAI clamped, or SiLU-and-mul) + the same
+  quantisation.
+
+Formats: MXFP8 (E4M3 + one E8M0 scale per 1x32 block), 1x128 block FP8 with
+fp32 scales, and per-token FP8 with an [M,1] fp32 scale.
+
+The CUDA library is loaded on first use; a missing library raises an error
+(there is no CPU fallback).
+"""
+from .binding import (  # noqa: F401
+    FORMATS, ACTS, F_GEMMA_WEIGHT, F_QUANT_FROM_FP32, F_ACT_ROUND_BF16,
+    SgqError, library, library_path, rmsnorm_add_quant, swiglu_quant, status_string,
+)

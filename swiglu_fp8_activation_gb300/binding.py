@@ -1,0 +1,159 @@
+"""ctypes binding of libsgq.so (include/sgq.h), with the same entry-point names.
+
+Argument marshalling only: shape, dtype and device checks, output allocation
+with torch.empty, and the call. Every arithmetic step runs in the CUDA kernels.
+If the library is missing, the first call raises SgqError: there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_NAME = "libsgq.so"
+
+FORMATS = {"mxfp8": 0, "block128": 1, "per_token": 2}
+ACTS = {"swiglu_oai": 0, "silu_mul": 1}
+F_GEMMA_WEIGHT, F_QUANT_FROM_FP32, F_ACT_ROUND_BF16 = 1, 2, 4
+GROUP = {"mxfp8": 32, "block128": 128}
+
+_lib = None
+
+
+class SgqError(RuntimeError):
+    """A non-zero status from the library, or a missing library."""
+
+    def __init__(self, msg: str, status: int | None = None):
+        super().__init__(msg)
+        self.status = status
+
+
+def library_path() -> str:
+    return os.environ.get("SGQ_LIBRARY", os.path.join(HERE, LIB_NAME))
+
+
+def library() -> C.CDLL:
+    """Load libsgq.so (built in-tree by __graft_entry__.build())."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise SgqError(f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+        L = C.CDLL(path)
+        vp, i64 = C.c_void_p, C.c_int64
+        L.rmsnorm_add_quant.restype = C.c_int
+        L.rmsnorm_add_quant.argtypes = [C.c_int, C.c_uint32, i64, i64, C.c_float,
+                                        vp, vp, vp, vp, vp, vp, vp, vp]
+        L.swiglu_quant.restype = C.c_int
+        L.swiglu_quant.argtypes = [C.c_int, C.c_int, C.c_uint32, i64, i64, C.c_float, C.c_float,
+                                   C.c_float, vp, vp, vp, vp]
+        L.sgq_status_string.restype = C.c_char_p
+        L.sgq_status_string.argtypes = [C.c_int]
+        L.sgq_abi_version.restype = C.c_int
+        L.sgq_abi_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return library().sgq_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise SgqError(f"{what}: {status_string(status)} (status {status})", status)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> C.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+def scale_shape(fmt: str, M: int, W: int) -> tuple:
+    return (M, 1) if fmt == "per_token" else (M, W // GROUP[fmt])
+
+
+def scale_dtype(fmt: str) -> torch.dtype:
+    return torch.uint8 if fmt == "mxfp8" else torch.float32
+
+
+def _want(t: torch.Tensor, shape, dtype, name):
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype:
+        raise SgqError(f"{name}: expected {dtype} {tuple(shape)}, got {t.dtype} {tuple(t.shape)}")
+    if t.numel() and not t.is_contiguous():
+        raise SgqError(f"{name}: must be contiguous")
+
+
+def rmsnorm_add_quant(x: torch.Tensor, weight: torch.Tensor, *, fmt: str = "mxfp8",
+                      residual_in: torch.Tensor | None = None,
+                      residual_out: torch.Tensor | None = None, eps: float = 1e-6,
+                      gemma: bool = True, quant_from_fp32: bool = False, normed: bool = False,
+                      q_out: torch.Tensor | None = None, scale_out: torch.Tensor | None = None,
+                      normed_out: torch.Tensor | None = None, stream=None):
+    """Residual add + RMSNorm + FP8 quantisation (one kernel launch).
+
+    x [M,H] bf16; weight [H] bf16; residual_in [M,H] bf16 or None;
+    residual_out defaults to residual_in (in-place update) when residual_in is
+    given. Returns (q [M,H] uint8 E4M3, scale, normed [M,H] bf16 or None,
+    residual_out or None).
+    """
+    M, H = x.shape
+    _want(x, (M, H), torch.bfloat16, "x")
+    _want(weight, (H,), torch.bfloat16, "weight")
+    if residual_in is not None:
+        _want(residual_in, (M, H), torch.bfloat16, "residual_in")
+        if residual_out is None:
+            residual_out = residual_in
+    if residual_out is not None:
+        _want(residual_out, (M, H), torch.bfloat16, "residual_out")
+    dev = x.device
+    if q_out is None:
+        q_out = torch.empty((M, H), dtype=torch.uint8, device=dev)
+    if fmt not in FORMATS:
+        raise SgqError(f"unknown format {fmt!r}")
+    if scale_out is None:
+        scale_out = torch.empty(scale_shape(fmt, M, H), dtype=scale_dtype(fmt), device=dev)
+    if normed and normed_out is None:
+        normed_out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    flags = (F_GEMMA_WEIGHT if gemma else 0) | (F_QUANT_FROM_FP32 if quant_from_fp32 else 0)
+    st = library().rmsnorm_add_quant(FORMATS[fmt], flags, M, H, float(eps), _ptr(x),
+                                     _ptr(residual_in), _ptr(residual_out), _ptr(weight),
+                                     _ptr(q_out), _ptr(scale_out), _ptr(normed_out), _stream(stream))
+    _check(st, "rmsnorm_add_quant")
+    return q_out, scale_out, normed_out, residual_out
+
+
+def swiglu_quant(gate_up: torch.Tensor, *, fmt: str = "mxfp8", act: str = "swiglu_oai",
+                 quant_from_fp32: bool = True, round_act_bf16: bool = False, alpha: float = 1.702,
+                 beta: float = 1.0, limit: float = 7.0, q_out: torch.Tensor | None = None,
+                 scale_out: torch.Tensor | None = None, stream=None):
+    """SwiGLU + FP8 quantisation (one kernel launch).
+
+    gate_up [M, 2I] bf16 (gate = first half, up = second half). Returns
+    (q [M,I] uint8 E4M3, scale).
+    """
+    M, I2 = gate_up.shape
+    I = I2 // 2
+    _want(gate_up, (M, 2 * I), torch.bfloat16, "gate_up")
+    if I2 % 2:
+        raise SgqError("gate_up: width must be even")
+    if fmt not in FORMATS or act not in ACTS:
+        raise SgqError(f"unknown format/activation {fmt!r}/{act!r}")
+    dev = gate_up.device
+    if q_out is None:
+        q_out = torch.empty((M, I), dtype=torch.uint8, device=dev)
+    if scale_out is None:
+        scale_out = torch.empty(scale_shape(fmt, M, I), dtype=scale_dtype(fmt), device=dev)
+    flags = (F_QUANT_FROM_FP32 if quant_from_fp32 else 0) | (F_ACT_ROUND_BF16 if round_act_bf16 else 0)
+    st = library().swiglu_quant(FORMATS[fmt], ACTS[act], flags, M, I, float(alpha), float(beta),
+                                float(limit), _ptr(gate_up), _ptr(q_out), _ptr(scale_out), _stream(stream))
+    _check(st, "swiglu_quant")
+    return q_out, scale_out
