@@ -1,0 +1,565 @@
+"""Benchmark of the fused norm / SwiGLU + FP8 quantisation path on GB300.
+
+One step = the whole hot path once over the prefill-stress workload: residual
+add + Gemma RMSNorm + MXFP8 + bf16 copy at M=8192, H=6144, then OAI SwiGLU +
+MXFP8 at M=8192, I=3072 (inputs N(0,1) with 0.1% outliers x100 and 1% zero
+32-blocks). `value` is algorithmic HBM bytes per step / device time, in GB/s.
+
+Also reported: µs per launch at decode sizes (M = 8 .. 192, CUDA graph of 200
+back-to-back launches, median of 20 replays, the method of the MiniMax-M3.1
+MXFP8 fusion page's microbenchmark), the roofline of the dominant kernel, an
+end-to-end number through pinned host buffers, and the CPU oracle as a
+baseline. `--impl reference` times the CPU oracle on the same workload.
+
+Run: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused norm/swiglu+quant µs/launch (M=8-192); HBM GB/s vs peak at M=8192"
+M_PREFILL, H, I_PREFILL = 8192, 6144, 3072
+I_DECODE = 768
+DECODE_MS = (8, 16, 32, 64, 128, 192)
+ROTATE = 3
+WORKLOAD = ("prefill stress M=8192: add+Gemma-RMSNorm+MXFP8+bf16 copy+residual at H=6144, "
+            "then OAI-SwiGLU+MXFP8 (fp32 source) at I=3072; bf16 N(0,1), 0.1% outliers x100, 1% zero 32-blocks")
+
+
+def norm_bytes(M: int, Hd: int, residual=True, normed=True, fmt="mxfp8") -> int:
+    """Algorithmic HBM bytes of one norm launch (weight counted once)."""
+    per_row = 2 * Hd + Hd  # x read, E4M3 written
+    per_row += {"mxfp8": Hd // 32, "block128": 4 * (Hd // 128), "per_token": 4}[fmt]
+    if residual:
+        per_row += 4 * Hd   # residual read + updated residual written
+    if normed:
+        per_row += 2 * Hd
+    return M * per_row + 2 * Hd
+
+
+def swiglu_bytes(M: int, I: int, fmt="mxfp8") -> int:
+    per_row = 4 * I + I + {"mxfp8": I // 32, "block128": 4 * (I // 128), "per_token": 4}[fmt]
+    return M * per_row
+
+
+def step_bytes() -> int:
+    return norm_bytes(M_PREFILL, H) + swiglu_bytes(M_PREFILL, I_PREFILL)
+
+
+def _kernel_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "swiglu_fp8_activation_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def _measured_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(kernel)
+    if not entry or entry.get("source_sha") != _kernel_sha():
+        return None
+    return entry.get("bytes_per_launch")
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return 6800.0, "fallback"
+
+
+# --------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples SM clock, power and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+        self._t = None
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self._t.join(timeout=5)
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Max of a float over the ranks (identity for one rank)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------ GPU workload
+
+def _c_args(lib, dev_set, out, fmt=0):
+    """Raw C-ABI argument tuples of one norm and one SwiGLU launch."""
+    import ctypes as C
+
+    import torch
+
+    from swiglu_fp8_activation_gb300.binding import F_GEMMA_WEIGHT, F_QUANT_FROM_FP32
+    p = lambda t: C.c_void_p(t.data_ptr()) if t is not None else None
+    stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    x, r, w, gu = dev_set
+    norm = (fmt, F_GEMMA_WEIGHT, x.shape[0], x.shape[1], 1e-6, p(x), p(r), p(out["r_out"]), p(w), p(out["q"]),
+            p(out["s"]), p(out["n"]), stream)
+    swiglu = (fmt, 0, F_QUANT_FROM_FP32, gu.shape[0], gu.shape[1] // 2, 1.702, 1.0, 7.0, p(gu), p(out["q2"]),
+              p(out["s2"]), stream)
+    return norm, swiglu
+
+
+def _call(fn, args):
+    st = fn(*args)
+    if st != 0:
+        raise RuntimeError(f"launch failed with status {st}")
+
+
+class Prefill:
+    """Device-resident inputs (ROTATE sets) and outputs of the prefill step."""
+
+    def __init__(self, dev):
+        import torch
+
+        from swiglu_fp8_activation_gb300 import inputs, library
+        nc, sc = inputs.workloads()["cfg5_prefill"]
+        t = inputs.make_norm(nc)
+        gu = inputs.make_swiglu(sc)
+        self.host = {"x": t["x"], "r": t["r"], "w": t["w"], "gu": gu}
+        self.sets = []
+        for i in range(ROTATE):
+            self.sets.append(tuple(v.to(dev) for v in (t["x"], t["r"], t["w"], gu)))
+        M = nc.M
+        self.out = {"q": torch.empty(M, H, dtype=torch.uint8, device=dev),
+                    "s": torch.empty(M, H // 32, dtype=torch.uint8, device=dev),
+                    "n": torch.empty(M, H, dtype=torch.bfloat16, device=dev),
+                    "r_out": torch.empty(M, H, dtype=torch.bfloat16, device=dev),
+                    "q2": torch.empty(M, I_PREFILL, dtype=torch.uint8, device=dev),
+                    "s2": torch.empty(M, I_PREFILL // 32, dtype=torch.uint8, device=dev)}
+        self.lib = library()
+        self.args = [_c_args(self.lib, s, self.out) for s in self.sets]
+
+    def step(self, k, ev=None):
+        na, sa = self.args[k % ROTATE]
+        if ev is not None:
+            ev[0].record()
+        _call(self.lib.rmsnorm_add_quant, na)
+        if ev is not None:
+            ev[1].record()
+        _call(self.lib.swiglu_quant, sa)
+        if ev is not None:
+            ev[2].record()
+
+
+def time_prefill(pf, steps, warmup, world):
+    import torch
+    for k in range(warmup):
+        pf.step(k)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record()
+    for k in range(steps):
+        pf.step(k, evs[k])
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    total_ms = start.elapsed_time(end)
+    norm_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    swiglu_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    return total_ms, statistics.mean(norm_ms), statistics.mean(swiglu_ms)
+
+
+def graph_us_per_launch(fn, iters=200, reps=20):
+    """µs per launch: a CUDA graph of `iters` back-to-back launches, 3 warm
+    replays, median of `reps` timed replays."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(iters):
+            fn()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        g.replay()
+        e.record()
+        torch.cuda.synchronize()
+        ts.append(s.elapsed_time(e) * 1000.0 / iters)
+    return statistics.median(ts)
+
+
+def decode_table(dev):
+    """µs per launch at M = 8..192 for the two decode workloads (fused norm
+    +MXFP8+bf16 copy at H=6144; OAI SwiGLU+MXFP8 at I=768)."""
+    import torch
+
+    from swiglu_fp8_activation_gb300 import inputs, rmsnorm_add_quant, swiglu_quant
+    out = {"norm_mxfp8_bf16copy_H6144": {}, "swiglu_oai_mxfp8_I768": {}}
+    for M in DECODE_MS:
+        nc = inputs.norm_case_gemma_mx(M)
+        t = inputs.make_norm(nc)
+        x, r, w = (t[k].to(dev) for k in ("x", "r", "w"))
+        q = torch.empty(M, H, dtype=torch.uint8, device=dev)
+        s = torch.empty(M, H // 32, dtype=torch.uint8, device=dev)
+        n = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+        ro = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+        fn = lambda: rmsnorm_add_quant(x, w, residual_in=r, residual_out=ro, q_out=q, scale_out=s, normed_out=n)
+        out["norm_mxfp8_bf16copy_H6144"][str(M)] = round(graph_us_per_launch(fn), 3)
+        gu = inputs.make_swiglu(inputs.swiglu_case_oai_mx(M)).to(dev)
+        q2 = torch.empty(M, I_DECODE, dtype=torch.uint8, device=dev)
+        s2 = torch.empty(M, I_DECODE // 32, dtype=torch.uint8, device=dev)
+        fn2 = lambda: swiglu_quant(gu, q_out=q2, scale_out=s2)
+        out["swiglu_oai_mxfp8_I768"][str(M)] = round(graph_us_per_launch(fn2), 3)
+    return out
+
+
+def other_configs(dev):
+    """µs per launch (CUDA-graph replay, as above) of the Qwen3-like 1x128 and
+    MLA-like per-token workloads."""
+    import torch
+
+    from swiglu_fp8_activation_gb300 import inputs, rmsnorm_add_quant, swiglu_quant
+    res = {}
+    w = inputs.workloads()
+    for case in w["cfg3_block128"] + w["cfg4_per_token"]:
+        if isinstance(case, inputs.NormCase):
+            t = inputs.make_norm(case)
+            x, wt = t["x"].to(dev), t["w"].to(dev)
+            q = torch.empty(case.M, case.H, dtype=torch.uint8, device=dev)
+            shape = (case.M, 1) if case.fmt == "per_token" else (case.M, case.H // 128)
+            s = torch.empty(shape, dtype=torch.float32, device=dev)
+            fn = (lambda x=x, wt=wt, q=q, s=s, c=case: rmsnorm_add_quant(
+                x, wt, fmt=c.fmt, eps=c.eps, gemma=c.gemma, quant_from_fp32=c.from_fp32, q_out=q, scale_out=s))
+            key, nbytes = f"{case.name}_W{case.H}_M{case.M}", norm_bytes(case.M, case.H, False, False, case.fmt)
+        else:
+            gu = inputs.make_swiglu(case).to(dev)
+            q = torch.empty(case.M, case.I, dtype=torch.uint8, device=dev)
+            s = torch.empty(case.M, case.I // 128, dtype=torch.float32, device=dev)
+            fn = (lambda gu=gu, q=q, s=s, c=case: swiglu_quant(
+                gu, fmt=c.fmt, act=c.act, quant_from_fp32=c.from_fp32, round_act_bf16=c.round_act_bf16,
+                q_out=q, scale_out=s))
+            key, nbytes = f"{case.name}_I{case.I}_M{case.M}", swiglu_bytes(case.M, case.I, case.fmt)
+        us = graph_us_per_launch(fn, iters=100, reps=10)
+        res[key] = {"us": round(us, 3), "GBps": round(nbytes / us / 1e3, 1)}
+    return res
+
+
+def time_e2e(pf, dev, steps):
+    """The same step through the public API with host buffers: per step, H2D
+    copies of x, r, gate_up from pinned memory, the two launches, and D2H
+    copies of every output into pinned memory. Returns (ms/step, h2d, d2h)."""
+    import torch
+
+    from swiglu_fp8_activation_gb300 import rmsnorm_add_quant, swiglu_quant
+    hin = {k: pf.host[k].pin_memory() for k in ("x", "r", "gu")}
+    x, r, w, gu = pf.sets[0]
+    hout = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in pf.out.items()}
+    h2d = sum(v.numel() * v.element_size() for v in hin.values())
+    d2h = sum(v.numel() * v.element_size() for v in hout.values())
+
+    def one():
+        x.copy_(hin["x"], non_blocking=True)
+        r.copy_(hin["r"], non_blocking=True)
+        gu.copy_(hin["gu"], non_blocking=True)
+        o = pf.out
+        rmsnorm_add_quant(x, w, residual_in=r, residual_out=o["r_out"], q_out=o["q"], scale_out=o["s"],
+                          normed_out=o["n"])
+        swiglu_quant(gu, q_out=o["q2"], scale_out=o["s2"])
+        for k, v in o.items():
+            hout[k].copy_(v, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        one()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / steps, h2d, d2h
+
+
+def cpu_oracle_gbps(budget_s: float, rows_per_chunk: int = 8, host=None):
+    """The CPU oracle as it stands (single thread, no diagnostics) on prefill
+    rows, norm then SwiGLU in turns, until `budget_s` seconds have passed.
+    Returns (GB/s on the same algorithmic bytes, rows processed, seconds)."""
+    import oracle
+    from swiglu_fp8_activation_gb300 import inputs
+    if host is None:
+        nc, sc = inputs.workloads()["cfg5_prefill"]
+        t = inputs.make_norm(nc)
+        host = {"x": t["x"], "r": t["r"], "w": t["w"], "gu": inputs.make_swiglu(sc)}
+    xb, rb, wb = (inputs.bf16_bits(host[k]) for k in ("x", "r", "w"))
+    gub = inputs.bf16_bits(host["gu"])
+    done_rows, nbytes = 0, 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s and done_rows < M_PREFILL:
+        sl = slice(done_rows, done_rows + rows_per_chunk)
+        oracle.rmsnorm_add_quant("mxfp8", xb[sl], rb[sl], wb, eps=1e-6, gemma=True, from_fp32=False,
+                                 diagnostics=False)
+        oracle.swiglu_quant("mxfp8", "swiglu_oai", gub[sl], from_fp32=True, diagnostics=False)
+        n = xb[sl].shape[0]
+        nbytes += norm_bytes(n, H) - 2 * H + swiglu_bytes(n, I_PREFILL)
+        done_rows += n
+    dt = time.perf_counter() - t0
+    return nbytes / dt / 1e9, done_rows, dt
+
+
+# ---------------------------------------------------------------- arms
+
+def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm: each step runs the oracle on a
+    bounded sample of the same workload (16 rows of the norm, 16 of SwiGLU)."""
+    if rank != 0:
+        return
+    import oracle
+    from swiglu_fp8_activation_gb300 import inputs
+    oracle.lib()
+    nc, sc = inputs.workloads()["cfg5_prefill"]
+    t = inputs.make_norm(nc)
+    host = {"x": t["x"], "r": t["r"], "w": t["w"], "gu": inputs.make_swiglu(sc)}
+    rows = 16
+    xb, rb, wb = (inputs.bf16_bits(host[k]) for k in ("x", "r", "w"))
+    gub = inputs.bf16_bits(host["gu"])
+
+    def step(k):
+        sl = slice((k * rows) % M_PREFILL, (k * rows) % M_PREFILL + rows)
+        oracle.rmsnorm_add_quant("mxfp8", xb[sl], rb[sl], wb, eps=1e-6, gemma=True, from_fp32=False,
+                                 diagnostics=False)
+        oracle.swiglu_quant("mxfp8", "swiglu_oai", gub[sl], from_fp32=True, diagnostics=False)
+
+    for k in range(args.warmup):
+        step(k)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        step(args.warmup + k)
+    dt = time.perf_counter() - t0
+    nbytes = args.steps * (norm_bytes(rows, H) + swiglu_bytes(rows, I_PREFILL))
+    gbps = nbytes / dt / 1e9
+    sample = f"{rows} norm rows + {rows} SwiGLU rows of the M=8192 workload per step"
+    line = {"impl": "reference", "metric": METRIC, "value": round(gbps, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample_rows_per_step": rows},
+            "cpu_baseline": {"value": round(gbps, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(gbps, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def _gpu_id():
+    """nvidia-smi's id of the current CUDA device (its UUID), if nvidia-smi knows it."""
+    try:
+        import torch
+        u = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        gid = u if u.startswith("GPU-") else f"GPU-{u}"
+        r = subprocess.run(["nvidia-smi", "-i", gid, "--query-gpu=index", "--format=csv,noheader"],
+                           capture_output=True, text=True, timeout=30)
+        return gid if r.returncode == 0 else None
+    except Exception:
+        return None
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    import oracle
+    oracle.lib()   # build the CPU oracle before any timing
+    pf = Prefill(dev)
+    peak, peak_kind = _peaks()
+    with ClockSampler(_gpu_id()) as clocks:
+        total_ms, norm_ms, swiglu_ms = time_prefill(pf, args.steps, args.warmup, world)
+        decode = decode_table(dev) if rank == 0 and not args.quick else None
+        others = other_configs(dev) if rank == 0 and not args.quick else None
+    total_ms = max_over_ranks(total_ms, world)
+    e2e_ms, h2d, d2h = time_e2e(pf, dev, args.e2e_steps)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    if rank != 0:
+        barrier(world)
+        return
+    sb = step_bytes()
+    ms_step = total_ms / args.steps
+    value = world * sb / (ms_step * 1e-3) / 1e9
+    nb = norm_bytes(M_PREFILL, H)
+    norm_gbs = nb / (norm_ms * 1e-3) / 1e9
+    swiglu_gbs = swiglu_bytes(M_PREFILL, I_PREFILL) / (swiglu_ms * 1e-3) / 1e9
+    cpu_gbs, cpu_rows, cpu_s = cpu_oracle_gbps(args.cpu_budget, host=pf.host)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M_PREFILL, "H": H, "I": I_PREFILL, "format": "mxfp8",
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": f"inputs larger than L2, rotated over {ROTATE} buffer sets",
+                   "bytes_per_step": sb},
+        "roofline": {"bound": "hbm", "kernel": "norm_quant_kernel (add+Gemma RMSNorm+MXFP8+bf16 copy)",
+                     "achieved": round(norm_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(norm_gbs / peak, 4), "peak_kind": peak_kind,
+                     "traffic": _measured_traffic("norm_mxfp8_H6144_M8192"), "algorithmic_bytes": nb},
+        "kernels": {"norm_us": round(norm_ms * 1e3, 2), "norm_GBps": round(norm_gbs, 1),
+                    "swiglu_us": round(swiglu_ms * 1e3, 2), "swiglu_GBps": round(swiglu_gbs, 1),
+                    "swiglu_frac": round(swiglu_gbs / peak, 4)},
+        "decode_us_per_launch": decode,
+        "other_configs": others,
+        "e2e": {"value": round(sb / (e2e_ms * 1e-3) / 1e9 * world, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 3),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "cpu_baseline": {"value": round(cpu_gbs, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{cpu_rows} rows of each op of the M=8192 workload in {cpu_s:.1f} s"},
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    barrier(world)
+
+
+def run_profile(args):
+    """Only one kernel of the prefill step (for ncu): `--warmup` untimed then
+    `--steps` timed launches on the M=8192 workload (inputs > L2, rotated)."""
+    import torch
+    dev = torch.device("cuda", 0)
+    pf = Prefill(dev)
+    fn = pf.lib.rmsnorm_add_quant if args.profile == "norm" else pf.lib.swiglu_quant
+    pick = 0 if args.profile == "norm" else 1
+    for k in range(args.warmup):
+        _call(fn, pf.args[k % ROTATE][pick])
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for k in range(args.steps):
+        _call(fn, pf.args[k % ROTATE][pick])
+    e.record()
+    torch.cuda.synchronize()
+    us = s.elapsed_time(e) * 1e3 / args.steps
+    nbytes = norm_bytes(M_PREFILL, H) if args.profile == "norm" else swiglu_bytes(M_PREFILL, I_PREFILL)
+    print(json.dumps({"profile": args.profile, "us_per_launch": round(us, 2),
+                      "GBps": round(nbytes / us / 1e3, 1), "launches": args.warmup + args.steps}), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle time")
+    ap.add_argument("--quick", action="store_true", help="skip the decode and other-config tables")
+    ap.add_argument("--profile", choices=("norm", "swiglu"), help="time one kernel only (for ncu)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    world, rank, local = dist_env()
+    if args.profile:
+        run_profile(args)
+        return
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -40,7 +40,8 @@
  *     a rejected call leaves every buffer untouched. SGQ_ERR_LAUNCH reports a
  *     failed launch (cudaGetLastError after the launch).
  *   - Non-finite inputs (inf, NaN) are outside the contract: the kernels do
- *     not fault on them, but their outputs are unspecified.
+ *     not fault on them, but their outputs are unspecified. So are norm rows
+ *     whose sum of squares overflows fp32 (|h| of order 1e19 / sqrt(H)).
  */
 #ifndef SGQ_H
 #define SGQ_H

@@ -20,7 +20,7 @@ from .build import build_oracle
 FORMATS = {"mxfp8": 0, "block128": 1, "per_token": 2}
 ACTS = {"swiglu_oai": 0, "silu_mul": 1}
 F_GEMMA, F_FROM_FP32, F_ACT_ROUND_BF16 = 1, 2, 4
-AMB_SRC, AMB_CODE = 1, 2
+AMB_SRC, AMB_CODE, AMB_TIE = 1, 2, 4
 REL_WINDOW = 2.0 ** -20
 
 _lib = None

@@ -1,0 +1,149 @@
+"""Element-by-element comparison of a CUDA result with the CPU oracle.
+
+TEST INFRASTRUCTURE ONLY (used by the tests and the smoke check).
+
+Tolerances:
+  * bf16 outputs (updated residual, normed copy): within 1 bf16 ulp.
+  * scales: exact, except in groups the oracle excuses (`gamb`): the group's
+    decisive amax lies within 2^-20 relative of a power of two (E8M0) or of a
+    bf16 rounding boundary (bf16 source). An fp32 scale of a source quantised
+    from fp32 carries the fp32 rounding of amax itself, so there it must lie
+    within 2^-20 relative of the oracle's scale.
+  * E4M3 codes, compared as sign-magnitude integers (so +0 and -0 agree): at
+    most 1 step apart, on at most 1e-4 of the elements of non-excused groups.
+    In excused groups the dequantised values agree within one E4M3 step.
+    Elements the oracle marks as ties (fp32-source FP8 formats: y/s within
+    2^-22 of an E4M3 midpoint, where either neighbour is a correct rounding)
+    must be within one step but do not count toward the 1e-4.
+The check also counts mismatches at elements the oracle did not flag as near
+a rounding boundary (`unflagged`), a stricter signal reported in the stats.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import AMB_CODE, AMB_TIE
+
+MAX_CODE_MISMATCH_FRACTION = 1e-4
+FP32_SCALE_REL = 2.0 ** -20
+
+_E4M3 = None
+
+
+def _e4m3_table() -> np.ndarray:
+    global _E4M3
+    if _E4M3 is None:
+        from . import e4m3_decode
+        _E4M3 = np.array([e4m3_decode(c) for c in range(256)])
+    return _E4M3
+
+
+def _bf16_key(bits: np.ndarray) -> np.ndarray:
+    """Monotone integer key of bf16 bit patterns (adjacent values differ by 1)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    mag = b & 0x7FFF
+    return np.where(b & 0x8000, -mag, mag)
+
+
+def _code_key(q: np.ndarray) -> np.ndarray:
+    q = np.asarray(q, dtype=np.uint8).astype(np.int64)
+    mag = q & 0x7F
+    return np.where(q & 0x80, -mag, mag)
+
+
+def check_bf16(name: str, want: np.ndarray, got: np.ndarray) -> dict:
+    d = np.abs(_bf16_key(want) - _bf16_key(got))
+    assert want.shape == got.shape, (name, want.shape, got.shape)
+    assert d.max(initial=0) <= 1, f"{name}: bf16 differs by {d.max()} ulp at {np.argwhere(d > 1)[:5].tolist()}"
+    return {f"{name}_exact_frac": float((d == 0).mean()) if d.size else 1.0}
+
+
+def _group_size(fmt: str, width: int) -> int:
+    return {"mxfp8": 32, "block128": 128, "per_token": width}[fmt]
+
+
+def _dequant(fmt: str, q: np.ndarray, scale: np.ndarray, gs: int) -> np.ndarray:
+    vals = _e4m3_table()[q]
+    if fmt == "mxfp8":
+        s = 2.0 ** (scale.astype(np.int64) - 127)
+    else:
+        s = scale.astype(np.float64)
+    return vals * np.repeat(s, gs, axis=1)
+
+
+def check_quant(fmt: str, ref: dict, q: np.ndarray, scale: np.ndarray, from_fp32: bool) -> dict:
+    """Compare codes and scales with the oracle result `ref` (same rows)."""
+    q = np.asarray(q)
+    scale = np.asarray(scale)
+    M, W = ref["q"].shape
+    assert q.shape == (M, W), (q.shape, (M, W))
+    gs = _group_size(fmt, W)
+    ng = W // gs
+    rs = ref["scale"].reshape(M, ng)
+    scale = scale.reshape(M, ng)
+    gamb = ref["gamb"].reshape(M, ng).astype(bool)
+    stats = {}
+    # scales
+    if fmt == "mxfp8":
+        diff = rs.astype(np.int64) != scale.astype(np.int64)
+        bad = diff & ~gamb
+        assert not bad.any(), f"E8M0 scale mismatch in non-excused groups at {np.argwhere(bad)[:5].tolist()}"
+        assert (np.abs(rs.astype(np.int64) - scale.astype(np.int64)) <= 1).all(), "E8M0 scale off by more than 1"
+        stats["scale_excused_diff"] = int(diff.sum())
+    else:
+        assert scale.dtype == np.float32
+        rsd, sd = rs.astype(np.float64), scale.astype(np.float64)
+        rel = np.abs(sd - rsd) / np.where(rsd == 0, 1.0, rsd)
+        zero_ok = (rsd == 0) == (sd == 0)
+        assert zero_ok.all(), "zero scale mismatch"
+        if from_fp32:
+            assert rel.max(initial=0) <= FP32_SCALE_REL, f"fp32 scale rel diff {rel.max()} > 2^-20"
+            stats["scale_max_rel"] = float(rel.max(initial=0))
+        else:
+            bad = (sd != rsd) & ~gamb
+            assert not bad.any(), f"fp32 scale mismatch in non-excused groups at {np.argwhere(bad)[:5].tolist()}"
+            assert rel.max(initial=0) <= 2.0 ** -7, "fp32 scale off by more than a bf16 ulp of amax"
+            stats["scale_excused_diff"] = int((sd != rsd).sum())
+    # codes
+    step = np.abs(_code_key(ref["q"]) - _code_key(q))
+    excused = np.repeat(gamb, gs, axis=1) | np.repeat((rs != scale) if fmt == "mxfp8" else np.zeros_like(gamb), gs, axis=1)
+    if fmt != "mxfp8" and from_fp32:
+        excused = np.zeros_like(excused)   # all fp32-source FP8 groups: compare codes directly
+    plain = ~excused
+    n_plain = int(plain.sum())
+    tie = (ref["amb"] & AMB_TIE) != 0
+    assert step[plain].max(initial=0) <= 1, f"E4M3 code off by {step[plain].max()} steps"
+    mism = (step != 0) & plain & ~tie
+    frac = float(mism.sum()) / max(n_plain, 1)
+    stats["tie_mismatch"] = int(((step != 0) & plain & tie).sum())
+    assert frac <= MAX_CODE_MISMATCH_FRACTION, f"E4M3 mismatch fraction {frac:.2e} > 1e-4"
+    if excused.any():
+        dq_ref = _dequant(fmt, ref["q"], rs, gs)
+        dq = _dequant(fmt, q, scale, gs)
+        s_big = np.maximum(np.repeat(_scale_values(fmt, rs), gs, axis=1), np.repeat(_scale_values(fmt, scale), gs, axis=1))
+        tol = 2.0 ** -3 * np.maximum(np.abs(dq_ref), np.abs(dq)) + 2.0 ** -9 * s_big
+        e = np.abs(dq_ref - dq)
+        assert (e[excused] <= tol[excused] * (1 + 1e-9)).all(), "excused group dequantised values differ by more than one step"
+    flagged = (ref["amb"] & AMB_CODE) != 0
+    stats.update(code_mismatch=int(mism.sum()), code_mismatch_frac=frac,
+                 unflagged=int((mism & ~flagged).sum()), excused_elems=int(excused.sum()))
+    return stats
+
+
+def _scale_values(fmt: str, s: np.ndarray) -> np.ndarray:
+    if fmt == "mxfp8":
+        return 2.0 ** (s.astype(np.int64) - 127)
+    return s.astype(np.float64)
+
+
+def check_norm(fmt: str, ref: dict, q, scale, normed_bits=None, residual_bits=None, *, from_fp32: bool) -> dict:
+    stats = check_quant(fmt, ref, q, scale, from_fp32)
+    if residual_bits is not None:
+        stats.update(check_bf16("residual", ref["residual"], np.asarray(residual_bits)))
+    if normed_bits is not None:
+        stats.update(check_bf16("normed", ref["normed"], np.asarray(normed_bits)))
+    return stats
+
+
+def check_swiglu(fmt: str, ref: dict, q, scale, *, from_fp32: bool) -> dict:
+    return check_quant(fmt, ref, q, scale, from_fp32)

@@ -42,8 +42,14 @@ enum { ORA_MXFP8 = 0, ORA_BLOCK128 = 1, ORA_PER_TOKEN = 2 };
 enum { ORA_SWIGLU_OAI = 0, ORA_SILU_MUL = 1 };
 enum { ORA_F_GEMMA = 1u << 0, ORA_F_FROM_FP32 = 1u << 1, ORA_F_ACT_ROUND_BF16 = 1u << 2 };
 
-/* Per-element ambiguity flags written to `amb`. */
-enum { ORA_AMB_SRC = 1, ORA_AMB_CODE = 2 };
+/* Per-element ambiguity flags written to `amb`. ORA_AMB_TIE marks an
+ * element of an FP8 group quantised from fp32 whose argument y/s lies within
+ * 2^-22 of an E4M3 midpoint. There the normalisation factor cancels from
+ * y/s = 448 * (h_j*w_j) / (h_k*w_k) (k the amax element), a ratio of short
+ * bf16 products that often equals a midpoint exactly; only the fp32 rounding
+ * of the stored scale then picks a side, so either neighbour is a correct
+ * rounding of y * 448 / amax. */
+enum { ORA_AMB_SRC = 1, ORA_AMB_CODE = 2, ORA_AMB_TIE = 4 };
 
 /* ------------------------------------------------------------------ bf16 */
 
@@ -103,6 +109,13 @@ double ora_e4m3_decode(uint8_t c) {
     return s ? -mag : mag;
 }
 
+/* The 127 finite non-negative E4M3 values, decoded once when the library loads. */
+static double e4m3_value[0x7F];
+
+__attribute__((constructor)) static void init_e4m3_values(void) {
+    for (int c = 0; c <= 0x7E; ++c) e4m3_value[c] = ora_e4m3_decode((uint8_t)c);
+}
+
 /* Round to nearest E4M3 by searching all 127 finite non-negative codes; a tie
  * goes to the code with an even mantissa; magnitudes past 448 take 448 (the
  * nearest finite code), i.e. saturating rounding. The sign is copied. */
@@ -112,7 +125,7 @@ uint8_t ora_e4m3_encode(double v) {
     int best = 0;
     double best_d = INFINITY;
     for (int c = 0; c <= 0x7E; ++c) {
-        double d = fabs(ora_e4m3_decode((uint8_t)c) - a);
+        double d = fabs(e4m3_value[c] - a);
         if (d < best_d || (d == best_d && (c & 1) == 0)) {
             best = c;
             best_d = d;
@@ -128,7 +141,7 @@ uint8_t ora_e4m3_encode(double v) {
 static int near_e4m3_boundary(double t, double rel) {
     double a = fabs(t);
     for (int c = 0; c < 0x7E; ++c) {
-        double mid = 0.5 * (ora_e4m3_decode((uint8_t)c) + ora_e4m3_decode((uint8_t)(c + 1)));
+        double mid = 0.5 * (e4m3_value[c] + e4m3_value[c + 1]);
         if (fabs(a - mid) <= rel * a) return 1;
     }
     return 0;
@@ -210,6 +223,7 @@ static void quant_group(int fmt, int from_fp32, const double* src, const double*
             double tj = (s == 0.0f) ? 0.0 : (double)(float)(src[j] / (double)s);
             q[j] = ora_e4m3_encode(tj);
             element_flags(tj, src_amb[j], t ? t + j : 0, amb ? amb + j : 0, rel);
+            if (amb && from_fp32 && near_e4m3_boundary(tj, ldexp(1.0, -22))) amb[j] |= ORA_AMB_TIE;
         }
     }
     if (gamb) *gamb = (unsigned char)g_amb;

@@ -123,6 +123,10 @@ def rmsnorm_add_quant(x: torch.Tensor, weight: torch.Tensor, *, fmt: str = "mxfp
         scale_out = torch.empty(scale_shape(fmt, M, H), dtype=scale_dtype(fmt), device=dev)
     if normed and normed_out is None:
         normed_out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    _want(q_out, (M, H), torch.uint8, "q_out")
+    _want(scale_out, scale_shape(fmt, M, H), scale_dtype(fmt), "scale_out")
+    if normed_out is not None:
+        _want(normed_out, (M, H), torch.bfloat16, "normed_out")
     flags = (F_GEMMA_WEIGHT if gemma else 0) | (F_QUANT_FROM_FP32 if quant_from_fp32 else 0)
     st = library().rmsnorm_add_quant(FORMATS[fmt], flags, M, H, float(eps), _ptr(x),
                                      _ptr(residual_in), _ptr(residual_out), _ptr(weight),
@@ -152,6 +156,8 @@ def swiglu_quant(gate_up: torch.Tensor, *, fmt: str = "mxfp8", act: str = "swigl
         q_out = torch.empty((M, I), dtype=torch.uint8, device=dev)
     if scale_out is None:
         scale_out = torch.empty(scale_shape(fmt, M, I), dtype=scale_dtype(fmt), device=dev)
+    _want(q_out, (M, I), torch.uint8, "q_out")
+    _want(scale_out, scale_shape(fmt, M, I), scale_dtype(fmt), "scale_out")
     flags = (F_QUANT_FROM_FP32 if quant_from_fp32 else 0) | (F_ACT_ROUND_BF16 if round_act_bf16 else 0)
     st = library().swiglu_quant(FORMATS[fmt], ACTS[act], flags, M, I, float(alpha), float(beta),
                                 float(limit), _ptr(gate_up), _ptr(q_out), _ptr(scale_out), _stream(stream))

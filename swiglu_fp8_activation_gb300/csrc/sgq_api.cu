@@ -1,0 +1,183 @@
+// sgq_api.cu -- the C ABI declared in include/sgq.h: host-side argument
+// checks, launch planning and one kernel launch per call. Nothing here
+// allocates, synchronises or keeps state between calls.
+#include <math.h>
+#include <stdint.h>
+
+#include <cuda_runtime.h>
+
+#include "sgq.h"
+#include "sgq_launch.h"
+
+namespace sgq {
+
+// Rows of width W: `nv` chunks per thread and `tpr` threads per row, preferring
+// an exact fit (W/8 = tpr * nv with tpr a multiple of 32) and the most chunks
+// per thread; otherwise the fewest threads that cover the row. Small M takes
+// fewer rows per CTA so that the grid spreads over the SMs.
+bool plan_rows(int64_t M, int W, int sm_count, Plan* p) {
+    const int nchunks = W / 8;
+    int nv = 0, tpr = 0;
+    for (int cand = kMaxNV; cand >= 1; --cand) {
+        if (nchunks % (32 * cand) == 0 && nchunks / cand <= kMaxTPR) {
+            nv = cand;
+            tpr = nchunks / cand;
+            break;
+        }
+    }
+    if (nv == 0) {
+        nv = (nchunks + 31) / 32 < kMaxNV ? (nchunks + 31) / 32 : kMaxNV;
+        tpr = ((nchunks + nv - 1) / nv + 31) / 32 * 32;
+    }
+    if (tpr > kMaxTPR) return false;
+    int rpc = kTargetCTA / tpr > 1 ? kTargetCTA / tpr : 1;
+    const int64_t per_sm = sm_count > 0 ? (M + sm_count - 1) / sm_count : M;
+    if (per_sm < rpc) rpc = per_sm > 1 ? (int)per_sm : 1;
+    p->nv = nv;
+    p->tpr = tpr;
+    p->rpc = rpc;
+    p->grid = (M + rpc - 1) / rpc;
+    return p->grid <= 0x7FFFFFFF;
+}
+
+}  // namespace sgq
+
+namespace {
+
+// Largest element count of one tensor: its byte sizes (at most 4 bytes an
+// element) stay far inside size_t and the kernels' 64-bit offsets.
+constexpr int64_t kMaxElements = int64_t(1) << 56;
+
+bool aligned(const void* p, uintptr_t a) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Half-open byte ranges [a, a+na) and [b, b+nb) intersect (null or empty never does).
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+int group_of(int fmt) { return fmt == SGQ_FMT_MXFP8 ? 32 : fmt == SGQ_FMT_FP8_BLOCK128 ? 128 : 8; }
+
+size_t scale_bytes(int fmt, int64_t M, int64_t W) {
+    if (fmt == SGQ_FMT_MXFP8) return (size_t)(M * (W / 32));
+    if (fmt == SGQ_FMT_FP8_BLOCK128) return (size_t)(M * (W / 128)) * 4;
+    return (size_t)M * 4;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+struct Span {
+    const void* p;
+    size_t n;
+};
+
+// True when any two of the spans intersect.
+bool any_overlap(const Span* s, int k) {
+    for (int i = 0; i < k; ++i)
+        for (int j = i + 1; j < k; ++j)
+            if (overlap(s[i].p, s[i].n, s[j].p, s[j].n)) return true;
+    return false;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sgq_abi_version(void) { return SGQ_ABI_VERSION; }
+
+const char* sgq_status_string(int status) {
+    switch (status) {
+        case SGQ_OK: return "ok";
+        case SGQ_ERR_INVALID_ARG: return "invalid argument";
+        case SGQ_ERR_UNSUPPORTED: return "unsupported width";
+        case SGQ_ERR_MISALIGNED: return "misaligned pointer";
+        case SGQ_ERR_LAUNCH: return "kernel launch failed";
+        default: return "unknown status";
+    }
+}
+
+int rmsnorm_add_quant(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, const void* x,
+                      const void* residual_in, void* residual_out, const void* weight, void* q_out,
+                      void* scale_out, void* normed_out, sgq_stream_t stream) {
+    if (fmt < SGQ_FMT_MXFP8 || fmt > SGQ_FMT_FP8_PER_TOKEN) return SGQ_ERR_INVALID_ARG;
+    if (flags & ~(SGQ_F_GEMMA_WEIGHT | SGQ_F_QUANT_FROM_FP32)) return SGQ_ERR_INVALID_ARG;
+    if (M < 0 || H <= 0 || !(eps >= 0.0f) || isinf(eps)) return SGQ_ERR_INVALID_ARG;
+    if (H % group_of(fmt) != 0 || H > SGQ_MAX_WIDTH) return SGQ_ERR_UNSUPPORTED;
+    if (M > kMaxElements / H) return SGQ_ERR_INVALID_ARG;
+    if (M == 0) return SGQ_OK;
+    if (!x || !weight || !q_out || !scale_out) return SGQ_ERR_INVALID_ARG;
+    if (residual_out && !residual_in) return SGQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(residual_in, 16) || !aligned(residual_out, 16) || !aligned(weight, 16) ||
+        !aligned(q_out, 16) || !aligned(normed_out, 16) || !aligned(scale_out, fmt == SGQ_FMT_MXFP8 ? 1 : 4))
+        return SGQ_ERR_MISALIGNED;
+    const size_t act = (size_t)M * (size_t)H * 2;
+    // residual_out == residual_in is the one overlap allowed (in-place update)
+    const void* r_out_span = residual_out == residual_in ? nullptr : residual_out;
+    const Span spans[] = {{x, act},      {residual_in, act}, {weight, (size_t)H * 2}, {q_out, (size_t)M * H},
+                          {scale_out, scale_bytes(fmt, M, H)}, {normed_out, act}, {r_out_span, act}};
+    if (any_overlap(spans, 7)) return SGQ_ERR_INVALID_ARG;
+
+    sgq::Plan plan;
+    if (!sgq::plan_rows(M, (int)H, sm_count(), &plan)) return SGQ_ERR_UNSUPPORTED;
+    sgq::NormArgs a;
+    a.x = static_cast<const uint16_t*>(x);
+    a.r_in = static_cast<const uint16_t*>(residual_in);
+    a.r_out = static_cast<uint16_t*>(residual_out);
+    a.w = static_cast<const uint16_t*>(weight);
+    a.q = static_cast<uint8_t*>(q_out);
+    a.scale = scale_out;
+    a.normed = static_cast<uint16_t*>(normed_out);
+    a.M = M;
+    a.H = (int)H;
+    a.tpr = plan.tpr;
+    a.rpc = plan.rpc;
+    a.eps = eps;
+    a.flags = flags;
+    if (sgq::launch_norm(fmt, plan, a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return SGQ_ERR_LAUNCH;
+    return SGQ_OK;
+}
+
+int swiglu_quant(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float alpha, float beta,
+                 float limit, const void* gate_up, void* q_out, void* scale_out, sgq_stream_t stream) {
+    if (fmt < SGQ_FMT_MXFP8 || fmt > SGQ_FMT_FP8_PER_TOKEN) return SGQ_ERR_INVALID_ARG;
+    if (act != SGQ_ACT_SWIGLU_OAI && act != SGQ_ACT_SILU_MUL) return SGQ_ERR_INVALID_ARG;
+    if (flags & ~(SGQ_F_QUANT_FROM_FP32 | SGQ_F_ACT_ROUND_BF16)) return SGQ_ERR_INVALID_ARG;
+    if ((flags & SGQ_F_ACT_ROUND_BF16) && act != SGQ_ACT_SILU_MUL) return SGQ_ERR_INVALID_ARG;
+    if (M < 0 || I <= 0) return SGQ_ERR_INVALID_ARG;
+    if (act == SGQ_ACT_SWIGLU_OAI && (!isfinite(alpha) || !isfinite(beta) || !(limit > 0.0f)))
+        return SGQ_ERR_INVALID_ARG;
+    if (I % group_of(fmt) != 0 || I > SGQ_MAX_WIDTH) return SGQ_ERR_UNSUPPORTED;
+    if (M > kMaxElements / (2 * I)) return SGQ_ERR_INVALID_ARG;
+    if (M == 0) return SGQ_OK;
+    if (!gate_up || !q_out || !scale_out) return SGQ_ERR_INVALID_ARG;
+    if (!aligned(gate_up, 16) || !aligned(q_out, 16) || !aligned(scale_out, fmt == SGQ_FMT_MXFP8 ? 1 : 4))
+        return SGQ_ERR_MISALIGNED;
+    const Span spans[] = {{gate_up, (size_t)M * I * 4}, {q_out, (size_t)M * I}, {scale_out, scale_bytes(fmt, M, I)}};
+    if (any_overlap(spans, 3)) return SGQ_ERR_INVALID_ARG;
+
+    sgq::Plan plan;
+    if (!sgq::plan_rows(M, (int)I, sm_count(), &plan)) return SGQ_ERR_UNSUPPORTED;
+    sgq::SwigluArgs a;
+    a.gu = static_cast<const uint16_t*>(gate_up);
+    a.q = static_cast<uint8_t*>(q_out);
+    a.scale = scale_out;
+    a.M = M;
+    a.I = (int)I;
+    a.tpr = plan.tpr;
+    a.rpc = plan.rpc;
+    a.flags = flags;
+    a.act = act;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.limit = limit;
+    if (sgq::launch_swiglu(fmt, plan, a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return SGQ_ERR_LAUNCH;
+    return SGQ_OK;
+}
+
+}  // extern "C"

@@ -29,3 +29,19 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def sgq_lib():
+    """The CUDA library, built in-tree if it is missing or older than its sources."""
+    import glob
+
+    import __graft_entry__ as g
+    from swiglu_fp8_activation_gb300 import binding
+
+    lib = os.path.join(g.PKG, "libsgq.so")
+    srcs = glob.glob(os.path.join(g.CSRC, "*")) + glob.glob(os.path.join(ROOT, "include", "*.h"))
+    if not os.path.exists(lib) or os.path.getmtime(lib) < max(os.path.getmtime(s) for s in srcs):
+        g.build_cuda()
+        binding._lib = None
+    return binding.library()

@@ -1,0 +1,132 @@
+"""The C ABI of libsgq.so (include/sgq.h), checked without a GPU: the library
+loads, exports every declared function, agrees with the Python binding and
+the oracle on enum and flag values, and rejects bad arguments on the host
+with the documented status before anything is launched (fake, never
+dereferenced pointers)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import oracle
+from swiglu_fp8_activation_gb300 import binding
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "sgq.h")
+OK, INVALID, UNSUPPORTED, MISALIGNED = 0, 1, 2, 3
+BASE = 1 << 40          # fake device addresses: aligned, far apart, never touched
+MB = 1 << 20
+
+
+def _header():
+    with open(HEADER) as f:
+        return f.read()
+
+
+def _declared_functions():
+    return re.findall(r"^(?:int|const char\*)\s+(\w+)\(", _header(), flags=re.M)
+
+
+def _header_value(name):
+    m = re.search(rf"\b{name}\s*=\s*(\d+)", _header()) or re.search(rf"#define\s+{name}\s+\(1u << (\d+)\)", _header())
+    assert m, name
+    v = int(m.group(1))
+    return (1 << v) if "<<" in m.group(0) else v
+
+
+def test_library_exports_every_declared_function(sgq_lib):
+    names = _declared_functions()
+    assert set(names) == {"rmsnorm_add_quant", "swiglu_quant", "sgq_status_string", "sgq_abi_version"}
+    for n in names:
+        assert hasattr(sgq_lib, n), n
+    m = re.search(r"#define SGQ_ABI_VERSION (\d+)", _header())
+    assert sgq_lib.sgq_abi_version() == int(m.group(1))
+
+
+def test_enum_and_flag_values_agree():
+    for name, key in (("SGQ_FMT_MXFP8", "mxfp8"), ("SGQ_FMT_FP8_BLOCK128", "block128"),
+                      ("SGQ_FMT_FP8_PER_TOKEN", "per_token")):
+        assert _header_value(name) == binding.FORMATS[key] == oracle.FORMATS[key]
+    for name, key in (("SGQ_ACT_SWIGLU_OAI", "swiglu_oai"), ("SGQ_ACT_SILU_MUL", "silu_mul")):
+        assert _header_value(name) == binding.ACTS[key] == oracle.ACTS[key]
+    assert _header_value("SGQ_F_GEMMA_WEIGHT") == binding.F_GEMMA_WEIGHT == oracle.F_GEMMA
+    assert _header_value("SGQ_F_QUANT_FROM_FP32") == binding.F_QUANT_FROM_FP32 == oracle.F_FROM_FP32
+    assert _header_value("SGQ_F_ACT_ROUND_BF16") == binding.F_ACT_ROUND_BF16 == oracle.F_ACT_ROUND_BF16
+
+
+def test_status_strings(sgq_lib):
+    for s, word in ((0, "ok"), (1, "invalid"), (2, "unsupported"), (3, "misaligned"), (4, "launch"), (99, "unknown")):
+        assert word in sgq_lib.sgq_status_string(s).decode()
+
+
+def _p(i):
+    return C.c_void_p(BASE + i * 64 * MB)
+
+
+def norm(lib, fmt=0, flags=1, M=8, H=256, eps=1e-6, x=_p(0), r=_p(1), ro=_p(2), w=_p(3), q=_p(4), s=_p(5),
+         n=_p(6)):
+    return lib.rmsnorm_add_quant(fmt, flags, M, H, eps, x, r, ro, w, q, s, n, None)
+
+
+def swiglu(lib, fmt=0, act=0, flags=2, M=8, I=256, alpha=1.702, beta=1.0, limit=7.0, gu=_p(0), q=_p(1), s=_p(2)):
+    return lib.swiglu_quant(fmt, act, flags, M, I, alpha, beta, limit, gu, q, s, None)
+
+
+def test_norm_argument_errors(sgq_lib):
+    L = sgq_lib
+    assert norm(L, M=0) == OK                         # empty: no launch
+    assert norm(L, M=0, x=None, q=None) == OK
+    assert norm(L, fmt=3) == INVALID
+    assert norm(L, fmt=-1) == INVALID
+    assert norm(L, flags=1 | 4) == INVALID            # ACT_ROUND_BF16 is not a norm flag
+    assert norm(L, flags=1 << 7) == INVALID
+    assert norm(L, M=-1) == INVALID
+    assert norm(L, H=0) == INVALID
+    assert norm(L, eps=-1e-6) == INVALID
+    assert norm(L, eps=float("nan")) == INVALID
+    assert norm(L, eps=float("inf")) == INVALID
+    assert norm(L, H=48) == UNSUPPORTED               # MX needs H % 32 == 0
+    assert norm(L, fmt=1, H=96) == UNSUPPORTED        # 1x128 needs H % 128 == 0
+    assert norm(L, fmt=2, H=20) == UNSUPPORTED        # per-token needs H % 8 == 0
+    assert norm(L, H=32768 + 32) == UNSUPPORTED       # above SGQ_MAX_WIDTH
+    for kw in ("x", "w", "q", "s"):
+        assert norm(L, **{kw: None}) == INVALID, kw
+    assert norm(L, r=None) == INVALID                 # residual_out without residual_in
+    assert norm(L, x=C.c_void_p(BASE + 8)) == MISALIGNED
+    assert norm(L, q=C.c_void_p(BASE + 4 * 64 * MB + 8)) == MISALIGNED
+    assert norm(L, fmt=1, s=C.c_void_p(BASE + 5 * 64 * MB + 2)) == MISALIGNED
+    assert norm(L, n=C.c_void_p(BASE + 6 * 64 * MB + 1)) == MISALIGNED
+    assert norm(L, q=_p(0)) == INVALID                # q_out overlaps x
+    assert norm(L, n=_p(1)) == INVALID                # normed_out overlaps residual_in
+    assert norm(L, ro=C.c_void_p(BASE + 64 * MB + 256)) == INVALID   # partial residual overlap
+    assert norm(L, s=_p(4)) == INVALID                # scale overlaps q
+    assert norm(L, M=1 << 45, H=32768) == INVALID     # 2^60 elements: sizes would overflow
+    assert swiglu(L, M=1 << 45, I=32768) == INVALID
+
+
+def test_swiglu_argument_errors(sgq_lib):
+    L = sgq_lib
+    assert swiglu(L, M=0) == OK
+    assert swiglu(L, fmt=7) == INVALID
+    assert swiglu(L, act=2) == INVALID
+    assert swiglu(L, flags=4) == INVALID              # ACT_ROUND_BF16 needs SiLU-and-mul
+    assert swiglu(L, flags=1) == INVALID              # GEMMA_WEIGHT is not a SwiGLU flag
+    assert swiglu(L, limit=0.0) == INVALID
+    assert swiglu(L, limit=float("nan")) == INVALID
+    assert swiglu(L, alpha=float("inf")) == INVALID
+    assert swiglu(L, I=-32) == INVALID
+    assert swiglu(L, I=48) == UNSUPPORTED
+    assert swiglu(L, fmt=1, I=64) == UNSUPPORTED
+    assert swiglu(L, gu=None) == INVALID
+    assert swiglu(L, gu=C.c_void_p(BASE + 4)) == MISALIGNED
+    assert swiglu(L, q=_p(0)) == INVALID              # q_out overlaps gate_up
+
+
+def test_binding_rejects_wrong_tensors():
+    import torch
+    x = torch.zeros(4, 64, dtype=torch.float32)
+    w = torch.zeros(64, dtype=torch.bfloat16)
+    with pytest.raises(binding.SgqError):
+        binding.rmsnorm_add_quant(x, w)
+    with pytest.raises(binding.SgqError):
+        binding.swiglu_quant(torch.zeros(4, 64, dtype=torch.bfloat16), fmt="nope")

@@ -1,0 +1,291 @@
+"""GPU parity: the CUDA kernels (called through the C ABI via the binding)
+against the fp64 CPU oracle, element by element, under the stated tolerances
+(oracle/parity.py). Covers the five workload families at their full sizes
+(sampled rows where the oracle would be slow), every format x op x quant
+source on ragged widths, degenerate rows, guard bands around every output,
+CUDA-graph replay, determinism and a side stream."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.parity import check_norm, check_swiglu
+from swiglu_fp8_activation_gb300 import inputs, rmsnorm_add_quant, swiglu_quant
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+def _log(name, stats):
+    path = os.environ.get("SGQ_PARITY_STATS")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps({"case": name, **stats}) + "\n")
+
+
+def _bits(t):
+    return inputs.bf16_bits(t.cpu())
+
+
+def _rows(M, n, seed=0):
+    """All rows when few, else the first, the last and n-2 sampled rows."""
+    if M <= n:
+        return np.arange(M)
+    rng = np.random.default_rng(seed)
+    mid = rng.choice(np.arange(1, M - 1), size=n - 2, replace=False)
+    return np.unique(np.r_[0, mid, M - 1])
+
+
+def run_norm(fmt, x, r, w, *, eps, gemma, from_fp32, normed=True, residual="separate", sample=None, name=""):
+    """x, r (or None), w: CPU bf16 tensors. residual: 'separate' | 'inplace'."""
+    M, H = x.shape
+    xd, wd = x.to(DEV), w.to(DEV)
+    rd = r.to(DEV) if r is not None else None
+    r_out = None
+    if rd is not None:
+        r_out = rd if residual == "inplace" else torch.empty_like(rd)
+    q, s, n, ro = rmsnorm_add_quant(xd, wd, fmt=fmt, residual_in=rd, residual_out=r_out, eps=eps, gemma=gemma,
+                                    quant_from_fp32=from_fp32, normed=normed)
+    torch.cuda.synchronize()
+    rows = np.arange(M) if sample is None else _rows(M, sample)
+    xb = _bits(x)[rows]
+    rb = _bits(r)[rows] if r is not None else None
+    ref = oracle.rmsnorm_add_quant(fmt, xb, rb, _bits(w), eps=eps, gemma=gemma, from_fp32=from_fp32,
+                                   normed=normed)
+    st = check_norm(fmt, ref, q.cpu().numpy()[rows], s.cpu().numpy()[rows],
+                    _bits(n)[rows] if normed else None, _bits(ro)[rows] if ro is not None else None,
+                    from_fp32=from_fp32)
+    _log(name or f"norm_{fmt}_M{M}_H{H}", st)
+    return st
+
+
+def run_swiglu(fmt, act, gu, *, from_fp32, round_act_bf16=False, alpha=1.702, beta=1.0, limit=7.0, sample=None,
+               name=""):
+    M = gu.shape[0]
+    q, s = swiglu_quant(gu.to(DEV), fmt=fmt, act=act, quant_from_fp32=from_fp32, round_act_bf16=round_act_bf16,
+                        alpha=alpha, beta=beta, limit=limit)
+    torch.cuda.synchronize()
+    rows = np.arange(M) if sample is None else _rows(M, sample)
+    ref = oracle.swiglu_quant(fmt, act, _bits(gu)[rows], from_fp32=from_fp32, round_act_bf16=round_act_bf16,
+                              alpha=alpha, beta=beta, limit=limit)
+    st = check_swiglu(fmt, ref, q.cpu().numpy()[rows], s.cpu().numpy()[rows], from_fp32=from_fp32)
+    _log(name or f"swiglu_{fmt}_{act}_M{M}_I{gu.shape[1] // 2}", st)
+    return st
+
+
+def run_norm_case(case, **kw):
+    t = inputs.make_norm(case)
+    return run_norm(case.fmt, t["x"], t["r"], t["w"], eps=case.eps, gemma=case.gemma, from_fp32=case.from_fp32,
+                    normed=case.normed_copy, name=f"{case.name}_M{case.M}_H{case.H}", **kw)
+
+
+def run_swiglu_case(case, **kw):
+    gu = inputs.make_swiglu(case)
+    return run_swiglu(case.fmt, case.act, gu, from_fp32=case.from_fp32, round_act_bf16=case.round_act_bf16,
+                      alpha=case.alpha, beta=case.beta, limit=case.limit, name=f"{case.name}_M{case.M}_I{case.I}", **kw)
+
+
+# ------------------------------------------------------------ the workloads
+
+def test_cfg1_gemma_norm_mxfp8_bf16_copy():
+    st = run_norm_case(inputs.workloads()["cfg1_norm_mx"][0])
+    assert st["residual_exact_frac"] == 1.0
+
+
+@pytest.mark.parametrize("case", inputs.workloads()["cfg1_norm_mx_sweep"], ids=lambda c: f"M{c.M}")
+def test_cfg1_sweep_inplace_residual(case):
+    run_norm_case(case, residual="inplace")
+
+
+@pytest.mark.parametrize("case", inputs.workloads()["cfg2_swiglu_mx"], ids=lambda c: f"M{c.M}")
+def test_cfg2_oai_swiglu_mxfp8(case):
+    run_swiglu_case(case)
+
+
+@pytest.mark.parametrize("case", inputs.workloads()["cfg3_block128"], ids=lambda c: f"{c.name}_M{c.M}")
+def test_cfg3_block128(case):
+    if isinstance(case, inputs.NormCase):
+        run_norm_case(case)
+    else:
+        run_swiglu_case(case)
+
+
+@pytest.mark.parametrize("case", inputs.workloads()["cfg4_per_token"], ids=lambda c: f"W{c.H}_M{c.M}")
+def test_cfg4_per_token(case):
+    run_norm_case(case, sample=64)
+
+
+@pytest.mark.parametrize("case", inputs.workloads()["cfg5_prefill"], ids=lambda c: c.name)
+def test_cfg5_prefill_stress(case):
+    if isinstance(case, inputs.NormCase):
+        run_norm_case(case, sample=48)
+    else:
+        run_swiglu_case(case, sample=48)
+
+
+# ------------------------------------------------- formats x ops x widths
+
+WIDTHS = {"mxfp8": [32, 160, 1056, 2176, 6144], "block128": [128, 384, 1536, 2176, 12288],
+          "per_token": [8, 24, 520, 7168, 16384]}
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "block128", "per_token"])
+@pytest.mark.parametrize("from_fp32", [False, True])
+@pytest.mark.parametrize("gemma", [True, False])
+def test_norm_formats_ragged(fmt, from_fp32, gemma):
+    for H in WIDTHS[fmt]:
+        for M in (1, 37):
+            t = inputs.norm_inputs(M, H, seed=H + M, x_std=2.0, r_std=0.5, w_mean=0.0 if gemma else 1.0, w_std=0.1)
+            run_norm(fmt, t["x"], t["r"], t["w"], eps=1e-6, gemma=gemma, from_fp32=from_fp32)
+            run_norm(fmt, t["x"], None, t["w"], eps=1e-5, gemma=gemma, from_fp32=from_fp32, normed=False)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "block128", "per_token"])
+@pytest.mark.parametrize("act,from_fp32,round_bf16", [("swiglu_oai", True, False), ("swiglu_oai", False, False),
+                                                      ("silu_mul", False, True), ("silu_mul", True, False),
+                                                      ("silu_mul", False, False)])
+def test_swiglu_formats_ragged(fmt, act, from_fp32, round_bf16):
+    for I in WIDTHS[fmt]:
+        for M in (1, 37):
+            gu = inputs.swiglu_inputs(M, I, seed=I + M, std=3.0)
+            run_swiglu(fmt, act, gu, from_fp32=from_fp32, round_act_bf16=round_bf16)
+
+
+def test_oai_parameters_and_unclamped_limit():
+    gu = inputs.swiglu_inputs(16, 1024, seed=9, std=4.0)
+    run_swiglu("mxfp8", "swiglu_oai", gu, from_fp32=True, alpha=1.0, beta=0.5, limit=3.0)
+    run_swiglu("block128", "swiglu_oai", gu, from_fp32=True, limit=float("inf"))
+
+
+# ------------------------------------------------------------ edge rows
+
+def _bf16(a):
+    return inputs.to_bf16(np.asarray(a, dtype=np.float64))
+
+
+def _edge_rows(H, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = [
+        np.zeros(H),                                       # all zero
+        np.full(H, 3.0),                                   # constant
+        np.where(np.arange(H) % 2 == 0, 1.0, -1.0),        # alternating signs
+        rng.standard_normal(H) * 1e-38,                    # bf16 subnormal / tiny
+        rng.standard_normal(H) * 1e15,                     # huge, with sum(h^2) still finite in fp32
+        np.r_[1e4, rng.standard_normal(H - 1) * 1e-3],     # one dominating element
+        np.where((np.arange(H) // 32) % 2 == 0, 0.0, rng.standard_normal(H)),   # every other 32-block zero
+        np.where(np.arange(H) % 32 < 31, 0.0, 5.0),         # one non-zero per block
+    ]
+    return np.stack(rows)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "block128", "per_token"])
+@pytest.mark.parametrize("from_fp32", [False, True])
+def test_norm_edge_rows(fmt, from_fp32):
+    H = 1024
+    x = _bf16(_edge_rows(H))
+    w = _bf16(np.random.default_rng(1).standard_normal(H) * 0.1)
+    run_norm(fmt, x, None, w, eps=1e-6, gemma=True, from_fp32=from_fp32)
+    r = _bf16(-_edge_rows(H, 5) * 0.5)
+    run_norm(fmt, x, r, w, eps=1e-6, gemma=True, from_fp32=from_fp32)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "block128", "per_token"])
+def test_swiglu_edge_rows(fmt):
+    I = 512
+    rows = _edge_rows(I)
+    g = np.r_[rows, np.full((1, I), -1e4), np.full((1, I), 50.0)]
+    u = np.r_[rows[::-1] * 0.25, np.full((1, I), 3.0), np.full((1, I), -1e3)]
+    gu = _bf16(np.concatenate([g, u], axis=1))
+    for act, f32, rb in (("swiglu_oai", True, False), ("silu_mul", False, True)):
+        run_swiglu(fmt, act, gu, from_fp32=f32, round_act_bf16=rb)
+
+
+# ------------------------------------------- guard bands, graphs, streams
+
+GUARD = 4096
+
+
+def _guarded(nbytes):
+    buf = torch.full((GUARD + nbytes + GUARD,), 0xA5, dtype=torch.uint8, device=DEV)
+    return buf, buf[GUARD:GUARD + nbytes]
+
+
+def _intact(buf, nbytes):
+    b = buf.cpu().numpy()
+    return (b[:GUARD] == 0xA5).all() and (b[GUARD + nbytes:] == 0xA5).all()
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "block128", "per_token"])
+@pytest.mark.parametrize("M,H", [(1, 32 * 4 * 3), (37, 1056 * 4), (5, 2176 * 4 - 512 * 4)])
+def test_outputs_stay_inside_their_buffers(fmt, M, H):
+    if fmt == "block128":
+        H = H // 128 * 128
+    t = inputs.norm_inputs(M, H, seed=2, x_std=1.0, r_std=1.0, w_mean=0.0, w_std=0.1)
+    x, r, w = (t[k].to(DEV) for k in ("x", "r", "w"))
+    ns = {"mxfp8": M * H // 32, "block128": M * H // 128 * 4, "per_token": M * 4}[fmt]
+    bq, q = _guarded(M * H)
+    bs, s = _guarded(ns)
+    bn, n = _guarded(M * H * 2)
+    br, ro = _guarded(M * H * 2)
+    sv = s if fmt == "mxfp8" else s.view(torch.float32)
+    rmsnorm_add_quant(x, w, fmt=fmt, residual_in=r, residual_out=ro.view(torch.bfloat16).view(M, H),
+                      q_out=q.view(M, H), scale_out=sv.view(M, -1), normed_out=n.view(torch.bfloat16).view(M, H))
+    bg, gq = _guarded(M * H)
+    bgs, gs = _guarded(ns)
+    gu = inputs.swiglu_inputs(M, H, seed=3, std=2.0).to(DEV)
+    swiglu_quant(gu, fmt=fmt, q_out=gq.view(M, H), scale_out=(gs if fmt == "mxfp8" else gs.view(torch.float32)).view(M, -1))
+    torch.cuda.synchronize()
+    for b, nb in ((bq, M * H), (bs, ns), (bn, M * H * 2), (br, M * H * 2), (bg, M * H), (bgs, ns)):
+        assert _intact(b, nb)
+
+
+def test_graph_replay_matches_eager():
+    case = inputs.norm_case_gemma_mx(64)
+    t = inputs.make_norm(case)
+    x, r, w = (t[k].to(DEV) for k in ("x", "r", "w"))
+    gu = inputs.make_swiglu(inputs.swiglu_case_oai_mx(64)).to(DEV)
+    ro = torch.empty_like(r)
+    q, s, n, _ = rmsnorm_add_quant(x, w, residual_in=r, residual_out=ro, normed=True)
+    q2, s2 = swiglu_quant(gu)
+    torch.cuda.synchronize()
+    eager = [v.clone() for v in (q, s, n, ro, q2, s2)]
+    for v in (q, s, n, ro, q2, s2):
+        v.zero_()
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(200):
+            rmsnorm_add_quant(x, w, residual_in=r, residual_out=ro, q_out=q, scale_out=s, normed_out=n)
+            swiglu_quant(gu, q_out=q2, scale_out=s2)
+    g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager, (q, s, n, ro, q2, s2)):
+        assert torch.equal(a, b)
+
+
+def test_deterministic_and_side_stream():
+    case = inputs.norm_case_block128(256)
+    t = inputs.make_norm(case)
+    x, w = t["x"].to(DEV), t["w"].to(DEV)
+    a = rmsnorm_add_quant(x, w, fmt="block128", gemma=False, quant_from_fp32=True)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        b = rmsnorm_add_quant(x, w, fmt="block128", gemma=False, quant_from_fp32=True, stream=side)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_misaligned_device_view_is_rejected():
+    from swiglu_fp8_activation_gb300 import SgqError
+    x = torch.zeros(4, 264, dtype=torch.bfloat16, device=DEV)[:, 8:]   # row stride breaks contiguity
+    w = torch.zeros(256, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(SgqError):
+        rmsnorm_add_quant(x, w)
+    flat = torch.zeros(4 * 256 + 1, dtype=torch.bfloat16, device=DEV)[1:].view(4, 256)   # 2-byte offset
+    with pytest.raises(SgqError) as e:
+        rmsnorm_add_quant(flat, w)
+    assert e.value.status == 3

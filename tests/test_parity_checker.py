@@ -1,0 +1,91 @@
+"""The parity checker accepts the oracle's own result and rejects planted
+mistakes (a code two steps off, a scale off by one, too many one-step code
+mismatches, a bf16 output two ulps off). Runs on the CPU."""
+import numpy as np
+import pytest
+
+import oracle
+from oracle.parity import check_norm, check_swiglu
+from swiglu_fp8_activation_gb300 import inputs
+
+
+def _norm(fmt, from_fp32=False):
+    case = inputs.norm_case_gemma_mx(16, 1024)
+    t = inputs.make_norm(case)
+    return oracle.rmsnorm_add_quant(fmt, inputs.bf16_bits(t["x"]), inputs.bf16_bits(t["r"]),
+                                    inputs.bf16_bits(t["w"]), eps=case.eps, gemma=True, from_fp32=from_fp32)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "block128", "per_token"])
+@pytest.mark.parametrize("from_fp32", [False, True])
+def test_checker_accepts_the_oracle(fmt, from_fp32):
+    ref = _norm(fmt, from_fp32)
+    st = check_norm(fmt, ref, ref["q"].copy(), ref["scale"].copy(), ref["normed"], ref["residual"],
+                    from_fp32=from_fp32)
+    assert st["code_mismatch"] == 0
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "block128", "per_token"])
+def test_checker_rejects_planted_mistakes(fmt):
+    ref = _norm(fmt)
+    # a code two steps away
+    q = ref["q"].copy()
+    j = np.argmax((q & 0x7F) > 8)
+    q.flat[j] = q.flat[j] - 2
+    with pytest.raises(AssertionError):
+        check_norm(fmt, ref, q, ref["scale"], from_fp32=False)
+    # a scale off by one code / one fp32 ulp in a non-excused group
+    s = ref["scale"].copy()
+    k = int(np.argmin(ref["gamb"].reshape(-1)))
+    assert ref["gamb"].reshape(-1)[k] == 0
+    if fmt == "mxfp8":
+        s.reshape(-1)[k] += 1
+    else:
+        s.reshape(-1)[k] = np.nextafter(s.reshape(-1)[k], np.float32(1e30))
+    with pytest.raises(AssertionError):
+        check_norm(fmt, ref, ref["q"], s, from_fp32=False)
+    # one-step code mismatches on more than 1e-4 of the elements
+    q = ref["q"].copy()
+    idx = np.flatnonzero(((q & 0x7F) > 8) & ((q & 0x7F) < 0x7E))[:20]
+    q.flat[idx] += 1
+    with pytest.raises(AssertionError):
+        check_norm(fmt, ref, q, ref["scale"], from_fp32=False)
+    # bf16 copy two ulps off
+    n = ref["normed"].copy()
+    n.flat[5] += 2
+    with pytest.raises(AssertionError):
+        check_norm(fmt, ref, ref["q"], ref["scale"], n, None, from_fp32=False)
+
+
+def test_checker_accepts_one_ulp_and_one_rare_step():
+    ref = _norm("mxfp8")
+    n = ref["normed"].copy()
+    n.flat[3] += 1
+    r = ref["residual"].copy()
+    r.flat[7] -= 1
+    check_norm("mxfp8", ref, ref["q"], ref["scale"], n, r, from_fp32=False)
+    big = oracle.swiglu_quant("mxfp8", "swiglu_oai", inputs.bf16_bits(inputs.swiglu_inputs(64, 768, seed=3, std=2.0)),
+                              from_fp32=True)
+    q = big["q"].copy()
+    j = int(np.flatnonzero(((q & 0x7F) > 8) & ((q & 0x7F) < 0x7E) & (big["gamb"].repeat(32, axis=1).reshape(q.shape) == 0))[0])
+    q.flat[j] += 1   # 1 of 49152 elements: below 1e-4
+    st = check_swiglu("mxfp8", big, q, big["scale"], from_fp32=True)
+    assert st["code_mismatch"] == 1
+
+
+def test_ties_do_not_count_but_must_be_within_one_step():
+    # fp32-source 1x128 norm with plain weights: exact ties are common
+    case = inputs.norm_case_block128(64, 4096)
+    t = inputs.make_norm(case)
+    ref = oracle.rmsnorm_add_quant("block128", inputs.bf16_bits(t["x"]), None, inputs.bf16_bits(t["w"]),
+                                   eps=case.eps, gemma=False, from_fp32=True)
+    tie = (ref["amb"] & oracle.AMB_TIE) != 0
+    assert tie.sum() > 30          # about 4e-4 of the elements
+    q = ref["q"].copy()
+    idx = np.flatnonzero(tie & ((q & 0x7F) > 8) & ((q & 0x7F) < 0x7E))
+    q.flat[idx] += 1               # flip every tie by one step: still accepted
+    st = check_norm("block128", ref, q, ref["scale"], from_fp32=True)
+    assert st["tie_mismatch"] == idx.size and st["code_mismatch"] == 0
+    q.flat[idx[0]] += 1            # two steps at a tie: rejected
+    with pytest.raises(AssertionError):
+        check_norm("block128", ref, q, ref["scale"], from_fp32=True)
