@@ -53,7 +53,7 @@ extern "C" {
 #endif
 
 #define SGQ_ABI_VERSION 1
-#define SGQ_MAX_WIDTH 32768
+#define SGQ_MAX_WIDTH 16384
 
 /* Quantisation format of the output activation. */
 typedef enum sgq_format {

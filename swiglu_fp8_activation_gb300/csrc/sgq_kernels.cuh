@@ -43,7 +43,8 @@ struct SwigluArgs {
 //   MX:  code = E8M0 of the 1x32 block's amax; q = E4M3(src * 2^(127-code)),
 //        the scaling being exact (a power of two).
 //   FP8: s = amax / 448 (IEEE fp32 division); q = E4M3(src / s) with the IEEE
-//        fp32 quotient; s = 0 (all-zero group) stores s = 0 and q = 0.
+//        fp32 quotient (div_rn from one correctly rounded reciprocal per
+//        group); s = 0 (all-zero group) stores s = 0 and q = 0.
 template <int FMT, int NV>
 __device__ __forceinline__ void quantize_store(const float (&src)[NV][8], int64_t row, bool row_ok,
                                                int t, int tpr, int lrow, int W, uint8_t* q,
@@ -80,8 +81,14 @@ __device__ __forceinline__ void quantize_store(const float (&src)[NV][8], int64_
             if ((c & 3) == 0) static_cast<uint8_t*>(scale)[row * (W >> 5) + (c >> 2)] = (uint8_t)code;
         } else {
             const float s = __fdiv_rn(amax, 448.0f);
+            if (s >= 0x1p-126f) {
+                const float r = __frcp_rn(s);   // once per group, then one FMA pair per element
 #pragma unroll
-            for (int k = 0; k < 8; ++k) tq[k] = (s == 0.0f) ? 0.0f : __fdiv_rn(src[v][k], s);
+                for (int k = 0; k < 8; ++k) tq[k] = div_rn(src[v][k], s, r);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) tq[k] = (s == 0.0f) ? 0.0f : __fdiv_rn(src[v][k], s);
+            }
             if (FMT == FMT_B128 && (c & 15) == 0) static_cast<float*>(scale)[row * (W >> 7) + (c >> 4)] = s;
             if (FMT == FMT_PT && c == 0) static_cast<float*>(scale)[row] = s;
         }
@@ -104,15 +111,18 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
     const int H = a.H, nchunks = H >> 3;
     const int64_t base = row * (int64_t)H;
 
-    // 1. issue every load of the row before any arithmetic
-    uint4 xv[NV], rv[NV];
+    // 1. issue every load of the row (x, r and the weight) before any arithmetic
+    pdl_wait();
+    uint4 xv[NV], rv[NV], wv[NV];
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
         const int c = t + v * tpr;
         const bool ok = row_ok && c < nchunks;
         xv[v] = ok ? ld_once(a.x + base + (int64_t)c * 8) : make_uint4(0, 0, 0, 0);
         rv[v] = (ok && a.r_in) ? ld_coherent(a.r_in + base + (int64_t)c * 8) : make_uint4(0, 0, 0, 0);
+        wv[v] = ok ? ld_shared_by_rows(a.w + (int64_t)c * 8) : make_uint4(0, 0, 0, 0);
     }
+    pdl_trigger();
 
     // 2. h = x + r in fp32; write the updated residual; partial sum of squares
     float h[NV][8];
@@ -148,7 +158,7 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
             continue;
         }
         float wf[8], y[8];
-        bf16x8_to_f32(ld_shared_by_rows(a.w + (int64_t)c * 8), wf);
+        bf16x8_to_f32(wv[v], wf);
 #pragma unroll
         for (int k = 0; k < 8; ++k) y[k] = h[v][k] * inv * (gemma ? 1.0f + wf[k] : wf[k]);
         const uint4 yb = f32x8_to_bf16x8(y);
@@ -165,12 +175,29 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
     quantize_store<FMT, NV>(src, row, row_ok, t, tpr, lrow, H, a.q, a.scale, part_amax);
 }
 
-__device__ __forceinline__ float sigmoid(float z) {
-    return __frcp_rn(1.0f + expf(-z));
+// The activation of two (gate, up) pairs, in fp32:
+//   OAI:  g' = min(g, limit), u' = min(max(u, -limit), limit),
+//         a = (g' * sigmoid(alpha * g')) * (u' + beta); alpha * g' is carried
+//         with its exact FMA residual into the sigmoid;
+//   SiLU: a = (g * sigmoid(g)) * u, the first factor rounded to bf16 when
+//         round_silu is set.
+template <int ACT>
+__device__ __forceinline__ float2 activation2(float2 g, float2 u, float alpha, float beta, float limit,
+                                              bool round_silu) {
+    if (ACT == ACT_OAI) {
+        const float2 gc = make_float2(fminf(g.x, limit), fminf(g.y, limit));
+        const float2 uc = make_float2(fminf(fmaxf(u.x, -limit), limit), fminf(fmaxf(u.y, -limit), limit));
+        const float2 zh = __fmul2_rn(f2(alpha), gc);
+        const float2 zl = __ffma2_rn(f2(alpha), gc, __fmul2_rn(zh, f2(-1.0f)));
+        return __fmul2_rn(__fmul2_rn(gc, sigmoid2(zh, zl)), __fadd2_rn(uc, f2(beta)));
+    }
+    float2 s = __fmul2_rn(g, sigmoid2(g, f2(0.0f)));
+    if (round_silu) s = make_float2(round_bf16(s.x), round_bf16(s.y));
+    return __fmul2_rn(s, u);
 }
 
 // SwiGLU + quantisation. One row per `tpr` threads.
-template <int FMT, int NV>
+template <int FMT, int NV, int ACT>
 __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs a) {
     __shared__ float part_amax[32];
     const int tpr = a.tpr;
@@ -181,6 +208,7 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
     const int I = a.I, nchunks = I >> 3;
     const uint16_t* grow = a.gu + row * (int64_t)(2 * I);
 
+    pdl_wait();
     uint4 gv[NV], uv[NV];
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
@@ -189,8 +217,9 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
         gv[v] = ok ? ld_once(grow + (int64_t)c * 8) : make_uint4(0, 0, 0, 0);
         uv[v] = ok ? ld_once(grow + I + (int64_t)c * 8) : make_uint4(0, 0, 0, 0);
     }
+    pdl_trigger();
 
-    const bool from32 = (a.flags & F_FROM_FP32) != 0, round_silu = (a.flags & F_ACT_BF16) != 0;
+    const bool round_silu = (a.flags & F_ACT_BF16) != 0;
     float src[NV][8];
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
@@ -198,19 +227,18 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
         bf16x8_to_f32(gv[v], g);
         bf16x8_to_f32(uv[v], u);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            float act;
-            if (a.act == ACT_OAI) {
-                const float gc = fminf(g[k], a.limit);
-                const float uc = fminf(fmaxf(u[k], -a.limit), a.limit);
-                act = gc * sigmoid(a.alpha * gc) * (uc + a.beta);
-            } else {
-                float s = g[k] * sigmoid(g[k]);
-                if (round_silu) s = round_bf16(s);
-                act = s * u[k];
-            }
-            src[v][k] = from32 ? act : round_bf16(act);
+        for (int k = 0; k < 8; k += 2) {
+            const float2 act = activation2<ACT>(make_float2(g[k], g[k + 1]), make_float2(u[k], u[k + 1]),
+                                                a.alpha, a.beta, a.limit, round_silu);
+            src[v][k] = act.x;
+            src[v][k + 1] = act.y;
         }
+    }
+    if (!(a.flags & F_FROM_FP32)) {    // quantise the bf16 rounding of the activation
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) src[v][k] = round_bf16(src[v][k]);
     }
     // chunks past the row end loaded zeros, and every activation of 0 and 0 is 0
 

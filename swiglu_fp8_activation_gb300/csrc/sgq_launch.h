@@ -21,6 +21,25 @@ struct Plan {
 // more than kMaxTPR threads per row.
 bool plan_rows(int64_t M, int W, int sm_count, Plan* p);
 
+// Launch kernel k on `stream` with programmatic stream serialisation: the
+// grid may begin launching while the preceding kernel on the stream finishes
+// (the kernels wait in pdl_wait() before touching memory).
+template <typename Args>
+cudaError_t launch_pdl(void (*k)(const Args), const Plan& p, const Args& a, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.blockDim = dim3((unsigned)(p.rpc * p.tpr));
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 cudaError_t launch_norm(int fmt, const Plan& p, const NormArgs& a, cudaStream_t stream);
 cudaError_t launch_swiglu(int fmt, const Plan& p, const SwigluArgs& a, cudaStream_t stream);
 

@@ -19,8 +19,7 @@ NormKernel pick(int nv) {
 
 cudaError_t launch_norm(int fmt, const Plan& p, const NormArgs& a, cudaStream_t stream) {
     NormKernel k = fmt == FMT_MX ? pick<FMT_MX>(p.nv) : fmt == FMT_B128 ? pick<FMT_B128>(p.nv) : pick<FMT_PT>(p.nv);
-    k<<<(unsigned)p.grid, (unsigned)(p.rpc * p.tpr), 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(k, p, a, stream);
 }
 
 }  // namespace sgq

@@ -6,21 +6,25 @@ namespace sgq {
 namespace {
 using SwigluKernel = void (*)(const SwigluArgs);
 
-template <int FMT>
+template <int FMT, int ACT>
 SwigluKernel pick(int nv) {
     switch (nv) {
-        case 1: return swiglu_quant_kernel<FMT, 1>;
-        case 2: return swiglu_quant_kernel<FMT, 2>;
-        case 3: return swiglu_quant_kernel<FMT, 3>;
-        default: return swiglu_quant_kernel<FMT, 4>;
+        case 1: return swiglu_quant_kernel<FMT, 1, ACT>;
+        case 2: return swiglu_quant_kernel<FMT, 2, ACT>;
+        case 3: return swiglu_quant_kernel<FMT, 3, ACT>;
+        default: return swiglu_quant_kernel<FMT, 4, ACT>;
     }
+}
+
+template <int ACT>
+SwigluKernel pick_fmt(int fmt, int nv) {
+    return fmt == FMT_MX ? pick<FMT_MX, ACT>(nv) : fmt == FMT_B128 ? pick<FMT_B128, ACT>(nv) : pick<FMT_PT, ACT>(nv);
 }
 }  // namespace
 
 cudaError_t launch_swiglu(int fmt, const Plan& p, const SwigluArgs& a, cudaStream_t stream) {
-    SwigluKernel k = fmt == FMT_MX ? pick<FMT_MX>(p.nv) : fmt == FMT_B128 ? pick<FMT_B128>(p.nv) : pick<FMT_PT>(p.nv);
-    k<<<(unsigned)p.grid, (unsigned)(p.rpc * p.tpr), 0, stream>>>(a);
-    return cudaGetLastError();
+    SwigluKernel k = a.act == ACT_OAI ? pick_fmt<ACT_OAI>(fmt, p.nv) : pick_fmt<ACT_SILU>(fmt, p.nv);
+    return launch_pdl(k, p, a, stream);
 }
 
 }  // namespace sgq

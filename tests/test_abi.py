@@ -88,7 +88,7 @@ def test_norm_argument_errors(sgq_lib):
     assert norm(L, H=48) == UNSUPPORTED               # MX needs H % 32 == 0
     assert norm(L, fmt=1, H=96) == UNSUPPORTED        # 1x128 needs H % 128 == 0
     assert norm(L, fmt=2, H=20) == UNSUPPORTED        # per-token needs H % 8 == 0
-    assert norm(L, H=32768 + 32) == UNSUPPORTED       # above SGQ_MAX_WIDTH
+    assert norm(L, H=16384 + 32) == UNSUPPORTED       # above SGQ_MAX_WIDTH
     for kw in ("x", "w", "q", "s"):
         assert norm(L, **{kw: None}) == INVALID, kw
     assert norm(L, r=None) == INVALID                 # residual_out without residual_in
@@ -100,8 +100,8 @@ def test_norm_argument_errors(sgq_lib):
     assert norm(L, n=_p(1)) == INVALID                # normed_out overlaps residual_in
     assert norm(L, ro=C.c_void_p(BASE + 64 * MB + 256)) == INVALID   # partial residual overlap
     assert norm(L, s=_p(4)) == INVALID                # scale overlaps q
-    assert norm(L, M=1 << 45, H=32768) == INVALID     # 2^60 elements: sizes would overflow
-    assert swiglu(L, M=1 << 45, I=32768) == INVALID
+    assert norm(L, M=1 << 45, H=16384) == INVALID     # 2^59 elements: sizes would overflow
+    assert swiglu(L, M=1 << 45, I=16384) == INVALID
 
 
 def test_swiglu_argument_errors(sgq_lib):

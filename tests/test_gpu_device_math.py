@@ -1,0 +1,101 @@
+"""The two arithmetic shortcuts of the kernels, checked on the GPU:
+
+* sigmoid2() (split exponent, fitted 2^x polynomial, refined reciprocal)
+  against fp64 over |z| <= 130, within 2^-22 relative;
+* activation2() (the OAI SwiGLU of the kernels) against fp64, within 2^-21
+  relative, including an element whose exact value lies 3.1e-7 relative
+  above an E4M3 rounding boundary;
+* div_rn() (one reciprocal per group + Markstein's FMA correction) against
+  CUDA's correctly rounded __fdiv_rn, bit for bit, for the FP8 quotients the
+  kernels form (|a| <= b * 448 * (1 + 2^-20), b normal) and for random pairs.
+"""
+import ctypes as C
+import os
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def devlib():
+    import __graft_entry__ as g
+    out_dir = os.path.join(ROOT, "_build")
+    os.makedirs(out_dir, exist_ok=True)
+    so = os.path.join(out_dir, "libdevice_math_check.so")
+    cmd = [g._nvcc(), *g.ARCH, "-O3", "-std=c++17", "-shared", "-Xcompiler", "-fPIC", "-I", g.CSRC,
+           "-o", so, os.path.join(ROOT, "tests", "cuda", "device_math_check.cu")]
+    subprocess.run(cmd, check=True)
+    L = C.CDLL(so)
+    for f in (L.run_sigmoid, L.run_div, L.run_oai):
+        f.restype = C.c_int
+    return L
+
+
+def _p(t):
+    return C.c_void_p(t.data_ptr())
+
+
+def test_sigmoid_accuracy(devlib):
+    z = np.concatenate([np.linspace(-130, 130, 2_000_001), np.array([0.0, -0.0, 1e-30, -1e-30, 87.3, -87.3, 1e30, -1e30]),
+                        np.random.default_rng(0).standard_normal(200_000) * 8]).astype(np.float32)
+    zt = torch.from_numpy(z).cuda()
+    out = torch.empty_like(zt)
+    assert devlib.run_sigmoid(_p(zt), _p(out), z.size) == 0
+    got = out.cpu().numpy().astype(np.float64)
+    zd = z.astype(np.float64)
+    with np.errstate(over="ignore"):
+        want = 1.0 / (1.0 + np.exp(-zd))
+    tiny = want < 2.0 ** -126                       # below the fp32 normal range: absolute check
+    rel = np.abs(got - want) / np.where(tiny, 1.0, want)
+    assert rel[~tiny].max() <= 2.0 ** -22, rel[~tiny].max()
+    assert np.abs(got - want)[tiny].max() <= 2.0 ** -126
+    assert (got[z == 0] == 0.5).all()
+
+
+def test_oai_activation_accuracy(devlib):
+    rng = np.random.default_rng(2)
+    n = 2_000_000
+    g = torch.from_numpy(rng.standard_normal(n) * 4.0).bfloat16().float().numpy()
+    u = torch.from_numpy(rng.standard_normal(n) * 4.0).bfloat16().float().numpy()
+    # the element that an error of 2.8e-7 pushed across an E4M3 boundary
+    g[:2], u[:2] = -1.578125, -3.25
+    alpha, beta, limit = np.float32(1.702), 1.0, 7.0
+    gt, ut = torch.from_numpy(g).cuda(), torch.from_numpy(u).cuda()
+    out = torch.empty_like(gt)
+    assert devlib.run_oai(_p(gt), _p(ut), _p(out), n, C.c_float(alpha), C.c_float(beta), C.c_float(limit)) == 0
+    got = out.cpu().numpy().astype(np.float64)
+    gc = np.minimum(g.astype(np.float64), limit)
+    uc = np.clip(u.astype(np.float64), -limit, limit)
+    want = gc / (1.0 + np.exp(-float(alpha) * gc)) * (uc + beta)
+    ok = np.abs(want) > 2.0 ** -100
+    rel = np.abs(got - want)[ok] / np.abs(want)[ok]
+    assert rel.max() <= 2.0 ** -21, rel.max()
+    assert got[0] > 0.2265625          # exact value 0.22656257..., the boundary is 29/128
+
+
+def test_div_rn_matches_ieee_division(devlib):
+    rng = np.random.default_rng(1)
+    n = 4_000_000
+    # the kernels' case: b = amax / 448, |a| <= amax
+    amax = (rng.standard_normal(n) * 2.0 ** rng.integers(-100, 100, n)).astype(np.float32)
+    amax = np.abs(amax) + np.float32(2.0 ** -100)
+    b = (amax / np.float32(448.0)).astype(np.float32)
+    a = (amax * rng.uniform(-1, 1, n)).astype(np.float32)
+    # bf16-valued numerators, where exact E4M3 midpoints are common
+    a[: n // 4] = torch.from_numpy(a[: n // 4]).bfloat16().float().numpy()
+    a[n // 4: n // 2] = amax[n // 4: n // 2] * rng.choice([-1, 1], n // 4)
+    # unrelated random pairs
+    a2 = (rng.standard_normal(n) * 2.0 ** rng.integers(-60, 60, n)).astype(np.float32)
+    b2 = (np.abs(rng.standard_normal(n)) * 2.0 ** rng.integers(-60, 60, n) + 2.0 ** -100).astype(np.float32)
+    for aa, bb in ((a, b), (a2, b2)):
+        at, bt = torch.from_numpy(aa).cuda(), torch.from_numpy(bb).cuda()
+        qf, qi = torch.empty_like(at), torch.empty_like(at)
+        assert devlib.run_div(_p(at), _p(bt), _p(qf), _p(qi), n) == 0
+        qf, qi = qf.cpu().numpy(), qi.cpu().numpy()
+        normal = (np.abs(qi) >= 2.0 ** -126) & np.isfinite(qi)     # overflowing pairs never occur in the kernels
+        np.testing.assert_array_equal(qf.view(np.uint32)[normal], qi.view(np.uint32)[normal])
