@@ -541,24 +541,59 @@ def run_ours(args, world, rank, local):
 
 
 def run_profile(args):
-    """Only one kernel of the prefill step (for ncu): `--warmup` untimed then
-    `--steps` timed launches on the M=8192 workload (inputs > L2, rotated)."""
+    """One kernel only (for ncu): `--warmup` untimed then `--steps` timed
+    launches. norm / swiglu: the M=8192 prefill workload (inputs > L2,
+    rotated). pertoken: RMSNorm + per-token FP8 at W=7168, M=4096 (three
+    rotating input sets, 176 MB together). silu128: SiLU-and-mul + 1x128
+    (bf16 roundings) at I=12288, M=2048 (three sets, 302 MB together)."""
     import torch
     dev = torch.device("cuda", 0)
-    pf = Prefill(dev)
-    fn = pf.lib.rmsnorm_add_quant if args.profile == "norm" else pf.lib.swiglu_quant
-    pick = 0 if args.profile == "norm" else 1
+    if args.profile == "silu128":
+        from swiglu_fp8_activation_gb300 import inputs, library
+        import ctypes as C
+        M, I = 2048, 12288
+        gu = inputs.swiglu_inputs(M, I, seed=2, std=1.0)
+        sets = [gu.to(dev) for _ in range(ROTATE)]
+        q = torch.empty(M, I, dtype=torch.uint8, device=dev)
+        sc = torch.empty(M, I // 128, dtype=torch.float32, device=dev)
+        lib = library()
+        stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+        arglist = [(1, 1, 4, M, I, 1.702, 1.0, 7.0, C.c_void_p(g.data_ptr()), C.c_void_p(q.data_ptr()),
+                    C.c_void_p(sc.data_ptr()), stream) for g in sets]
+        fn = lib.swiglu_quant
+        nbytes = swiglu_bytes(M, I, "block128")
+        get = lambda k: arglist[k % ROTATE]
+    elif args.profile == "pertoken":
+        from swiglu_fp8_activation_gb300 import inputs, library
+        case = inputs.norm_case_per_token(4096, 7168)
+        t = inputs.make_norm(case)
+        sets = [(t["x"].to(dev), t["w"].to(dev)) for _ in range(ROTATE)]
+        q = torch.empty(case.M, case.H, dtype=torch.uint8, device=dev)
+        sc = torch.empty(case.M, 1, dtype=torch.float32, device=dev)
+        import ctypes as C
+        lib = library()
+        stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+        arglist = [(2, 0, case.M, case.H, case.eps, C.c_void_p(x.data_ptr()), None, None, C.c_void_p(w.data_ptr()),
+                    C.c_void_p(q.data_ptr()), C.c_void_p(sc.data_ptr()), None, stream) for x, w in sets]
+        fn, pick = lib.rmsnorm_add_quant, None
+        nbytes = norm_bytes(case.M, case.H, False, False, "per_token")
+        get = lambda k: arglist[k % ROTATE]
+    else:
+        pf = Prefill(dev)
+        fn = pf.lib.rmsnorm_add_quant if args.profile == "norm" else pf.lib.swiglu_quant
+        pick = 0 if args.profile == "norm" else 1
+        nbytes = norm_bytes(M_PREFILL, H) if args.profile == "norm" else swiglu_bytes(M_PREFILL, I_PREFILL)
+        get = lambda k: pf.args[k % ROTATE][pick]
     for k in range(args.warmup):
-        _call(fn, pf.args[k % ROTATE][pick])
+        _call(fn, get(k))
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record()
     for k in range(args.steps):
-        _call(fn, pf.args[k % ROTATE][pick])
+        _call(fn, get(k))
     e.record()
     torch.cuda.synchronize()
     us = s.elapsed_time(e) * 1e3 / args.steps
-    nbytes = norm_bytes(M_PREFILL, H) if args.profile == "norm" else swiglu_bytes(M_PREFILL, I_PREFILL)
     print(json.dumps({"profile": args.profile, "us_per_launch": round(us, 2),
                       "GBps": round(nbytes / us / 1e3, 1), "launches": args.warmup + args.steps}), flush=True)
 
@@ -572,7 +607,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle time")
     ap.add_argument("--quick", action="store_true", help="skip the decode and other-config tables")
-    ap.add_argument("--profile", choices=("norm", "swiglu"), help="time one kernel only (for ncu)")
+    ap.add_argument("--profile", choices=("norm", "swiglu", "pertoken", "silu128"),
+                    help="time one kernel only (for ncu)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")

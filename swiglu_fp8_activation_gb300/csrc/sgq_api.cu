@@ -11,25 +11,35 @@
 
 namespace sgq {
 
-// Rows of width W: `nv` chunks per thread and `tpr` threads per row, preferring
-// an exact fit (W/8 = tpr * nv with tpr a multiple of 32) and the most chunks
-// per thread; otherwise the fewest threads that cover the row. Small M takes
-// fewer rows per CTA so that the grid spreads over the SMs.
+// Rows of width W: `nv` chunks per thread and `tpr` threads per row (a
+// multiple of 32, at most kMaxTPR), preferring an exact fit W/8 = tpr * nv.
+//  * Large M (bandwidth-bound): the most chunks per thread, so that each
+//    thread keeps more loads in flight and rows need fewer threads.
+//  * Small M (latency-bound, the whole grid fits in one wave even at one
+//    chunk per thread): the fewest chunks per thread, so that each thread's
+//    serial work is shortest.
+// Several rows share a CTA up to kTargetCTA threads; small M takes fewer rows
+// per CTA so that the grid spreads over the SMs.
 bool plan_rows(int64_t M, int W, int sm_count, Plan* p) {
     const int nchunks = W / 8;
+    const bool small = sm_count > 0 && M * (int64_t)nchunks <= (int64_t)sm_count * 1024;
     int nv = 0, tpr = 0;
-    for (int cand = kMaxNV; cand >= 1; --cand) {
+    for (int i = 0; i < kMaxNV && nv == 0; ++i) {          // exact fits first
+        const int cand = small ? 1 + i : kMaxNV - i;
         if (nchunks % (32 * cand) == 0 && nchunks / cand <= kMaxTPR) {
             nv = cand;
             tpr = nchunks / cand;
-            break;
         }
     }
-    if (nv == 0) {
-        nv = (nchunks + 31) / 32 < kMaxNV ? (nchunks + 31) / 32 : kMaxNV;
-        tpr = ((nchunks + nv - 1) / nv + 31) / 32 * 32;
+    for (int i = 0; i < kMaxNV && nv == 0; ++i) {          // else the fewest threads that cover the row
+        const int cand = small ? 1 + i : kMaxNV - i;
+        const int t = ((nchunks + cand - 1) / cand + 31) / 32 * 32;
+        if (t <= kMaxTPR && (small || (nchunks + 31) / 32 >= cand || cand == 1)) {
+            nv = cand;
+            tpr = t;
+        }
     }
-    if (tpr > kMaxTPR) return false;
+    if (nv == 0 || tpr > kMaxTPR) return false;
     int rpc = kTargetCTA / tpr > 1 ? kTargetCTA / tpr : 1;
     const int64_t per_sm = sm_count > 0 ? (M + sm_count - 1) / sm_count : M;
     if (per_sm < rpc) rpc = per_sm > 1 ? (int)per_sm : 1;

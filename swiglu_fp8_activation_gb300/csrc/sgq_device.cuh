@@ -127,9 +127,12 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 
 // ------------------------------------------------------------ arithmetic
 
+// Hardware reciprocal approximation (about 1 ulp); subnormal inputs and
+// results flush to zero, which the callers never produce (they pass values
+// in [1, 2]).
 __device__ __forceinline__ float rcp_approx(float x) {
     float y;
-    asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
@@ -141,69 +144,84 @@ constexpr float kLog2eLo = 1.925963033500011e-08f;       // log2(e) - kLog2eHi
 // held in the low mantissa bits.
 constexpr float kRoundMagic = 12582912.0f;
 
-// 2^x for |x| <= 0.5005: degree-6 polynomial whose coefficients were fitted
-// for least relative error (Lawson-weighted least squares on 4000 Chebyshev
-// nodes, then rounded to fp32). Fit error 1.9e-9; fp32 Horner evaluation
-// stays within 1.4 ulp.
-constexpr float kExp2C0 = 1.0f, kExp2C1 = 0.6931471824645996f, kExp2C2 = 0.24022646248340607f,
-                kExp2C3 = 0.05550328269600868f, kExp2C4 = 0.009618490003049374f,
-                kExp2C5 = 0.0013400063617154956f, kExp2C6 = 0.00015345696010626853f;
-
 __device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
 
-// Logistic sigmoid 1/(1 + e^-z) of two values, z = zh + zl (zl: the exact
-// residual of the fp32 product that formed zh, or 0). Written from the
-// mathematics, on packed fp32x2 arithmetic, with every term kept on the
-// negative side so that no operand needs a separate negation:
-//   * E = e^-|z| = 2^q, q = -|z| log2 e carried as head qh = RN(-|z| log2e_hi)
-//     plus tail (the FMA residual of that product, |z| log2e_lo and the
-//     residual zl), in the manner of Cody and Waite's argument reduction;
-//   * q = n + f with n = round(qh) <= 0 and |f| <= 0.5005: 2^f from the
-//     polynomial above, times 2^n by adding n to the exponent field (two
-//     steps when E falls below the normal range, a rare branch);
-//   * sigmoid(|z|) = 1/(1+E) and sigmoid(-|z|) = E/(1+E), the hardware
-//     reciprocal refined by one Newton-Raphson step.
-// |z| is capped at 128, where e^-128 underflows fp32. Relative error about
-// 2 ulp.
-__device__ __forceinline__ float2 sigmoid2(float2 zh, float2 zl) {
-    const float2 az = make_float2(fminf(fabsf(zh.x), 128.0f), fminf(fabsf(zh.y), 128.0f));
-    // |z| = az + azl: the residual takes the sign of zh (it is zero past the cap)
-    const float2 azl = make_float2(
-        fabsf(zh.x) <= 128.0f ? __uint_as_float(__float_as_uint(zl.x) ^ (__float_as_uint(zh.x) & 0x80000000u)) : 0.0f,
-        fabsf(zh.y) <= 128.0f ? __uint_as_float(__float_as_uint(zl.y) ^ (__float_as_uint(zh.y) & 0x80000000u)) : 0.0f);
-    const float2 qh = __fmul2_rn(az, f2(-kLog2eHi));                     // -|z| log2e, rounded
-    float2 tail = __ffma2_rn(az, f2(kLog2eHi), qh);                      // |z| log2e_hi + qh, exact
-    tail = __ffma2_rn(az, f2(kLog2eLo), tail);
-    tail = __ffma2_rn(azl, f2(kLog2eHi), tail);                          // q = qh - tail
-    const float2 big = __fadd2_rn(qh, f2(kRoundMagic));                  // round(qh) in the low bits
-    const float2 n = __fadd2_rn(big, f2(-kRoundMagic));
-    float2 f = __ffma2_rn(n, f2(-1.0f), qh);                             // qh - n, exact
-    f = __ffma2_rn(tail, f2(-1.0f), f);
-    float2 e = __ffma2_rn(f2(kExp2C6), f, f2(kExp2C5));
-    e = __ffma2_rn(e, f, f2(kExp2C4));
-    e = __ffma2_rn(e, f, f2(kExp2C3));
-    e = __ffma2_rn(e, f, f2(kExp2C2));
-    e = __ffma2_rn(e, f, f2(kExp2C1));
-    e = __ffma2_rn(e, f, f2(kExp2C0));                                   // 2^f in [0.7, 1.42]
-    // 2^n: add n to the exponent field. Exact while n >= -125 (e's field is 126 or 127).
-    const int nx = __float_as_int(big.x) - __float_as_int(kRoundMagic);
-    const int ny = __float_as_int(big.y) - __float_as_int(kRoundMagic);
-    if (min(nx, ny) >= -125) {
-        e = make_float2(__uint_as_float(__float_as_uint(e.x) + ((uint32_t)nx << 23)),
-                        __uint_as_float(__float_as_uint(e.y) + ((uint32_t)ny << 23)));
-    } else {   // |z| > 86.6: E below the normal range, scale in two exact steps
-        e = make_float2(__uint_as_float(__float_as_uint(e.x) + ((uint32_t)max(nx, -125) << 23)),
-                        __uint_as_float(__float_as_uint(e.y) + ((uint32_t)max(ny, -125) << 23)));
-        e = __fmul2_rn(e, make_float2(__uint_as_float((uint32_t)(127 + min(nx + 125, 0)) << 23),
-                                      __uint_as_float((uint32_t)(127 + min(ny + 125, 0)) << 23)));
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Arguments of sigmoid8() must lie in [kSigLo, kSigHi]. Past kSigHi the
+// sigmoid is 1.0 in fp32 (1 - e^-20 rounds to 1); below kSigLo it is 0
+// (e^-104 is below half the smallest fp32 subnormal), so callers clamp first.
+constexpr float kSigLo = -104.0f, kSigHi = 20.0f;
+
+// Logistic sigmoid 1/(1 + E), E = e^-z, of the 8 values of one chunk, with
+// z = zh - nzl (nzl: the negated exact residual of the fp32 product that
+// formed zh, used when TAIL is set). Written from the mathematics on packed
+// fp32x2 arithmetic:
+//   * E = 2^q, q = -z log2 e carried as head qh = RN(-z log2e_hi) plus tail
+//     (the FMA residual of that product, z log2e_lo and the residual of z),
+//     in the manner of Cody and Waite's argument reduction;
+//   * q = n + f with n = round(qh) and |f| <= 0.5005: the hardware 2^x
+//     approximation only ever sees |f| <= 0.5005 (where it is accurate to
+//     about 2 ulp), and 2^n is added to the exponent field; the
+//     round-to-integer constant's bit pattern shifted left by 23 is zero mod
+//     2^32, so the rounded head's bits shifted left by 23 are n << 23;
+//   * sigmoid = 1/(1+E), the hardware reciprocal refined by one
+//     Newton-Raphson step. With z in [-104, 20], n lies in [-29, 150]; where
+//     n > 126 (z < -87.7, a branch taken once per chunk) E would overflow and
+//     the sigmoid, which is then 2^-q to within 2^-126 relative, is formed as
+//     2^-f * 2^-n in two exact scaling steps.
+template <bool TAIL>
+__device__ __forceinline__ void sigmoid8(const float (&zh)[8], const float (&nzl)[8], float (&out)[8]) {
+    float2 e[4], fr[4];
+    uint32_t nb[8];
+    float qmax = -1.0e30f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 z = make_float2(zh[2 * i], zh[2 * i + 1]);
+        const float2 qh = __fmul2_rn(z, f2(-kLog2eHi));                  // -z log2e, rounded
+        float2 tail = __ffma2_rn(z, f2(kLog2eHi), qh);                   // z log2e_hi + qh, exact
+        tail = __ffma2_rn(z, f2(kLog2eLo), tail);
+        if (TAIL) tail = __ffma2_rn(make_float2(nzl[2 * i], nzl[2 * i + 1]), f2(-kLog2eHi), tail);   // q = qh - tail
+        const float2 big = __fadd2_rn(qh, f2(kRoundMagic));              // round(qh) in the low bits
+        const float2 n = __fadd2_rn(big, f2(-kRoundMagic));
+        float2 f = __ffma2_rn(n, f2(-1.0f), qh);                         // qh - n, exact
+        f = __ffma2_rn(tail, f2(-1.0f), f);                              // |f| <= 0.5005
+        fr[i] = f;
+        e[i] = make_float2(ex2_approx(f.x), ex2_approx(f.y));            // 2^f in [0.7, 1.42]
+        nb[2 * i] = __float_as_uint(big.x) << 23;                        // n << 23 (mod 2^32)
+        nb[2 * i + 1] = __float_as_uint(big.y) << 23;
+        qmax = fmaxf(qmax, fmaxf(qh.x, qh.y));
     }
-    const float2 d = __fadd2_rn(e, f2(1.0f));
-    const float2 nd = __ffma2_rn(e, f2(-1.0f), f2(-1.0f));               // -(1 + E)
-    const float2 r0 = make_float2(rcp_approx(d.x), rcp_approx(d.y));
-    const float2 res = __ffma2_rn(nd, r0, f2(1.0f));                     // 1 - d*r0
-    const float2 r = __ffma2_rn(r0, res, r0);                            // one Newton-Raphson step
-    const float2 er = __fmul2_rn(e, r);
-    return make_float2(zh.x < 0.0f ? er.x : r.x, zh.y < 0.0f ? er.y : r.y);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 E = make_float2(__uint_as_float(__float_as_uint(e[i].x) + nb[2 * i]),
+                                     __uint_as_float(__float_as_uint(e[i].y) + nb[2 * i + 1]));
+        const float2 d = __fadd2_rn(E, f2(1.0f));
+        const float2 nd = __ffma2_rn(E, f2(-1.0f), f2(-1.0f));             // -(1 + E)
+        const float2 r0 = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+        const float2 res = __ffma2_rn(nd, r0, f2(1.0f));                   // 1 - d*r0
+        const float2 r = __ffma2_rn(r0, res, r0);                          // one Newton-Raphson step
+        out[2 * i] = r.x;
+        out[2 * i + 1] = r.y;
+    }
+    if (qmax >= 126.5f) {        // some n > 126: sigmoid = 2^-f * 2^-n for those
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int n = (int)nb[2 * i + j] >> 23;
+                if (n > 126) {
+                    const float mf = j ? fr[i].y : fr[i].x;
+                    const float g = ex2_approx(-mf) * 0x1p-126f;        // 2^-f * 2^-126, normal
+                    out[2 * i + j] = g * __uint_as_float((uint32_t)(127 - (n - 126)) << 23);
+                }
+            }
+        }
+    }
 }
 
 // a / b rounded to nearest even, given r = RN(1/b) (b and r normal). q0 = a*r
@@ -253,6 +271,24 @@ __device__ __forceinline__ float row_reduce(float v, float* part, int tpr, int l
     const int w0 = lrow * (tpr >> 5), nw = tpr >> 5;
     float r = part[w0];
     for (int i = 1; i < nw; ++i) r = IS_MAX ? fmaxf(r, part[w0 + i]) : r + part[w0 + i];
+    return r;
+}
+
+// Sum of `a` and max of `b` over the `tpr` threads of one row, in one
+// shared-memory round (one __syncthreads); same rules as row_reduce.
+__device__ __forceinline__ float2 row_reduce_sum_max(float a, float b, float2* part, int tpr, int lrow) {
+    a = warp_sum(a);
+    b = warp_max(b);
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) part[warp] = make_float2(a, b);
+    __syncthreads();
+    const int w0 = lrow * (tpr >> 5), nw = tpr >> 5;
+    float2 r = part[w0];
+    for (int i = 1; i < nw; ++i) {
+        const float2 q = part[w0 + i];
+        r.x += q.x;
+        r.y = fmaxf(r.y, q.y);
+    }
     return r;
 }
 

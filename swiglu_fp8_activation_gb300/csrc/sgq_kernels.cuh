@@ -36,73 +36,69 @@ struct SwigluArgs {
     float alpha, beta, limit;
 };
 
-// Quantise the thread's NV chunks of one row (src = quant source values,
-// zero in chunks past the row end or in rows past M) and store codes and
-// scales. Every thread of the CTA must call it (the per-token format reduces
-// over the row through shared memory).
+// Quantise one chunk (8 source values of row `row`, chunk index c) and store
+// its 8 E4M3 codes and, from the first chunk of its group, the scale. Every
+// lane of the warp must call it for MX and 1x128 (the group amax is a lane
+// shuffle); `store` is false for lanes without a valid chunk (their src is 0).
 //   MX:  code = E8M0 of the 1x32 block's amax; q = E4M3(src * 2^(127-code)),
 //        the scaling being exact (a power of two).
 //   FP8: s = amax / 448 (IEEE fp32 division); q = E4M3(src / s) with the IEEE
 //        fp32 quotient (div_rn from one correctly rounded reciprocal per
-//        group); s = 0 (all-zero group) stores s = 0 and q = 0.
-template <int FMT, int NV>
-__device__ __forceinline__ void quantize_store(const float (&src)[NV][8], int64_t row, bool row_ok,
-                                               int t, int tpr, int lrow, int W, uint8_t* q,
-                                               void* scale, float* part_amax) {
-    const int nchunks = W >> 3;
-    float row_amax = 0.0f;
-    if (FMT == FMT_PT) {
-        float m = 0.0f;
+//        group); s = 0 (all-zero group) stores s = 0 and q = 0. The per-token
+//        format passes its row scale and reciprocal in (pt_s, pt_r).
+template <int FMT>
+__device__ __forceinline__ void quantize_chunk(const float (&src)[8], int64_t row, int c, bool store, int W,
+                                               uint8_t* q, void* scale, float pt_s = 0.0f, float pt_r = 0.0f) {
+    float m = 0.0f;
+    if (FMT != FMT_PT) {
 #pragma unroll
-        for (int v = 0; v < NV; ++v)
-#pragma unroll
-            for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(src[v][k]));
-        row_amax = row_reduce<true>(m, part_amax, tpr, lrow);
+        for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(src[k]));
+        m = group_max<FMT == FMT_MX ? 4 : 16>(m);        // all lanes take part
     }
+    if (!store) return;
+    float tq[8];
+    if (FMT == FMT_MX) {
+        const uint32_t code = mx_scale_code(m);
+        const float is = mx_inv_scale(code);
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
-        const int c = t + v * tpr;
-        float amax;
-        if (FMT == FMT_PT) {
-            amax = row_amax;
-        } else {
-            float m = 0.0f;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(src[v][k]));
-            amax = group_max<FMT == FMT_MX ? 4 : 16>(m);   // all lanes take part
+        for (int k = 0; k < 8; k += 2) {
+            const float2 t = __fmul2_rn(make_float2(src[k], src[k + 1]), f2(is));
+            tq[k] = t.x;
+            tq[k + 1] = t.y;
         }
-        if (!row_ok || c >= nchunks) continue;
-        float tq[8];
-        if (FMT == FMT_MX) {
-            const uint32_t code = mx_scale_code(amax);
-            const float is = mx_inv_scale(code);
+        if ((c & 3) == 0) static_cast<uint8_t*>(scale)[row * (W >> 5) + (c >> 2)] = (uint8_t)code;
+    } else {
+        const float s = FMT == FMT_PT ? pt_s : __fdiv_rn(m, 448.0f);
+        if (s >= 0x1p-126f) {
+            const float r = FMT == FMT_PT ? pt_r : __frcp_rn(s);   // once per group, then one FMA pair per element
 #pragma unroll
-            for (int k = 0; k < 8; ++k) tq[k] = src[v][k] * is;
-            if ((c & 3) == 0) static_cast<uint8_t*>(scale)[row * (W >> 5) + (c >> 2)] = (uint8_t)code;
+            for (int k = 0; k < 8; ++k) tq[k] = div_rn(src[k], s, r);
         } else {
-            const float s = __fdiv_rn(amax, 448.0f);
-            if (s >= 0x1p-126f) {
-                const float r = __frcp_rn(s);   // once per group, then one FMA pair per element
 #pragma unroll
-                for (int k = 0; k < 8; ++k) tq[k] = div_rn(src[v][k], s, r);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) tq[k] = (s == 0.0f) ? 0.0f : __fdiv_rn(src[v][k], s);
-            }
-            if (FMT == FMT_B128 && (c & 15) == 0) static_cast<float*>(scale)[row * (W >> 7) + (c >> 4)] = s;
-            if (FMT == FMT_PT && c == 0) static_cast<float*>(scale)[row] = s;
+            for (int k = 0; k < 8; ++k) tq[k] = (s == 0.0f) ? 0.0f : __fdiv_rn(src[k], s);
         }
-        const uint2 packed = make_uint2(f32x4_to_e4m3x4(tq[0], tq[1], tq[2], tq[3]),
-                                        f32x4_to_e4m3x4(tq[4], tq[5], tq[6], tq[7]));
-        st8(q + row * W + (int64_t)c * 8, packed);
+        if (FMT == FMT_B128 && (c & 15) == 0) static_cast<float*>(scale)[row * (W >> 7) + (c >> 4)] = s;
+        if (FMT == FMT_PT && c == 0) static_cast<float*>(scale)[row] = s;
     }
+    const uint2 packed = make_uint2(f32x4_to_e4m3x4(tq[0], tq[1], tq[2], tq[3]),
+                                    f32x4_to_e4m3x4(tq[4], tq[5], tq[6], tq[7]));
+    st8(q + row * W + (int64_t)c * 8, packed);
+}
+
+// Per-token scale and its reciprocal from the row amax (one per row).
+__device__ __forceinline__ float2 per_token_scale(float row_amax) {
+    const float s = __fdiv_rn(row_amax, 448.0f);
+    return make_float2(s, s >= 0x1p-126f ? __frcp_rn(s) : 0.0f);
 }
 
 // Residual add + RMSNorm + quantisation. One row per `tpr` threads.
-template <int FMT, int NV>
+// y is formed as inv * (h * w'), w' = 1 + w or w: the per-token format then
+// needs no second reduction, since inv > 0 and rounding is monotone, so
+// RN(inv * max|h w'|) is exactly the largest |y| (and its bf16 rounding the
+// largest bf16 |y|); the max of |h w'| travels with the sum of squares.
+template <int FMT, int NV, bool HAS_RES>
 __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
-    __shared__ float part_ss[32];
-    __shared__ float part_amax[32];
+    __shared__ float2 part[32];
     const int tpr = a.tpr;
     const int lrow = threadIdx.x / tpr;
     const int t = threadIdx.x - lrow * tpr;
@@ -119,81 +115,131 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
         const int c = t + v * tpr;
         const bool ok = row_ok && c < nchunks;
         xv[v] = ok ? ld_once(a.x + base + (int64_t)c * 8) : make_uint4(0, 0, 0, 0);
-        rv[v] = (ok && a.r_in) ? ld_coherent(a.r_in + base + (int64_t)c * 8) : make_uint4(0, 0, 0, 0);
+        if (HAS_RES) rv[v] = ok ? ld_coherent(a.r_in + base + (int64_t)c * 8) : make_uint4(0, 0, 0, 0);
         wv[v] = ok ? ld_shared_by_rows(a.w + (int64_t)c * 8) : make_uint4(0, 0, 0, 0);
     }
     pdl_trigger();
 
-    // 2. h = x + r in fp32; write the updated residual; partial sum of squares
-    float h[NV][8];
-    float ss = 0.0f;
+    // 2. h = x + r in fp32; write the updated residual; z = h * w'; partial
+    //    sum of squares (and max |z| for the per-token format)
+    const bool gemma = (a.flags & F_GEMMA) != 0, from32 = (a.flags & F_FROM_FP32) != 0;
+    float z[NV][8];
+    float ss = 0.0f, zmax = 0.0f;
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
         const int c = t + v * tpr;
-        bf16x8_to_f32(xv[v], h[v]);
-        if (a.r_in) {
+        float h[8], wf[8];
+        bf16x8_to_f32(xv[v], h);
+        if (HAS_RES) {
             float rf[8];
             bf16x8_to_f32(rv[v], rf);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) h[v][k] += rf[k];
+            for (int k = 0; k < 8; ++k) h[k] += rf[k];
+            if (a.r_out && row_ok && c < nchunks) st16(a.r_out + base + (int64_t)c * 8, f32x8_to_bf16x8(h));
         }
+        bf16x8_to_f32(wv[v], wf);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) ss = fmaf(h[v][k], h[v][k], ss);
-        if (a.r_out && row_ok && c < nchunks) st16(a.r_out + base + (int64_t)c * 8, f32x8_to_bf16x8(h[v]));
+        for (int k = 0; k < 8; ++k) {
+            ss = fmaf(h[k], h[k], ss);
+            z[v][k] = h[k] * (gemma ? 1.0f + wf[k] : wf[k]);
+            if (FMT == FMT_PT) zmax = fmaxf(zmax, fabsf(z[v][k]));
+        }
     }
 
     // 3. inv = 1/sqrt(mean(h^2) + eps), each step correctly rounded
-    ss = row_reduce<false>(ss, part_ss, tpr, lrow);
+    float row_zmax = 0.0f;
+    if (FMT == FMT_PT) {
+        const float2 r = row_reduce_sum_max(ss, zmax, part, tpr, lrow);
+        ss = r.x;
+        row_zmax = r.y;
+    } else {
+        ss = row_reduce<false>(ss, reinterpret_cast<float*>(part), tpr, lrow);
+    }
     const float inv = __frsqrt_rn(__fdiv_rn(ss, (float)H) + a.eps);
 
-    // 4. y = h * inv * (1 + w) or h * inv * w; bf16 copy; quant source
-    const bool gemma = (a.flags & F_GEMMA) != 0, from32 = (a.flags & F_FROM_FP32) != 0;
-    float src[NV][8];
+    // 4. y = inv * z; bf16 copy; quant source; quantise (MX and 1x128 chunk by
+    //    chunk; per-token after the whole row, with the row scale from ymax)
+    float2 pt = make_float2(0.0f, 0.0f);
+    if (FMT == FMT_PT) {
+        const float ymax = inv * row_zmax;                     // = max |y| exactly
+        pt = per_token_scale(from32 ? ymax : round_bf16(ymax));
+    }
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
         const int c = t + v * tpr;
-        if (!(row_ok && c < nchunks)) {
+        const bool ok = row_ok && c < nchunks;
+        float y[8], src[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) src[v][k] = 0.0f;
-            continue;
-        }
-        float wf[8], y[8];
-        bf16x8_to_f32(wv[v], wf);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) y[k] = h[v][k] * inv * (gemma ? 1.0f + wf[k] : wf[k]);
+        for (int k = 0; k < 8; ++k) y[k] = ok ? inv * z[v][k] : 0.0f;
         const uint4 yb = f32x8_to_bf16x8(y);
-        if (a.normed) st16(a.normed + base + (int64_t)c * 8, yb);
+        if (a.normed && ok) st16(a.normed + base + (int64_t)c * 8, yb);
         if (from32) {
 #pragma unroll
-            for (int k = 0; k < 8; ++k) src[v][k] = y[k];
+            for (int k = 0; k < 8; ++k) src[k] = y[k];
         } else {
-            bf16x8_to_f32(yb, src[v]);
+            bf16x8_to_f32(yb, src);
         }
+        quantize_chunk<FMT>(src, row, c, ok, H, a.q, a.scale, pt.x, pt.y);
     }
-
-    // 5. group amax, scales, E4M3 codes
-    quantize_store<FMT, NV>(src, row, row_ok, t, tpr, lrow, H, a.q, a.scale, part_amax);
 }
 
-// The activation of two (gate, up) pairs, in fp32:
+// The activation of one chunk of 8 (gate, up) values, in fp32:
 //   OAI:  g' = min(g, limit), u' = min(max(u, -limit), limit),
-//         a = (g' * sigmoid(alpha * g')) * (u' + beta); alpha * g' is carried
-//         with its exact FMA residual into the sigmoid;
+//         a = (g' * sigmoid(alpha * g')) * (u' + beta). The sigmoid's
+//         argument is alpha * clamp(g', glo, ghi), with [glo, ghi] the g'
+//         that alpha maps into [kSigLo, kSigHi] (where the clamp acts, the
+//         sigmoid of the clamped argument already equals the true one in
+//         fp32: 0 or 1), carried with its exact FMA residual;
 //   SiLU: a = (g * sigmoid(g)) * u, the first factor rounded to bf16 when
 //         round_silu is set.
 template <int ACT>
-__device__ __forceinline__ float2 activation2(float2 g, float2 u, float alpha, float beta, float limit,
-                                              bool round_silu) {
+__device__ __forceinline__ void activation8(const float (&g)[8], const float (&u)[8], float alpha, float beta,
+                                            float limit, float glo, float ghi, bool round_silu, float (&a)[8]) {
+    float sg[8];
     if (ACT == ACT_OAI) {
-        const float2 gc = make_float2(fminf(g.x, limit), fminf(g.y, limit));
-        const float2 uc = make_float2(fminf(fmaxf(u.x, -limit), limit), fminf(fmaxf(u.y, -limit), limit));
-        const float2 zh = __fmul2_rn(f2(alpha), gc);
-        const float2 zl = __ffma2_rn(f2(alpha), gc, __fmul2_rn(zh, f2(-1.0f)));
-        return __fmul2_rn(__fmul2_rn(gc, sigmoid2(zh, zl)), __fadd2_rn(uc, f2(beta)));
+        float gc[8], zh[8], nzl[8];
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+            gc[k] = fminf(g[k], limit);
+            gc[k + 1] = fminf(g[k + 1], limit);
+            const float2 gs = make_float2(fmaxf(fminf(gc[k], ghi), glo), fmaxf(fminf(gc[k + 1], ghi), glo));
+            const float2 z = __fmul2_rn(f2(alpha), gs);
+            const float2 nz = __ffma2_rn(f2(-alpha), gs, z);               // -(residual of alpha * gs)
+            zh[k] = z.x;
+            zh[k + 1] = z.y;
+            nzl[k] = nz.x;
+            nzl[k + 1] = nz.y;
+        }
+        sigmoid8<true>(zh, nzl, sg);
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+            const float2 uc = make_float2(fminf(fmaxf(u[k], -limit), limit), fminf(fmaxf(u[k + 1], -limit), limit));
+            const float2 r = __fmul2_rn(__fmul2_rn(make_float2(gc[k], gc[k + 1]), make_float2(sg[k], sg[k + 1])),
+                                        __fadd2_rn(uc, f2(beta)));
+            a[k] = r.x;
+            a[k + 1] = r.y;
+        }
+    } else {
+        float zc[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) zc[k] = fmaxf(fminf(g[k], kSigHi), kSigLo);
+        sigmoid8<false>(zc, zc, sg);
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+            float2 s = __fmul2_rn(make_float2(g[k], g[k + 1]), make_float2(sg[k], sg[k + 1]));
+            if (round_silu) s = make_float2(round_bf16(s.x), round_bf16(s.y));
+            const float2 r = __fmul2_rn(s, make_float2(u[k], u[k + 1]));
+            a[k] = r.x;
+            a[k + 1] = r.y;
+        }
     }
-    float2 s = __fmul2_rn(g, sigmoid2(g, f2(0.0f)));
-    if (round_silu) s = make_float2(round_bf16(s.x), round_bf16(s.y));
-    return __fmul2_rn(s, u);
+}
+
+// The range of g' that alpha maps into [kSigLo, kSigHi] (everything for alpha = 0).
+__device__ __forceinline__ float2 oai_gate_range(float alpha) {
+    if (alpha > 0.0f) return make_float2(kSigLo / alpha, kSigHi / alpha);
+    if (alpha < 0.0f) return make_float2(kSigHi / alpha, kSigLo / alpha);
+    return make_float2(-INFINITY, INFINITY);
 }
 
 // SwiGLU + quantisation. One row per `tpr` threads.
@@ -219,30 +265,45 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
     }
     pdl_trigger();
 
-    const bool round_silu = (a.flags & F_ACT_BF16) != 0;
-    float src[NV][8];
+    const bool round_silu = (a.flags & F_ACT_BF16) != 0, from32 = (a.flags & F_FROM_FP32) != 0;
+    const float2 gr = oai_gate_range(a.alpha);
+    if (FMT != FMT_PT) {               // MX and 1x128: chunk by chunk
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
-        float g[8], u[8];
-        bf16x8_to_f32(gv[v], g);
-        bf16x8_to_f32(uv[v], u);
+        for (int v = 0; v < NV; ++v) {
+            const int c = t + v * tpr;
+            float g[8], u[8], src[8];
+            bf16x8_to_f32(gv[v], g);
+            bf16x8_to_f32(uv[v], u);
+            activation8<ACT>(g, u, a.alpha, a.beta, a.limit, gr.x, gr.y, round_silu, src);
+            if (!from32) {
 #pragma unroll
-        for (int k = 0; k < 8; k += 2) {
-            const float2 act = activation2<ACT>(make_float2(g[k], g[k + 1]), make_float2(u[k], u[k + 1]),
-                                                a.alpha, a.beta, a.limit, round_silu);
-            src[v][k] = act.x;
-            src[v][k + 1] = act.y;
+                for (int k = 0; k < 8; ++k) src[k] = round_bf16(src[k]);
+            }
+            // chunks past the row end loaded zeros, and every activation of 0 and 0 is 0
+            quantize_chunk<FMT>(src, row, c, row_ok && c < nchunks, I, a.q, a.scale);
+        }
+    } else {                           // per-token: the whole row, then its amax
+        float src[NV][8];
+        float m = 0.0f;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            float g[8], u[8];
+            bf16x8_to_f32(gv[v], g);
+            bf16x8_to_f32(uv[v], u);
+            activation8<ACT>(g, u, a.alpha, a.beta, a.limit, gr.x, gr.y, round_silu, src[v]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if (!from32) src[v][k] = round_bf16(src[v][k]);
+                m = fmaxf(m, fabsf(src[v][k]));
+            }
+        }
+        const float2 pt = per_token_scale(row_reduce<true>(m, part_amax, tpr, lrow));
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const int c = t + v * tpr;
+            quantize_chunk<FMT>(src[v], row, c, row_ok && c < nchunks, I, a.q, a.scale, pt.x, pt.y);
         }
     }
-    if (!(a.flags & F_FROM_FP32)) {    // quantise the bf16 rounding of the activation
-#pragma unroll
-        for (int v = 0; v < NV; ++v)
-#pragma unroll
-            for (int k = 0; k < 8; ++k) src[v][k] = round_bf16(src[v][k]);
-    }
-    // chunks past the row end loaded zeros, and every activation of 0 and 0 is 0
-
-    quantize_store<FMT, NV>(src, row, row_ok, t, tpr, lrow, I, a.q, a.scale, part_amax);
 }
 
 }  // namespace sgq

@@ -1,5 +1,5 @@
-// Test-only kernels around the library's device arithmetic (sigmoid2,
-// activation2, div_rn),
+// Test-only kernels around the library's device arithmetic (sigmoid8,
+// activation8, div_rn),
 // compiled by tests/test_gpu_device_math.py and compared there against fp64
 // and against CUDA's own correctly rounded division.
 #include <cuda_runtime.h>
@@ -8,25 +8,29 @@
 
 namespace {
 
+// n must be a multiple of 8.
 __global__ void sigmoid_kernel(const float* z, float* out, int n) {
-    const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
-    if (i + 1 < n) {
-        const float2 r = sgq::sigmoid2(make_float2(z[i], z[i + 1]), make_float2(0.0f, 0.0f));
-        out[i] = r.x;
-        out[i + 1] = r.y;
-    } else if (i < n) {
-        out[i] = sgq::sigmoid2(make_float2(z[i], 0.0f), make_float2(0.0f, 0.0f)).x;
+    const int i = 8 * (blockIdx.x * blockDim.x + threadIdx.x);
+    if (i < n) {
+        float zz[8], r[8];
+        for (int k = 0; k < 8; ++k) zz[k] = fmaxf(fminf(z[i + k], sgq::kSigHi), sgq::kSigLo);
+        sgq::sigmoid8<false>(zz, zz, r);
+        for (int k = 0; k < 8; ++k) out[i + k] = r[k];
     }
 }
 
-// OAI activation of (g, u) pairs through the kernels' own activation2().
+// OAI activation through the kernels' own activation8(); n a multiple of 8.
 __global__ void oai_kernel(const float* g, const float* u, float* out, int n, float alpha, float beta, float limit) {
-    const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
-    if (i + 1 < n) {
-        const float2 r = sgq::activation2<sgq::ACT_OAI>(make_float2(g[i], g[i + 1]), make_float2(u[i], u[i + 1]),
-                                                    alpha, beta, limit, false);
-        out[i] = r.x;
-        out[i + 1] = r.y;
+    const int i = 8 * (blockIdx.x * blockDim.x + threadIdx.x);
+    if (i < n) {
+        float gg[8], uu[8], r[8];
+        for (int k = 0; k < 8; ++k) {
+            gg[k] = g[i + k];
+            uu[k] = u[i + k];
+        }
+        const float2 gr = sgq::oai_gate_range(alpha);
+        sgq::activation8<sgq::ACT_OAI>(gg, uu, alpha, beta, limit, gr.x, gr.y, false, r);
+        for (int k = 0; k < 8; ++k) out[i + k] = r[k];
     }
 }
 
@@ -42,12 +46,12 @@ __global__ void div_kernel(const float* a, const float* b, float* q_fast, float*
 }  // namespace
 
 extern "C" int run_sigmoid(const float* z, float* out, int n) {
-    sigmoid_kernel<<<(n / 2 + 256) / 256, 256>>>(z, out, n);
+    sigmoid_kernel<<<(n / 8 + 256) / 256, 256>>>(z, out, n);
     return (int)cudaDeviceSynchronize();
 }
 
 extern "C" int run_oai(const float* g, const float* u, float* out, int n, float alpha, float beta, float limit) {
-    oai_kernel<<<(n / 2 + 256) / 256, 256>>>(g, u, out, n, alpha, beta, limit);
+    oai_kernel<<<(n / 8 + 256) / 256, 256>>>(g, u, out, n, alpha, beta, limit);
     return (int)cudaDeviceSynchronize();
 }
 

@@ -1,8 +1,8 @@
 """The two arithmetic shortcuts of the kernels, checked on the GPU:
 
-* sigmoid2() (split exponent, fitted 2^x polynomial, refined reciprocal)
+* sigmoid8() (split exponent, fitted 2^x polynomial, refined reciprocal)
   against fp64 over |z| <= 130, within 2^-22 relative;
-* activation2() (the OAI SwiGLU of the kernels) against fp64, within 2^-21
+* activation8() (the OAI SwiGLU of the kernels) against fp64, within 2^-21
   relative, including an element whose exact value lies 3.1e-7 relative
   above an E4M3 rounding boundary;
 * div_rn() (one reciprocal per group + Markstein's FMA correction) against
@@ -43,6 +43,7 @@ def _p(t):
 def test_sigmoid_accuracy(devlib):
     z = np.concatenate([np.linspace(-130, 130, 2_000_001), np.array([0.0, -0.0, 1e-30, -1e-30, 87.3, -87.3, 1e30, -1e30]),
                         np.random.default_rng(0).standard_normal(200_000) * 8]).astype(np.float32)
+    z = np.concatenate([z, np.zeros((-z.size) % 8, np.float32)])      # whole chunks of 8
     zt = torch.from_numpy(z).cuda()
     out = torch.empty_like(zt)
     assert devlib.run_sigmoid(_p(zt), _p(out), z.size) == 0
