@@ -66,6 +66,38 @@ __device__ __forceinline__ uint4 ld_shared_by_rows(const void* p) {
     return __ldg(reinterpret_cast<const uint4*>(p));
 }
 
+// 16-byte asynchronous copy from global to shared memory, caching in L2 only
+// (with a 256-byte L2 prefetch). src_bytes = 0 writes zeros and reads nothing.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Wait until at most N of this thread's committed copy groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// With NV groups committed in order, wait for group v (v is a constant after unrolling).
+template <int NV>
+__device__ __forceinline__ void cp_async_wait_group_of(int v) {
+    const int pending = NV - 1 - v;
+    if (pending >= 3) cp_async_wait<3>();
+    else if (pending == 2) cp_async_wait<2>();
+    else if (pending == 1) cp_async_wait<1>();
+    else cp_async_wait<0>();
+}
+
+__device__ __forceinline__ uint4 ld_smem16(const uint4* p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"((uint32_t)__cvta_generic_to_shared(p)));
+    return v;
+}
+
 __device__ __forceinline__ void st16(void* p, uint4 v) {
     asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                  "r"(v.w)

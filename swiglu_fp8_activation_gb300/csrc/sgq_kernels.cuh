@@ -242,11 +242,20 @@ __device__ __forceinline__ float2 oai_gate_range(float alpha) {
     return make_float2(-INFINITY, INFINITY);
 }
 
-// SwiGLU + quantisation. One row per `tpr` threads.
+// Bytes of dynamic shared memory the SwiGLU kernel stages its loads in.
+__host__ __device__ constexpr int swiglu_stage_bytes(int nv, int threads) { return nv * 2 * threads * 16; }
+
+// SwiGLU + quantisation. One row per `tpr` threads. Each thread's gate and
+// up chunks are copied asynchronously into its own shared-memory slots
+// (stage[2v][thread], stage[2v+1][thread]), one commit group per chunk, so
+// the whole row is in flight without holding registers and chunk v is
+// processed as soon as its own group has landed.
 template <int FMT, int NV, int ACT>
 __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs a) {
+    extern __shared__ uint4 stage[];
     __shared__ float part_amax[32];
     const int tpr = a.tpr;
+    const int nt = blockDim.x;
     const int lrow = threadIdx.x / tpr;
     const int t = threadIdx.x - lrow * tpr;
     const int64_t row = (int64_t)blockIdx.x * a.rpc + lrow;
@@ -255,25 +264,28 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
     const uint16_t* grow = a.gu + row * (int64_t)(2 * I);
 
     pdl_wait();
-    uint4 gv[NV], uv[NV];
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
         const int c = t + v * tpr;
-        const bool ok = row_ok && c < nchunks;
-        gv[v] = ok ? ld_once(grow + (int64_t)c * 8) : make_uint4(0, 0, 0, 0);
-        uv[v] = ok ? ld_once(grow + I + (int64_t)c * 8) : make_uint4(0, 0, 0, 0);
+        const bool ok = row_ok && c < nchunks;   // else zero-fill, reading nothing
+        cp_async16(&stage[(2 * v) * nt + threadIdx.x], ok ? (const void*)(grow + (int64_t)c * 8) : (const void*)a.gu,
+                   ok ? 16 : 0);
+        cp_async16(&stage[(2 * v + 1) * nt + threadIdx.x],
+                   ok ? (const void*)(grow + I + (int64_t)c * 8) : (const void*)a.gu, ok ? 16 : 0);
+        cp_async_commit();
     }
     pdl_trigger();
 
     const bool round_silu = (a.flags & F_ACT_BF16) != 0, from32 = (a.flags & F_FROM_FP32) != 0;
     const float2 gr = oai_gate_range(a.alpha);
-    if (FMT != FMT_PT) {               // MX and 1x128: chunk by chunk
+    if (FMT != FMT_PT) {               // MX and 1x128: chunk by chunk, as each lands
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
             const int c = t + v * tpr;
             float g[8], u[8], src[8];
-            bf16x8_to_f32(gv[v], g);
-            bf16x8_to_f32(uv[v], u);
+            cp_async_wait_group_of<NV>(v);
+            bf16x8_to_f32(ld_smem16(&stage[(2 * v) * nt + threadIdx.x]), g);
+            bf16x8_to_f32(ld_smem16(&stage[(2 * v + 1) * nt + threadIdx.x]), u);
             activation8<ACT>(g, u, a.alpha, a.beta, a.limit, gr.x, gr.y, round_silu, src);
             if (!from32) {
 #pragma unroll
@@ -288,8 +300,9 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
             float g[8], u[8];
-            bf16x8_to_f32(gv[v], g);
-            bf16x8_to_f32(uv[v], u);
+            cp_async_wait_group_of<NV>(v);
+            bf16x8_to_f32(ld_smem16(&stage[(2 * v) * nt + threadIdx.x]), g);
+            bf16x8_to_f32(ld_smem16(&stage[(2 * v + 1) * nt + threadIdx.x]), u);
             activation8<ACT>(g, u, a.alpha, a.beta, a.limit, gr.x, gr.y, round_silu, src[v]);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {

@@ -25,11 +25,16 @@ bool plan_rows(int64_t M, int W, int sm_count, Plan* p);
 // grid may begin launching while the preceding kernel on the stream finishes
 // (the kernels wait in pdl_wait() before touching memory).
 template <typename Args>
-cudaError_t launch_pdl(void (*k)(const Args), const Plan& p, const Args& a, cudaStream_t stream) {
+cudaError_t launch_pdl(void (*k)(const Args), const Plan& p, const Args& a, cudaStream_t stream,
+                       int dynamic_smem = 0) {
+    if (dynamic_smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dynamic_smem);
+        if (e != cudaSuccess) return e;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
     cfg.blockDim = dim3((unsigned)(p.rpc * p.tpr));
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = (size_t)dynamic_smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

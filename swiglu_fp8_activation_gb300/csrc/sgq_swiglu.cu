@@ -24,7 +24,7 @@ SwigluKernel pick_fmt(int fmt, int nv) {
 
 cudaError_t launch_swiglu(int fmt, const Plan& p, const SwigluArgs& a, cudaStream_t stream) {
     SwigluKernel k = a.act == ACT_OAI ? pick_fmt<ACT_OAI>(fmt, p.nv) : pick_fmt<ACT_SILU>(fmt, p.nv);
-    return launch_pdl(k, p, a, stream);
+    return launch_pdl(k, p, a, stream, swiglu_stage_bytes(p.nv, p.rpc * p.tpr));
 }
 
 }  // namespace sgq
