@@ -160,6 +160,10 @@ const char* sgq_status_string(int status);
 /* SGQ_ABI_VERSION of the loaded library. */
 int sgq_abi_version(void);
 
+/* The CUDA error text of the calling thread's most recent call that returned
+ * SGQ_ERR_LAUNCH ("no launch error" if there was none). Static storage. */
+const char* sgq_launch_error(void);
+
 #ifdef __cplusplus
 }
 #endif

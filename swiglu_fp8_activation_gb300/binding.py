@@ -54,6 +54,8 @@ def library() -> C.CDLL:
         L.sgq_status_string.argtypes = [C.c_int]
         L.sgq_abi_version.restype = C.c_int
         L.sgq_abi_version.argtypes = []
+        L.sgq_launch_error.restype = C.c_char_p
+        L.sgq_launch_error.argtypes = []
         _lib = L
     return _lib
 
@@ -64,7 +66,8 @@ def status_string(status: int) -> str:
 
 def _check(status: int, what: str):
     if status != 0:
-        raise SgqError(f"{what}: {status_string(status)} (status {status})", status)
+        detail = f": {library().sgq_launch_error().decode()}" if status == 4 else ""
+        raise SgqError(f"{what}: {status_string(status)} (status {status}){detail}", status)
 
 
 def _ptr(t: torch.Tensor | None):

@@ -50,6 +50,12 @@ bool plan_rows(int64_t M, int W, int sm_count, Plan* p) {
     return p->grid <= 0x7FFFFFFF;
 }
 
+namespace {
+thread_local cudaError_t last_launch_error = cudaSuccess;
+}  // namespace
+
+void note_launch_error(cudaError_t e) { last_launch_error = e; }
+
 }  // namespace sgq
 
 namespace {
@@ -101,6 +107,10 @@ extern "C" {
 
 int sgq_abi_version(void) { return SGQ_ABI_VERSION; }
 
+const char* sgq_launch_error(void) {
+    return sgq::last_launch_error == cudaSuccess ? "no launch error" : cudaGetErrorString(sgq::last_launch_error);
+}
+
 const char* sgq_status_string(int status) {
     switch (status) {
         case SGQ_OK: return "ok";
@@ -149,7 +159,11 @@ int rmsnorm_add_quant(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, 
     a.rpc = plan.rpc;
     a.eps = eps;
     a.flags = flags;
-    if (sgq::launch_norm(fmt, plan, a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return SGQ_ERR_LAUNCH;
+    const cudaError_t e = sgq::launch_norm(fmt, plan, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        sgq::note_launch_error(e);
+        return SGQ_ERR_LAUNCH;
+    }
     return SGQ_OK;
 }
 
@@ -186,7 +200,11 @@ int swiglu_quant(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float a
     a.alpha = alpha;
     a.beta = beta;
     a.limit = limit;
-    if (sgq::launch_swiglu(fmt, plan, a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return SGQ_ERR_LAUNCH;
+    const cudaError_t e = sgq::launch_swiglu(fmt, plan, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        sgq::note_launch_error(e);
+        return SGQ_ERR_LAUNCH;
+    }
     return SGQ_OK;
 }
 

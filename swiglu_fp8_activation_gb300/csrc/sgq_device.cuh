@@ -4,9 +4,11 @@
 // One "row engine" serves both operations. A row of W elements is split into
 // 16-byte chunks of 8 bf16 values; `tpr` threads (a multiple of 32) own one
 // row, and thread t owns chunks t, t + tpr, ..., t + (NV-1)*tpr, so every
-// warp-wide load is 512 contiguous bytes. All NV chunks of a thread are loaded
-// before any arithmetic (the whole row sits in registers: no second read of
-// global memory and no shared-memory staging of the row). Reductions:
+// warp-wide copy is 512 contiguous bytes. All NV chunks of a thread are copied
+// asynchronously into its own shared-memory slots before any arithmetic (one
+// commit group per chunk), so the whole row is in flight without holding
+// registers, and each chunk is processed as soon as its group has landed; the
+// row is read from global memory once. Reductions:
 //   * sum of squares (RMSNorm) and per-token amax: warp shuffles, then one
 //     shared-memory step across the row's warps;
 //   * 1x32 (MX) amax: the 4 lanes that own one 32-block (2 xor-shuffles);
@@ -42,36 +44,18 @@ constexpr int kTargetCTA = 256;    // threads per CTA when several rows share on
 
 // ----------------------------------------------------------------- memory
 
-// Streaming 16-byte load of data read once by this kernel (x, gate_up):
-// non-coherent path, no L1 allocation, 256-byte L2 prefetch.
-__device__ __forceinline__ uint4 ld_once(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-// 16-byte load through the coherent path (the residual may be updated in place).
-__device__ __forceinline__ uint4 ld_coherent(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-// 16-byte load of data every row reads (the norm weight): cached.
-__device__ __forceinline__ uint4 ld_shared_by_rows(const void* p) {
-    return __ldg(reinterpret_cast<const uint4*>(p));
-}
-
 // 16-byte asynchronous copy from global to shared memory, caching in L2 only
 // (with a 256-byte L2 prefetch). src_bytes = 0 writes zeros and reads nothing.
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
     const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
     asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(src_bytes)
                  : "memory");
+}
+
+// The same, allocating in L1 as well: for data every row of the SM reads (the norm weight).
+__device__ __forceinline__ void cp_async16_cached(void* smem, const void* gmem, int src_bytes) {
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(src_bytes) : "memory");
 }
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }

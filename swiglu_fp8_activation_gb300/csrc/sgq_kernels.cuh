@@ -96,27 +96,43 @@ __device__ __forceinline__ float2 per_token_scale(float row_amax) {
 // needs no second reduction, since inv > 0 and rounding is monotone, so
 // RN(inv * max|h w'|) is exactly the largest |y| (and its bf16 rounding the
 // largest bf16 |y|); the max of |h w'| travels with the sum of squares.
+// Inputs staged per chunk by the norm kernel: x, the residual (if any) and w.
+__host__ __device__ constexpr int norm_stage_inputs(bool has_res) { return has_res ? 3 : 2; }
+__host__ __device__ constexpr int norm_stage_bytes(bool has_res, int nv, int threads) {
+    return nv * norm_stage_inputs(has_res) * threads * 16;
+}
+
 template <int FMT, int NV, bool HAS_RES>
 __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
+    extern __shared__ uint4 stage[];
     __shared__ float2 part[32];
+    constexpr int NIN = norm_stage_inputs(HAS_RES);
     const int tpr = a.tpr;
+    const int nt = blockDim.x;
     const int lrow = threadIdx.x / tpr;
     const int t = threadIdx.x - lrow * tpr;
     const int64_t row = (int64_t)blockIdx.x * a.rpc + lrow;
     const bool row_ok = row < a.M;
     const int H = a.H, nchunks = H >> 3;
     const int64_t base = row * (int64_t)H;
+    auto slot = [&](int v, int i) { return &stage[(NIN * v + i) * nt + threadIdx.x]; };
 
-    // 1. issue every load of the row (x, r and the weight) before any arithmetic
+    // 1. every load of the row (x, r and the weight) goes out at once, copied
+    //    asynchronously into this thread's shared-memory slots, one commit
+    //    group per chunk. A thread reads back only its own slots, and writes
+    //    the updated residual of a chunk only after that chunk's group has
+    //    landed, so an in-place residual update is safe.
     pdl_wait();
-    uint4 xv[NV], rv[NV], wv[NV];
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
         const int c = t + v * tpr;
-        const bool ok = row_ok && c < nchunks;
-        xv[v] = ok ? ld_once(a.x + base + (int64_t)c * 8) : make_uint4(0, 0, 0, 0);
-        if (HAS_RES) rv[v] = ok ? ld_coherent(a.r_in + base + (int64_t)c * 8) : make_uint4(0, 0, 0, 0);
-        wv[v] = ok ? ld_shared_by_rows(a.w + (int64_t)c * 8) : make_uint4(0, 0, 0, 0);
+        const bool ok = row_ok && c < nchunks;   // else zero-fill, reading nothing
+        const int nb = ok ? 16 : 0;
+        cp_async16(slot(v, 0), ok ? (const void*)(a.x + base + (int64_t)c * 8) : (const void*)a.x, nb);
+        if (HAS_RES)
+            cp_async16(slot(v, 1), ok ? (const void*)(a.r_in + base + (int64_t)c * 8) : (const void*)a.x, nb);
+        cp_async16_cached(slot(v, NIN - 1), ok ? (const void*)(a.w + (int64_t)c * 8) : (const void*)a.x, nb);
+        cp_async_commit();
     }
     pdl_trigger();
 
@@ -129,15 +145,16 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
     for (int v = 0; v < NV; ++v) {
         const int c = t + v * tpr;
         float h[8], wf[8];
-        bf16x8_to_f32(xv[v], h);
+        cp_async_wait_group_of<NV>(v);
+        bf16x8_to_f32(ld_smem16(slot(v, 0)), h);
         if (HAS_RES) {
             float rf[8];
-            bf16x8_to_f32(rv[v], rf);
+            bf16x8_to_f32(ld_smem16(slot(v, 1)), rf);
 #pragma unroll
             for (int k = 0; k < 8; ++k) h[k] += rf[k];
             if (a.r_out && row_ok && c < nchunks) st16(a.r_out + base + (int64_t)c * 8, f32x8_to_bf16x8(h));
         }
-        bf16x8_to_f32(wv[v], wf);
+        bf16x8_to_f32(ld_smem16(slot(v, NIN - 1)), wf);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             ss = fmaf(h[k], h[k], ss);

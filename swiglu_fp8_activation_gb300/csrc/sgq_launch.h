@@ -27,7 +27,9 @@ bool plan_rows(int64_t M, int W, int sm_count, Plan* p);
 template <typename Args>
 cudaError_t launch_pdl(void (*k)(const Args), const Plan& p, const Args& a, cudaStream_t stream,
                        int dynamic_smem = 0) {
-    if (dynamic_smem > 48 * 1024) {
+    // Above 48 KB of static plus dynamic shared memory a kernel must opt in
+    // (static use here is a few hundred bytes).
+    if (dynamic_smem > 40 * 1024) {
         const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dynamic_smem);
         if (e != cudaSuccess) return e;
     }
@@ -46,6 +48,9 @@ cudaError_t launch_pdl(void (*k)(const Args), const Plan& p, const Args& a, cuda
 }
 
 cudaError_t launch_norm(int fmt, const Plan& p, const NormArgs& a, cudaStream_t stream);
+
+// Records the CUDA error of a failed launch for sgq_launch_error() (per thread).
+void note_launch_error(cudaError_t e);
 cudaError_t launch_swiglu(int fmt, const Plan& p, const SwigluArgs& a, cudaStream_t stream);
 
 }  // namespace sgq

@@ -24,7 +24,7 @@ NormKernel pick_fmt(int fmt, int nv) {
 
 cudaError_t launch_norm(int fmt, const Plan& p, const NormArgs& a, cudaStream_t stream) {
     NormKernel k = a.r_in ? pick_fmt<true>(fmt, p.nv) : pick_fmt<false>(fmt, p.nv);
-    return launch_pdl(k, p, a, stream);
+    return launch_pdl(k, p, a, stream, norm_stage_bytes(a.r_in != nullptr, p.nv, p.rpc * p.tpr));
 }
 
 }  // namespace sgq

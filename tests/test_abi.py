@@ -36,7 +36,8 @@ def _header_value(name):
 
 def test_library_exports_every_declared_function(sgq_lib):
     names = _declared_functions()
-    assert set(names) == {"rmsnorm_add_quant", "swiglu_quant", "sgq_status_string", "sgq_abi_version"}
+    assert set(names) == {"rmsnorm_add_quant", "swiglu_quant", "sgq_status_string", "sgq_abi_version",
+                          "sgq_launch_error"}
     for n in names:
         assert hasattr(sgq_lib, n), n
     m = re.search(r"#define SGQ_ABI_VERSION (\d+)", _header())
@@ -52,6 +53,11 @@ def test_enum_and_flag_values_agree():
     assert _header_value("SGQ_F_GEMMA_WEIGHT") == binding.F_GEMMA_WEIGHT == oracle.F_GEMMA
     assert _header_value("SGQ_F_QUANT_FROM_FP32") == binding.F_QUANT_FROM_FP32 == oracle.F_FROM_FP32
     assert _header_value("SGQ_F_ACT_ROUND_BF16") == binding.F_ACT_ROUND_BF16 == oracle.F_ACT_ROUND_BF16
+
+
+def test_launch_error_text_without_a_failure(sgq_lib):
+    sgq_lib.sgq_launch_error.restype = C.c_char_p
+    assert sgq_lib.sgq_launch_error() == b"no launch error"
 
 
 def test_status_strings(sgq_lib):
