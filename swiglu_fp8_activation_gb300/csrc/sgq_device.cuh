@@ -82,14 +82,27 @@ __device__ __forceinline__ uint4 ld_smem16(const uint4* p) {
     return v;
 }
 
-__device__ __forceinline__ void st16(void* p, uint4 v) {
-    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w)
-                 : "memory");
+// Global stores of kernel outputs, predicated in PTX (no branch around them).
+// Nothing in these kernels reads an output back, so no memory clobber.
+__device__ __forceinline__ void st16_if(void* p, uint4 v, bool pred) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %5, 0;\n\t@p st.global.v4.u32 [%0], {%1,%2,%3,%4};\n}" ::"l"(p),
+        "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"((int)pred));
 }
 
-__device__ __forceinline__ void st8(void* p, uint2 v) {
-    asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+__device__ __forceinline__ void st8_if(void* p, uint2 v, bool pred) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %3, 0;\n\t@p st.global.v2.u32 [%0], {%1,%2};\n}" ::"l"(p),
+                 "r"(v.x), "r"(v.y), "r"((int)pred));
+}
+
+__device__ __forceinline__ void st_u8_if(void* p, uint32_t v, bool pred) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t@p st.global.u8 [%0], %1;\n}" ::"l"(p), "r"(v),
+                 "r"((int)pred));
+}
+
+__device__ __forceinline__ void st_f32_if(void* p, float v, bool pred) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t@p st.global.f32 [%0], %1;\n}" ::"l"(p), "f"(v),
+                 "r"((int)pred));
 }
 
 // ------------------------------------------------------------ conversions

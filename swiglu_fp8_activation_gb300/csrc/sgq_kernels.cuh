@@ -55,7 +55,6 @@ __device__ __forceinline__ void quantize_chunk(const float (&src)[8], int64_t ro
         for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(src[k]));
         m = group_max<FMT == FMT_MX ? 4 : 16>(m);        // all lanes take part
     }
-    if (!store) return;
     float tq[8];
     if (FMT == FMT_MX) {
         const uint32_t code = mx_scale_code(m);
@@ -66,23 +65,26 @@ __device__ __forceinline__ void quantize_chunk(const float (&src)[8], int64_t ro
             tq[k] = t.x;
             tq[k + 1] = t.y;
         }
-        if ((c & 3) == 0) static_cast<uint8_t*>(scale)[row * (W >> 5) + (c >> 2)] = (uint8_t)code;
+        st_u8_if(static_cast<uint8_t*>(scale) + row * (W >> 5) + (c >> 2), code, store && (c & 3) == 0);
     } else {
-        const float s = FMT == FMT_PT ? pt_s : __fdiv_rn(m, 448.0f);
-        if (s >= 0x1p-126f) {
-            const float r = FMT == FMT_PT ? pt_r : __frcp_rn(s);   // once per group, then one FMA pair per element
+        float s = pt_s, r = pt_r;
+        if (FMT == FMT_B128) {
+            s = __fdiv_rn(m, 448.0f);
+            r = s >= 0x1p-126f ? __frcp_rn(s) : 0.0f;   // once per group
+        }
+        if (s >= 0x1p-126f || s == 0.0f) {              // r = 0 for s = 0: every code is 0
 #pragma unroll
             for (int k = 0; k < 8; ++k) tq[k] = div_rn(src[k], s, r);
-        } else {
+        } else {                                         // subnormal scale (amax < 5.3e-36)
 #pragma unroll
-            for (int k = 0; k < 8; ++k) tq[k] = (s == 0.0f) ? 0.0f : __fdiv_rn(src[k], s);
+            for (int k = 0; k < 8; ++k) tq[k] = __fdiv_rn(src[k], s);
         }
-        if (FMT == FMT_B128 && (c & 15) == 0) static_cast<float*>(scale)[row * (W >> 7) + (c >> 4)] = s;
-        if (FMT == FMT_PT && c == 0) static_cast<float*>(scale)[row] = s;
+        if (FMT == FMT_B128) st_f32_if(static_cast<float*>(scale) + row * (W >> 7) + (c >> 4), s, store && (c & 15) == 0);
+        else st_f32_if(static_cast<float*>(scale) + row, s, store && c == 0);
     }
     const uint2 packed = make_uint2(f32x4_to_e4m3x4(tq[0], tq[1], tq[2], tq[3]),
                                     f32x4_to_e4m3x4(tq[4], tq[5], tq[6], tq[7]));
-    st8(q + row * W + (int64_t)c * 8, packed);
+    st8_if(q + row * W + (int64_t)c * 8, packed, store);
 }
 
 // Per-token scale and its reciprocal from the row amax (one per row).
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
             bf16x8_to_f32(ld_smem16(slot(v, 1)), rf);
 #pragma unroll
             for (int k = 0; k < 8; ++k) h[k] += rf[k];
-            if (a.r_out && row_ok && c < nchunks) st16(a.r_out + base + (int64_t)c * 8, f32x8_to_bf16x8(h));
+            if (a.r_out) st16_if(a.r_out + base + (int64_t)c * 8, f32x8_to_bf16x8(h), row_ok && c < nchunks);
         }
         bf16x8_to_f32(ld_smem16(slot(v, NIN - 1)), wf);
 #pragma unroll
@@ -187,9 +189,9 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
         const bool ok = row_ok && c < nchunks;
         float y[8], src[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) y[k] = ok ? inv * z[v][k] : 0.0f;
+        for (int k = 0; k < 8; ++k) y[k] = inv * z[v][k];     // z = 0 past the row end (zero-filled copies)
         const uint4 yb = f32x8_to_bf16x8(y);
-        if (a.normed && ok) st16(a.normed + base + (int64_t)c * 8, yb);
+        if (a.normed) st16_if(a.normed + base + (int64_t)c * 8, yb, ok);
         if (from32) {
 #pragma unroll
             for (int k = 0; k < 8; ++k) src[k] = y[k];
