@@ -47,6 +47,7 @@ bool plan_rows(int64_t M, int W, int sm_count, Plan* p) {
     p->tpr = tpr;
     p->rpc = rpc;
     p->grid = (M + rpc - 1) / rpc;
+    p->full = nchunks == tpr * nv && M % rpc == 0;
     return p->grid <= 0x7FFFFFFF;
 }
 

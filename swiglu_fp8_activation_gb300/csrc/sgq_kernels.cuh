@@ -104,7 +104,9 @@ __host__ __device__ constexpr int norm_stage_bytes(bool has_res, int nv, int thr
     return nv * norm_stage_inputs(has_res) * threads * 16;
 }
 
-template <int FMT, int NV, bool HAS_RES>
+// FULL: every thread's chunks lie inside the row and every row inside M (the
+// plan divides both exactly), so no bounds are checked.
+template <int FMT, int NV, bool HAS_RES, bool FULL>
 __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
     extern __shared__ uint4 stage[];
     __shared__ float2 part[32];
@@ -114,7 +116,7 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
     const int lrow = threadIdx.x / tpr;
     const int t = threadIdx.x - lrow * tpr;
     const int64_t row = (int64_t)blockIdx.x * a.rpc + lrow;
-    const bool row_ok = row < a.M;
+    const bool row_ok = FULL || row < a.M;
     const int H = a.H, nchunks = H >> 3;
     const int64_t base = row * (int64_t)H;
     auto slot = [&](int v, int i) { return &stage[(NIN * v + i) * nt + threadIdx.x]; };
@@ -128,7 +130,7 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
         const int c = t + v * tpr;
-        const bool ok = row_ok && c < nchunks;   // else zero-fill, reading nothing
+        const bool ok = FULL || (row_ok && c < nchunks);   // else zero-fill, reading nothing
         const int nb = ok ? 16 : 0;
         cp_async16(slot(v, 0), ok ? (const void*)(a.x + base + (int64_t)c * 8) : (const void*)a.x, nb);
         if (HAS_RES)
@@ -154,7 +156,7 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
             bf16x8_to_f32(ld_smem16(slot(v, 1)), rf);
 #pragma unroll
             for (int k = 0; k < 8; ++k) h[k] += rf[k];
-            if (a.r_out) st16_if(a.r_out + base + (int64_t)c * 8, f32x8_to_bf16x8(h), row_ok && c < nchunks);
+            if (a.r_out) st16_if(a.r_out + base + (int64_t)c * 8, f32x8_to_bf16x8(h), FULL || (row_ok && c < nchunks));
         }
         bf16x8_to_f32(ld_smem16(slot(v, NIN - 1)), wf);
 #pragma unroll
@@ -186,7 +188,7 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
         const int c = t + v * tpr;
-        const bool ok = row_ok && c < nchunks;
+        const bool ok = FULL || (row_ok && c < nchunks);
         float y[8], src[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) y[k] = inv * z[v][k];     // z = 0 past the row end (zero-filled copies)
@@ -269,7 +271,7 @@ __host__ __device__ constexpr int swiglu_stage_bytes(int nv, int threads) { retu
 // (stage[2v][thread], stage[2v+1][thread]), one commit group per chunk, so
 // the whole row is in flight without holding registers and chunk v is
 // processed as soon as its own group has landed.
-template <int FMT, int NV, int ACT>
+template <int FMT, int NV, int ACT, bool FULL>
 __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs a) {
     extern __shared__ uint4 stage[];
     __shared__ float part_amax[32];
@@ -278,7 +280,7 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
     const int lrow = threadIdx.x / tpr;
     const int t = threadIdx.x - lrow * tpr;
     const int64_t row = (int64_t)blockIdx.x * a.rpc + lrow;
-    const bool row_ok = row < a.M;
+    const bool row_ok = FULL || row < a.M;
     const int I = a.I, nchunks = I >> 3;
     const uint16_t* grow = a.gu + row * (int64_t)(2 * I);
 
@@ -286,7 +288,7 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
         const int c = t + v * tpr;
-        const bool ok = row_ok && c < nchunks;   // else zero-fill, reading nothing
+        const bool ok = FULL || (row_ok && c < nchunks);   // else zero-fill, reading nothing
         cp_async16(&stage[(2 * v) * nt + threadIdx.x], ok ? (const void*)(grow + (int64_t)c * 8) : (const void*)a.gu,
                    ok ? 16 : 0);
         cp_async16(&stage[(2 * v + 1) * nt + threadIdx.x],
@@ -311,7 +313,7 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
                 for (int k = 0; k < 8; ++k) src[k] = round_bf16(src[k]);
             }
             // chunks past the row end loaded zeros, and every activation of 0 and 0 is 0
-            quantize_chunk<FMT>(src, row, c, row_ok && c < nchunks, I, a.q, a.scale);
+            quantize_chunk<FMT>(src, row, c, FULL || (row_ok && c < nchunks), I, a.q, a.scale);
         }
     } else {                           // per-token: the whole row, then its amax
         float src[NV][8];
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
             const int c = t + v * tpr;
-            quantize_chunk<FMT>(src[v], row, c, row_ok && c < nchunks, I, a.q, a.scale, pt.x, pt.y);
+            quantize_chunk<FMT>(src[v], row, c, FULL || (row_ok && c < nchunks), I, a.q, a.scale, pt.x, pt.y);
         }
     }
 }
