@@ -47,6 +47,8 @@ def lib() -> C.CDLL:
         L.ora_swiglu_quant.restype = C.c_int
         L.ora_swiglu_quant.argtypes = [C.c_int, C.c_int, C.c_uint, C.c_long, C.c_long, C.c_float,
                                        C.c_float, C.c_float, p, p, p, p, p, p, p, C.c_double]
+        L.ora_quantize.restype = C.c_int
+        L.ora_quantize.argtypes = [C.c_int, C.c_long, C.c_long, p, p, p, p, p, p, C.c_double]
         _lib = L
     return _lib
 
@@ -145,3 +147,20 @@ def swiglu_quant(fmt: str, act: str, gate_up: np.ndarray, *, from_fp32: bool,
     if rc != 0:
         raise ValueError(f"oracle rejected arguments (fmt={fmt}, act={act}, M={M}, I={I})")
     return {"q": q, "scale": s, "a": a, "t": t, "amb": amb, "gamb": gamb}
+
+
+def quantize(fmt: str, src: np.ndarray, *, diagnostics: bool = True, rel: float = REL_WINDOW) -> dict:
+    """Standalone FP8 quantisation of bf16 rows src [M, W] (bf16 bits): the
+    quant of the unfused chains. Returns q, scale and, with diagnostics, t,
+    amb and gamb."""
+    M, W = src.shape
+    src = _u16(src, (M, W))
+    q = np.zeros((M, W), np.uint8)
+    s = _scale_array(fmt, M, W)
+    t = amb = gamb = None
+    if diagnostics:
+        t, amb, gamb = np.zeros((M, W)), np.zeros((M, W), np.uint8), np.zeros(s.shape, np.uint8)
+    rc = lib().ora_quantize(FORMATS[fmt], M, W, _ptr(src), _ptr(q), _ptr(s), _ptr(t), _ptr(amb), _ptr(gamb), rel)
+    if rc != 0:
+        raise ValueError(f"oracle rejected arguments (fmt={fmt}, M={M}, W={W})")
+    return {"q": q, "scale": s, "t": t, "amb": amb, "gamb": gamb}

@@ -363,3 +363,28 @@ int ora_swiglu_quant(int fmt, int act, unsigned flags, long M, long I, float alp
     free(act_amb);
     return 0;
 }
+
+/* ------------------------------------------------------- standalone quant */
+
+/*
+ * Quantisation of bf16 rows src [M, W] (the standalone quant of the unfused
+ * chains: "[ROCm][MiniMax-M3.1] Fuse MXFP8 quant ..." (vllm PR 65478),
+ * microbenchmark script (norm, then a separate MXFP8 quant); "[ROCm] Fuse
+ * per-token activation quant into RMSNorm ..." (sglang PR 34502),
+ * "Motivation" (the standalone per-token quant)). The source values are the
+ * bf16 values themselves. Outputs and diagnostics as above.
+ */
+int ora_quantize(int fmt, long M, long W, const uint16_t* src_bits, uint8_t* q, void* scale, double* t64,
+                 unsigned char* amb, unsigned char* gamb, double rel) {
+    if (fmt < 0 || fmt > 2 || M < 0 || W <= 0 || W % group_size(fmt, W) != 0) return -1;
+    double* v = (double*)malloc(sizeof(double) * (size_t)W * 2);
+    unsigned char* sa = (unsigned char*)malloc((size_t)W);
+    if (!v || !sa) { free(v); free(sa); return -1; }
+    for (long i = 0; i < M; ++i) {
+        for (long j = 0; j < W; ++j) v[j] = ora_bf16_decode(src_bits[i * W + j]);
+        quant_row(fmt, 0, v, W, i, q, scale, t64, amb, gamb, rel, v + W, sa);
+    }
+    free(v);
+    free(sa);
+    return 0;
+}

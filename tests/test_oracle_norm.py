@@ -240,3 +240,25 @@ def test_fp32_source_block128_differs_from_bf16_source_like_the_page():
     # ulp: at most 2^-8 relative)
     rel = np.abs(a["scale"].astype(np.float64) / b["scale"].astype(np.float64) - 1.0)
     assert rel.max() <= 2.0 ** -8 * (1 + 1e-6)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "block128", "per_token"])
+def test_standalone_quantize_matches_the_fused_norm_route(fmt):
+    # The standalone quant of bf16 rows equals the quantiser reached through a
+    # plain RMSNorm of an all-ones row with eps = 0 (which returns w), and the
+    # unfused chain norm -> bf16 -> standalone quant equals the fused
+    # bf16-source norm, bit for bit.
+    rng = np.random.default_rng(12)
+    v = bits(rng.standard_normal((3, 512)) * 2.0 ** rng.integers(-8, 8, (3, 1)))
+    alone = oracle.quantize(fmt, v)
+    for i in range(3):
+        via_norm = quantize_vector(fmt, v[i])
+        np.testing.assert_array_equal(alone["q"][i], via_norm["q"][0])
+        np.testing.assert_array_equal(alone["scale"][i], via_norm["scale"][0])
+    case = inputs.norm_case_gemma_mx(4, 1024)
+    t = inputs.make_norm(case)
+    x, r, w = (inputs.bf16_bits(t[k]) for k in ("x", "r", "w"))
+    fused = oracle.rmsnorm_add_quant(fmt, x, r, w, eps=case.eps, gemma=True, from_fp32=False)
+    chain = oracle.quantize(fmt, fused["normed"])
+    np.testing.assert_array_equal(chain["q"], fused["q"])
+    np.testing.assert_array_equal(chain["scale"], fused["scale"])
