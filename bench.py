@@ -287,11 +287,16 @@ def graph_us_per_launch(fn, iters=200, reps=20):
 
 def decode_table(dev):
     """µs per launch at M = 8..192 for the two decode workloads (fused norm
-    +MXFP8+bf16 copy at H=6144; OAI SwiGLU+MXFP8 at I=768)."""
+    +MXFP8+bf16 copy at H=6144; OAI SwiGLU+MXFP8 at I=768), each beside its
+    unfused chain (norm to bf16, then a separate MXFP8 quant; SwiGLU to bf16,
+    then a separate quant), both chains' launches in one graph, as the pages'
+    decode table compares them."""
     import torch
 
-    from swiglu_fp8_activation_gb300 import inputs, rmsnorm_add_quant, swiglu_quant
-    out = {"norm_mxfp8_bf16copy_H6144": {}, "swiglu_oai_mxfp8_I768": {}}
+    from swiglu_fp8_activation_gb300 import (inputs, quantize_fp8, rmsnorm_add, rmsnorm_add_quant, swiglu,
+                                              swiglu_quant)
+    out = {"norm_mxfp8_bf16copy_H6144": {}, "norm_then_quant_H6144": {},
+           "swiglu_oai_mxfp8_I768": {}, "swiglu_then_quant_I768": {}}
     for M in DECODE_MS:
         nc = inputs.norm_case_gemma_mx(M)
         t = inputs.make_norm(nc)
@@ -302,11 +307,22 @@ def decode_table(dev):
         ro = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
         fn = lambda: rmsnorm_add_quant(x, w, residual_in=r, residual_out=ro, q_out=q, scale_out=s, normed_out=n)
         out["norm_mxfp8_bf16copy_H6144"][str(M)] = round(graph_us_per_launch(fn), 3)
+
+        def norm_chain():
+            rmsnorm_add(x, w, residual_in=r, residual_out=ro, normed_out=n)
+            quantize_fp8(n, q_out=q, scale_out=s)
+        out["norm_then_quant_H6144"][str(M)] = round(graph_us_per_launch(norm_chain), 3)
         gu = inputs.make_swiglu(inputs.swiglu_case_oai_mx(M)).to(dev)
         q2 = torch.empty(M, I_DECODE, dtype=torch.uint8, device=dev)
         s2 = torch.empty(M, I_DECODE // 32, dtype=torch.uint8, device=dev)
+        a2 = torch.empty(M, I_DECODE, dtype=torch.bfloat16, device=dev)
         fn2 = lambda: swiglu_quant(gu, q_out=q2, scale_out=s2)
         out["swiglu_oai_mxfp8_I768"][str(M)] = round(graph_us_per_launch(fn2), 3)
+
+        def swiglu_chain():
+            swiglu(gu, out=a2)
+            quantize_fp8(a2, q_out=q2, scale_out=s2)
+        out["swiglu_then_quant_I768"][str(M)] = round(graph_us_per_launch(swiglu_chain), 3)
     return out
 
 

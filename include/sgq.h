@@ -1,12 +1,20 @@
 /*
  * sgq.h -- fused pre-GEMM activation epilogue for NVIDIA GB300 (sm_103a).
  *
- * Two operations, each one CUDA kernel launch on the caller's stream:
+ * Two fused operations, each one CUDA kernel launch on the caller's stream:
  *
  *   rmsnorm_add_quant  residual add + RMSNorm + FP8 activation quantisation
  *                      (+ optional bf16 copy of the normed rows)
  *   swiglu_quant       fp32 SwiGLU (OAI clamped, or SiLU-and-mul)
  *                      + the same quantisation
+ *
+ * and the three steps of the unfused chains they replace, also one launch
+ * each, so that "norm, then a separate quant" and "activation, then a
+ * separate quant" can be run and timed beside the fused forms:
+ *
+ *   rmsnorm_add        residual add + RMSNorm to bf16
+ *   swiglu             SwiGLU to bf16
+ *   quantize_fp8       FP8 quantisation of bf16 rows
  *
  * The operations follow these pages:
  *   [P1] "[ROCm][MiniMax-M3.1] Fuse MXFP8 quant into the add+RMSNorm and
@@ -20,7 +28,7 @@
  *   [P4] "[ROCm] Fuse per-token activation quant into RMSNorm" (sglang PR
  *        34502): "Change" (per-token FP8, [m, 1] scale).
  *
- * Conventions shared by both entry points
+ * Conventions shared by all entry points
  *   - All pointers are DEVICE pointers owned by the caller. The library
  *     allocates nothing, keeps no state between calls, never synchronises and
  *     launches nothing but its one kernel, so calls may be captured into CUDA
@@ -152,6 +160,57 @@ int rmsnorm_add_quant(int fmt, uint32_t flags, int64_t M, int64_t H, float eps,
  */
 int swiglu_quant(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float alpha,
                  float beta, float limit, const void* gate_up, void* q_out, void* scale_out,
+                 sgq_stream_t stream);
+
+/*
+ * Residual add + RMSNorm to bf16 alone: the first step of the unfused chain
+ * "norm, then a separate quant" that [P1] "Microbenchmark script" times
+ * against the fused kernel, and that [P2] "Modifications" and [P4]
+ * "Motivation" describe (the quant ran as its own launch after the norm).
+ * Computes h, residual_out and normed_out exactly as rmsnorm_add_quant does;
+ * writes no quantised output. quantize_fp8(normed_out) then equals
+ * rmsnorm_add_quant without SGQ_F_QUANT_FROM_FP32, byte for byte.
+ *
+ * Arguments as for rmsnorm_add_quant, except:
+ *   flags         SGQ_F_GEMMA_WEIGHT only (others rejected)
+ *   H             any multiple of 8 up to SGQ_MAX_WIDTH
+ *   normed_out    [M, H] bf16, written (required)
+ */
+int rmsnorm_add(uint32_t flags, int64_t M, int64_t H, float eps, const void* x,
+                const void* residual_in, void* residual_out, const void* weight,
+                void* normed_out, sgq_stream_t stream);
+
+/*
+ * SwiGLU to bf16 alone: the first step of the unfused chain "activation,
+ * then a separate quant" ([P1] "Microbenchmark script"; [P2]
+ * "Modifications"). out = bf16(a), a the fp32 activation of swiglu_quant
+ * (with SGQ_F_ACT_ROUND_BF16, silu(g) rounded to bf16 before the product).
+ * quantize_fp8(out) then equals swiglu_quant without SGQ_F_QUANT_FROM_FP32,
+ * byte for byte.
+ *
+ * Arguments as for swiglu_quant, except:
+ *   flags         SGQ_F_ACT_ROUND_BF16 with SGQ_ACT_SILU_MUL only
+ *   I             any multiple of 8 up to SGQ_MAX_WIDTH
+ *   out           [M, I] bf16, written
+ */
+int swiglu(int act, uint32_t flags, int64_t M, int64_t I, float alpha, float beta,
+           float limit, const void* gate_up, void* out, sgq_stream_t stream);
+
+/*
+ * FP8 quantisation of bf16 rows alone, in any of the three formats: the
+ * separate quant launch of the unfused chains ([P1] "Purpose" and
+ * "Microbenchmark script"; [P2] "Modifications"; [P4] "Motivation").
+ * q_out, scale_out = quantise(src) with the group rule of rmsnorm_add_quant.
+ *
+ * Arguments:
+ *   fmt           sgq_format_t
+ *   M, W          rows and width (W a multiple of the group, <= SGQ_MAX_WIDTH)
+ *   src           [M, W] bf16, read
+ *   q_out         [M, W] E4M3, written
+ *   scale_out     scales in the layout of fmt, written
+ *   stream        the stream to launch on
+ */
+int quantize_fp8(int fmt, int64_t M, int64_t W, const void* src, void* q_out, void* scale_out,
                  sgq_stream_t stream);
 
 /* A static, human-readable name of a status code. */

@@ -7,6 +7,10 @@ Two fused ops behind a C ABI (`libsgq.so`, declared in include/sgq.h):
 * `swiglu_quant`: fp32 SwiGLU (OAI clamped, or SiLU-and-mul) + the same
   quantisation.
 
+The three steps of the unfused chains they replace are exported too, one
+launch each, to run and time beside them: `rmsnorm_add` (norm to bf16),
+`swiglu` (activation to bf16) and `quantize_fp8` (FP8 quant of bf16 rows).
+
 Formats: MXFP8 (E4M3 + one E8M0 scale per 1x32 block), 1x128 block FP8 with
 fp32 scales, and per-token FP8 with an [M,1] fp32 scale.
 
@@ -16,4 +20,5 @@ The CUDA library is loaded on first use; a missing library raises an error
 from .binding import (  # noqa: F401
     FORMATS, ACTS, F_GEMMA_WEIGHT, F_QUANT_FROM_FP32, F_ACT_ROUND_BF16,
     SgqError, library, library_path, rmsnorm_add_quant, swiglu_quant, status_string,
+    rmsnorm_add, swiglu, quantize_fp8,
 )

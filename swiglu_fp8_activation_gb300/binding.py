@@ -50,6 +50,12 @@ def library() -> C.CDLL:
         L.swiglu_quant.restype = C.c_int
         L.swiglu_quant.argtypes = [C.c_int, C.c_int, C.c_uint32, i64, i64, C.c_float, C.c_float,
                                    C.c_float, vp, vp, vp, vp]
+        L.rmsnorm_add.restype = C.c_int
+        L.rmsnorm_add.argtypes = [C.c_uint32, i64, i64, C.c_float, vp, vp, vp, vp, vp, vp]
+        L.swiglu.restype = C.c_int
+        L.swiglu.argtypes = [C.c_int, C.c_uint32, i64, i64, C.c_float, C.c_float, C.c_float, vp, vp, vp]
+        L.quantize_fp8.restype = C.c_int
+        L.quantize_fp8.argtypes = [C.c_int, i64, i64, vp, vp, vp, vp]
         L.sgq_status_string.restype = C.c_char_p
         L.sgq_status_string.argtypes = [C.c_int]
         L.sgq_abi_version.restype = C.c_int
@@ -165,4 +171,74 @@ def swiglu_quant(gate_up: torch.Tensor, *, fmt: str = "mxfp8", act: str = "swigl
     st = library().swiglu_quant(FORMATS[fmt], ACTS[act], flags, M, I, float(alpha), float(beta),
                                 float(limit), _ptr(gate_up), _ptr(q_out), _ptr(scale_out), _stream(stream))
     _check(st, "swiglu_quant")
+    return q_out, scale_out
+
+
+def rmsnorm_add(x: torch.Tensor, weight: torch.Tensor, *, residual_in: torch.Tensor | None = None,
+                residual_out: torch.Tensor | None = None, eps: float = 1e-6, gemma: bool = True,
+                normed_out: torch.Tensor | None = None, stream=None):
+    """Residual add + RMSNorm to bf16 (the norm step of the unfused chain).
+
+    Returns (normed [M,H] bf16, residual_out or None); residual_out defaults
+    to residual_in (in-place update) when residual_in is given.
+    """
+    M, H = x.shape
+    _want(x, (M, H), torch.bfloat16, "x")
+    _want(weight, (H,), torch.bfloat16, "weight")
+    if residual_in is not None:
+        _want(residual_in, (M, H), torch.bfloat16, "residual_in")
+        if residual_out is None:
+            residual_out = residual_in
+    if residual_out is not None:
+        _want(residual_out, (M, H), torch.bfloat16, "residual_out")
+    if normed_out is None:
+        normed_out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
+    _want(normed_out, (M, H), torch.bfloat16, "normed_out")
+    st = library().rmsnorm_add(F_GEMMA_WEIGHT if gemma else 0, M, H, float(eps), _ptr(x), _ptr(residual_in),
+                               _ptr(residual_out), _ptr(weight), _ptr(normed_out), _stream(stream))
+    _check(st, "rmsnorm_add")
+    return normed_out, residual_out
+
+
+def swiglu(gate_up: torch.Tensor, *, act: str = "swiglu_oai", round_act_bf16: bool = False,
+           alpha: float = 1.702, beta: float = 1.0, limit: float = 7.0, out: torch.Tensor | None = None,
+           stream=None):
+    """SwiGLU to bf16 (the activation step of the unfused chain).
+
+    gate_up [M, 2I] bf16. Returns out [M, I] bf16.
+    """
+    M, I2 = gate_up.shape
+    I = I2 // 2
+    _want(gate_up, (M, 2 * I), torch.bfloat16, "gate_up")
+    if I2 % 2:
+        raise SgqError("gate_up: width must be even")
+    if act not in ACTS:
+        raise SgqError(f"unknown activation {act!r}")
+    if out is None:
+        out = torch.empty((M, I), dtype=torch.bfloat16, device=gate_up.device)
+    _want(out, (M, I), torch.bfloat16, "out")
+    st = library().swiglu(ACTS[act], F_ACT_ROUND_BF16 if round_act_bf16 else 0, M, I, float(alpha), float(beta),
+                          float(limit), _ptr(gate_up), _ptr(out), _stream(stream))
+    _check(st, "swiglu")
+    return out
+
+
+def quantize_fp8(src: torch.Tensor, *, fmt: str = "mxfp8", q_out: torch.Tensor | None = None,
+                 scale_out: torch.Tensor | None = None, stream=None):
+    """FP8 quantisation of bf16 rows (the separate quant of the unfused chain).
+
+    src [M, W] bf16. Returns (q [M,W] uint8 E4M3, scale).
+    """
+    M, W = src.shape
+    _want(src, (M, W), torch.bfloat16, "src")
+    if fmt not in FORMATS:
+        raise SgqError(f"unknown format {fmt!r}")
+    if q_out is None:
+        q_out = torch.empty((M, W), dtype=torch.uint8, device=src.device)
+    if scale_out is None:
+        scale_out = torch.empty(scale_shape(fmt, M, W), dtype=scale_dtype(fmt), device=src.device)
+    _want(q_out, (M, W), torch.uint8, "q_out")
+    _want(scale_out, scale_shape(fmt, M, W), scale_dtype(fmt), "scale_out")
+    st = library().quantize_fp8(FORMATS[fmt], M, W, _ptr(src), _ptr(q_out), _ptr(scale_out), _stream(stream))
+    _check(st, "quantize_fp8")
     return q_out, scale_out

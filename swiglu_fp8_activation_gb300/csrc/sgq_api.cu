@@ -102,6 +102,100 @@ bool any_overlap(const Span* s, int k) {
     return false;
 }
 
+
+int launched(cudaError_t e) {
+    if (e == cudaSuccess) return SGQ_OK;
+    sgq::note_launch_error(e);
+    return SGQ_ERR_LAUNCH;
+}
+
+// The norm launch behind rmsnorm_add_quant (q_out set) and rmsnorm_add
+// (q_out null: only the bf16 copy). Width divisibility by the quant group
+// and the output pointers required by each entry are checked by the caller.
+int norm_call(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, const void* x, const void* residual_in,
+              void* residual_out, const void* weight, void* q_out, void* scale_out, void* normed_out,
+              sgq_stream_t stream) {
+    if (M < 0 || H <= 0 || !(eps >= 0.0f) || isinf(eps)) return SGQ_ERR_INVALID_ARG;
+    if (H % 8 != 0 || H > SGQ_MAX_WIDTH) return SGQ_ERR_UNSUPPORTED;
+    if (M > kMaxElements / H) return SGQ_ERR_INVALID_ARG;
+    if (M == 0) return SGQ_OK;
+    if (!x || !weight) return SGQ_ERR_INVALID_ARG;
+    if (residual_out && !residual_in) return SGQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(residual_in, 16) || !aligned(residual_out, 16) || !aligned(weight, 16) ||
+        !aligned(q_out, 16) || !aligned(normed_out, 16) || !aligned(scale_out, fmt == SGQ_FMT_MXFP8 ? 1 : 4))
+        return SGQ_ERR_MISALIGNED;
+    const size_t act = (size_t)M * (size_t)H * 2;
+    // residual_out == residual_in is the one overlap allowed (in-place update)
+    const void* r_out_span = residual_out == residual_in ? nullptr : residual_out;
+    const Span spans[] = {{x, act},
+                          {residual_in, act},
+                          {weight, (size_t)H * 2},
+                          {q_out, (size_t)M * H},
+                          {scale_out, q_out ? scale_bytes(fmt, M, H) : 0},
+                          {normed_out, act},
+                          {r_out_span, act}};
+    if (any_overlap(spans, 7)) return SGQ_ERR_INVALID_ARG;
+
+    sgq::Plan plan;
+    if (!sgq::plan_rows(M, (int)H, sm_count(), &plan)) return SGQ_ERR_UNSUPPORTED;
+    sgq::NormArgs a;
+    a.x = static_cast<const uint16_t*>(x);
+    a.r_in = static_cast<const uint16_t*>(residual_in);
+    a.r_out = static_cast<uint16_t*>(residual_out);
+    a.w = static_cast<const uint16_t*>(weight);
+    a.q = static_cast<uint8_t*>(q_out);
+    a.scale = scale_out;
+    a.normed = static_cast<uint16_t*>(normed_out);
+    a.M = M;
+    a.H = (int)H;
+    a.tpr = plan.tpr;
+    a.rpc = plan.rpc;
+    a.eps = eps;
+    a.flags = flags;
+    return launched(sgq::launch_norm(fmt, plan, a, static_cast<cudaStream_t>(stream)));
+}
+
+// The SwiGLU launch behind swiglu_quant (q_out set) and swiglu (out set:
+// the bf16 activation, no quantisation).
+int swiglu_call(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float alpha, float beta, float limit,
+                const void* gate_up, void* q_out, void* scale_out, void* out, sgq_stream_t stream) {
+    if (act != SGQ_ACT_SWIGLU_OAI && act != SGQ_ACT_SILU_MUL) return SGQ_ERR_INVALID_ARG;
+    if ((flags & SGQ_F_ACT_ROUND_BF16) && act != SGQ_ACT_SILU_MUL) return SGQ_ERR_INVALID_ARG;
+    if (M < 0 || I <= 0) return SGQ_ERR_INVALID_ARG;
+    if (act == SGQ_ACT_SWIGLU_OAI && (!isfinite(alpha) || !isfinite(beta) || !(limit > 0.0f)))
+        return SGQ_ERR_INVALID_ARG;
+    if (I % 8 != 0 || I > SGQ_MAX_WIDTH) return SGQ_ERR_UNSUPPORTED;
+    if (M > kMaxElements / (2 * I)) return SGQ_ERR_INVALID_ARG;
+    if (M == 0) return SGQ_OK;
+    if (!gate_up) return SGQ_ERR_INVALID_ARG;
+    if (!aligned(gate_up, 16) || !aligned(q_out, 16) || !aligned(out, 16) ||
+        !aligned(scale_out, fmt == SGQ_FMT_MXFP8 ? 1 : 4))
+        return SGQ_ERR_MISALIGNED;
+    const Span spans[] = {{gate_up, (size_t)M * I * 4},
+                          {q_out, (size_t)M * I},
+                          {scale_out, q_out ? scale_bytes(fmt, M, I) : 0},
+                          {out, (size_t)M * I * 2}};
+    if (any_overlap(spans, 4)) return SGQ_ERR_INVALID_ARG;
+
+    sgq::Plan plan;
+    if (!sgq::plan_rows(M, (int)I, sm_count(), &plan)) return SGQ_ERR_UNSUPPORTED;
+    sgq::SwigluArgs a;
+    a.gu = static_cast<const uint16_t*>(gate_up);
+    a.q = static_cast<uint8_t*>(q_out);
+    a.scale = scale_out;
+    a.out = static_cast<uint16_t*>(out);
+    a.M = M;
+    a.I = (int)I;
+    a.tpr = plan.tpr;
+    a.rpc = plan.rpc;
+    a.flags = flags;
+    a.act = act;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.limit = limit;
+    return launched(sgq::launch_swiglu(fmt, plan, a, static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -128,85 +222,61 @@ int rmsnorm_add_quant(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, 
                       void* scale_out, void* normed_out, sgq_stream_t stream) {
     if (fmt < SGQ_FMT_MXFP8 || fmt > SGQ_FMT_FP8_PER_TOKEN) return SGQ_ERR_INVALID_ARG;
     if (flags & ~(SGQ_F_GEMMA_WEIGHT | SGQ_F_QUANT_FROM_FP32)) return SGQ_ERR_INVALID_ARG;
-    if (M < 0 || H <= 0 || !(eps >= 0.0f) || isinf(eps)) return SGQ_ERR_INVALID_ARG;
-    if (H % group_of(fmt) != 0 || H > SGQ_MAX_WIDTH) return SGQ_ERR_UNSUPPORTED;
-    if (M > kMaxElements / H) return SGQ_ERR_INVALID_ARG;
-    if (M == 0) return SGQ_OK;
-    if (!x || !weight || !q_out || !scale_out) return SGQ_ERR_INVALID_ARG;
-    if (residual_out && !residual_in) return SGQ_ERR_INVALID_ARG;
-    if (!aligned(x, 16) || !aligned(residual_in, 16) || !aligned(residual_out, 16) || !aligned(weight, 16) ||
-        !aligned(q_out, 16) || !aligned(normed_out, 16) || !aligned(scale_out, fmt == SGQ_FMT_MXFP8 ? 1 : 4))
-        return SGQ_ERR_MISALIGNED;
-    const size_t act = (size_t)M * (size_t)H * 2;
-    // residual_out == residual_in is the one overlap allowed (in-place update)
-    const void* r_out_span = residual_out == residual_in ? nullptr : residual_out;
-    const Span spans[] = {{x, act},      {residual_in, act}, {weight, (size_t)H * 2}, {q_out, (size_t)M * H},
-                          {scale_out, scale_bytes(fmt, M, H)}, {normed_out, act}, {r_out_span, act}};
-    if (any_overlap(spans, 7)) return SGQ_ERR_INVALID_ARG;
+    if (H > 0 && H % group_of(fmt) != 0) return SGQ_ERR_UNSUPPORTED;
+    if (M > 0 && (!q_out || !scale_out)) return SGQ_ERR_INVALID_ARG;
+    return norm_call(fmt, flags, M, H, eps, x, residual_in, residual_out, weight, q_out, scale_out, normed_out,
+                     stream);
+}
 
-    sgq::Plan plan;
-    if (!sgq::plan_rows(M, (int)H, sm_count(), &plan)) return SGQ_ERR_UNSUPPORTED;
-    sgq::NormArgs a;
-    a.x = static_cast<const uint16_t*>(x);
-    a.r_in = static_cast<const uint16_t*>(residual_in);
-    a.r_out = static_cast<uint16_t*>(residual_out);
-    a.w = static_cast<const uint16_t*>(weight);
-    a.q = static_cast<uint8_t*>(q_out);
-    a.scale = scale_out;
-    a.normed = static_cast<uint16_t*>(normed_out);
-    a.M = M;
-    a.H = (int)H;
-    a.tpr = plan.tpr;
-    a.rpc = plan.rpc;
-    a.eps = eps;
-    a.flags = flags;
-    const cudaError_t e = sgq::launch_norm(fmt, plan, a, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) {
-        sgq::note_launch_error(e);
-        return SGQ_ERR_LAUNCH;
-    }
-    return SGQ_OK;
+int rmsnorm_add(uint32_t flags, int64_t M, int64_t H, float eps, const void* x, const void* residual_in,
+                void* residual_out, const void* weight, void* normed_out, sgq_stream_t stream) {
+    if (flags & ~SGQ_F_GEMMA_WEIGHT) return SGQ_ERR_INVALID_ARG;
+    if (H > 0 && H % 8 != 0) return SGQ_ERR_UNSUPPORTED;
+    if (M > 0 && !normed_out) return SGQ_ERR_INVALID_ARG;
+    return norm_call(SGQ_FMT_MXFP8, flags, M, H, eps, x, residual_in, residual_out, weight, nullptr, nullptr,
+                     normed_out, stream);
 }
 
 int swiglu_quant(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float alpha, float beta,
                  float limit, const void* gate_up, void* q_out, void* scale_out, sgq_stream_t stream) {
     if (fmt < SGQ_FMT_MXFP8 || fmt > SGQ_FMT_FP8_PER_TOKEN) return SGQ_ERR_INVALID_ARG;
-    if (act != SGQ_ACT_SWIGLU_OAI && act != SGQ_ACT_SILU_MUL) return SGQ_ERR_INVALID_ARG;
     if (flags & ~(SGQ_F_QUANT_FROM_FP32 | SGQ_F_ACT_ROUND_BF16)) return SGQ_ERR_INVALID_ARG;
-    if ((flags & SGQ_F_ACT_ROUND_BF16) && act != SGQ_ACT_SILU_MUL) return SGQ_ERR_INVALID_ARG;
-    if (M < 0 || I <= 0) return SGQ_ERR_INVALID_ARG;
-    if (act == SGQ_ACT_SWIGLU_OAI && (!isfinite(alpha) || !isfinite(beta) || !(limit > 0.0f)))
-        return SGQ_ERR_INVALID_ARG;
-    if (I % group_of(fmt) != 0 || I > SGQ_MAX_WIDTH) return SGQ_ERR_UNSUPPORTED;
-    if (M > kMaxElements / (2 * I)) return SGQ_ERR_INVALID_ARG;
+    if (I > 0 && I % group_of(fmt) != 0) return SGQ_ERR_UNSUPPORTED;
+    if (M > 0 && (!q_out || !scale_out)) return SGQ_ERR_INVALID_ARG;
+    return swiglu_call(fmt, act, flags, M, I, alpha, beta, limit, gate_up, q_out, scale_out, nullptr, stream);
+}
+
+int swiglu(int act, uint32_t flags, int64_t M, int64_t I, float alpha, float beta, float limit,
+           const void* gate_up, void* out, sgq_stream_t stream) {
+    if (flags & ~SGQ_F_ACT_ROUND_BF16) return SGQ_ERR_INVALID_ARG;
+    if (I > 0 && I % 8 != 0) return SGQ_ERR_UNSUPPORTED;
+    if (M > 0 && !out) return SGQ_ERR_INVALID_ARG;
+    return swiglu_call(SGQ_FMT_MXFP8, act, flags, M, I, alpha, beta, limit, gate_up, nullptr, nullptr, out, stream);
+}
+
+int quantize_fp8(int fmt, int64_t M, int64_t W, const void* src, void* q_out, void* scale_out, sgq_stream_t stream) {
+    if (fmt < SGQ_FMT_MXFP8 || fmt > SGQ_FMT_FP8_PER_TOKEN) return SGQ_ERR_INVALID_ARG;
+    if (M < 0 || W <= 0) return SGQ_ERR_INVALID_ARG;
+    if (W % group_of(fmt) != 0 || W > SGQ_MAX_WIDTH) return SGQ_ERR_UNSUPPORTED;
+    if (M > kMaxElements / W) return SGQ_ERR_INVALID_ARG;
     if (M == 0) return SGQ_OK;
-    if (!gate_up || !q_out || !scale_out) return SGQ_ERR_INVALID_ARG;
-    if (!aligned(gate_up, 16) || !aligned(q_out, 16) || !aligned(scale_out, fmt == SGQ_FMT_MXFP8 ? 1 : 4))
+    if (!src || !q_out || !scale_out) return SGQ_ERR_INVALID_ARG;
+    if (!aligned(src, 16) || !aligned(q_out, 16) || !aligned(scale_out, fmt == SGQ_FMT_MXFP8 ? 1 : 4))
         return SGQ_ERR_MISALIGNED;
-    const Span spans[] = {{gate_up, (size_t)M * I * 4}, {q_out, (size_t)M * I}, {scale_out, scale_bytes(fmt, M, I)}};
+    const Span spans[] = {{src, (size_t)M * W * 2}, {q_out, (size_t)M * W}, {scale_out, scale_bytes(fmt, M, W)}};
     if (any_overlap(spans, 3)) return SGQ_ERR_INVALID_ARG;
 
     sgq::Plan plan;
-    if (!sgq::plan_rows(M, (int)I, sm_count(), &plan)) return SGQ_ERR_UNSUPPORTED;
-    sgq::SwigluArgs a;
-    a.gu = static_cast<const uint16_t*>(gate_up);
+    if (!sgq::plan_rows(M, (int)W, sm_count(), &plan)) return SGQ_ERR_UNSUPPORTED;
+    sgq::QuantArgs a;
+    a.src = static_cast<const uint16_t*>(src);
     a.q = static_cast<uint8_t*>(q_out);
     a.scale = scale_out;
     a.M = M;
-    a.I = (int)I;
+    a.W = (int)W;
     a.tpr = plan.tpr;
     a.rpc = plan.rpc;
-    a.flags = flags;
-    a.act = act;
-    a.alpha = alpha;
-    a.beta = beta;
-    a.limit = limit;
-    const cudaError_t e = sgq::launch_swiglu(fmt, plan, a, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) {
-        sgq::note_launch_error(e);
-        return SGQ_ERR_LAUNCH;
-    }
-    return SGQ_OK;
+    return launched(sgq::launch_quant(fmt, plan, a, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

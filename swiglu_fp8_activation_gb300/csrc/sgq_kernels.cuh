@@ -25,8 +25,9 @@ struct NormArgs {
 
 struct SwigluArgs {
     const uint16_t* gu;      // [M, 2I] bf16: gate = [0, I), up = [I, 2I)
-    uint8_t* q;              // [M, I] E4M3
+    uint8_t* q;              // [M, I] E4M3 (null when `out` is set)
     void* scale;
+    uint16_t* out;           // [M, I] bf16 activation instead of quantising, or null
     int64_t M;
     int I;
     int tpr;
@@ -34,6 +35,16 @@ struct SwigluArgs {
     uint32_t flags;
     int act;
     float alpha, beta, limit;
+};
+
+struct QuantArgs {
+    const uint16_t* src;     // [M, W] bf16
+    uint8_t* q;              // [M, W] E4M3
+    void* scale;
+    int64_t M;
+    int W;
+    int tpr;
+    int rpc;
 };
 
 // Quantise one chunk (8 source values of row `row`, chunk index c) and store
@@ -179,7 +190,9 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
     const float inv = __frsqrt_rn(__fdiv_rn(ss, (float)H) + a.eps);
 
     // 4. y = inv * z; bf16 copy; quant source; quantise (MX and 1x128 chunk by
-    //    chunk; per-token after the whole row, with the row scale from ymax)
+    //    chunk; per-token after the whole row, with the row scale from ymax).
+    //    Without q (the unfused norm) only the bf16 copy is written.
+    const bool quant = a.q != nullptr;
     float2 pt = make_float2(0.0f, 0.0f);
     if (FMT == FMT_PT) {
         const float ymax = inv * row_zmax;                     // = max |y| exactly
@@ -194,6 +207,7 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
         for (int k = 0; k < 8; ++k) y[k] = inv * z[v][k];     // z = 0 past the row end (zero-filled copies)
         const uint4 yb = f32x8_to_bf16x8(y);
         if (a.normed) st16_if(a.normed + base + (int64_t)c * 8, yb, ok);
+        if (!quant) continue;
         if (from32) {
 #pragma unroll
             for (int k = 0; k < 8; ++k) src[k] = y[k];
@@ -308,6 +322,10 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
             bf16x8_to_f32(ld_smem16(&stage[(2 * v) * nt + threadIdx.x]), g);
             bf16x8_to_f32(ld_smem16(&stage[(2 * v + 1) * nt + threadIdx.x]), u);
             activation8<ACT>(g, u, a.alpha, a.beta, a.limit, gr.x, gr.y, round_silu, src);
+            if (a.out) {                   // the unfused activation: bf16 out, no quantisation
+                st16_if(a.out + row * I + (int64_t)c * 8, f32x8_to_bf16x8(src), FULL || (row_ok && c < nchunks));
+                continue;
+            }
             if (!from32) {
 #pragma unroll
                 for (int k = 0; k < 8; ++k) src[k] = round_bf16(src[k]);
@@ -336,6 +354,64 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
         for (int v = 0; v < NV; ++v) {
             const int c = t + v * tpr;
             quantize_chunk<FMT>(src[v], row, c, FULL || (row_ok && c < nchunks), I, a.q, a.scale, pt.x, pt.y);
+        }
+    }
+}
+
+// Bytes of dynamic shared memory the standalone quant kernel stages its loads in.
+__host__ __device__ constexpr int quant_stage_bytes(int nv, int threads) { return nv * threads * 16; }
+
+// Standalone FP8 quantisation of bf16 rows (the quant of the unfused
+// chains). Same row engine and quantiser as the fused kernels; the source is
+// the bf16 value itself.
+template <int FMT, int NV, bool FULL>
+__global__ void __launch_bounds__(kMaxTPR) quant_kernel(const QuantArgs a) {
+    extern __shared__ uint4 stage[];
+    __shared__ float part_amax[32];
+    const int tpr = a.tpr;
+    const int nt = blockDim.x;
+    const int lrow = threadIdx.x / tpr;
+    const int t = threadIdx.x - lrow * tpr;
+    const int64_t row = (int64_t)blockIdx.x * a.rpc + lrow;
+    const bool row_ok = FULL || row < a.M;
+    const int W = a.W, nchunks = W >> 3;
+    const uint16_t* srow = a.src + row * (int64_t)W;
+
+    pdl_wait();
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        const int c = t + v * tpr;
+        const bool ok = FULL || (row_ok && c < nchunks);   // else zero-fill, reading nothing
+        cp_async16(&stage[v * nt + threadIdx.x], ok ? (const void*)(srow + (int64_t)c * 8) : (const void*)a.src,
+                   ok ? 16 : 0);
+        cp_async_commit();
+    }
+    pdl_trigger();
+
+    if (FMT != FMT_PT) {
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const int c = t + v * tpr;
+            float src[8];
+            cp_async_wait_group_of<NV>(v);
+            bf16x8_to_f32(ld_smem16(&stage[v * nt + threadIdx.x]), src);
+            quantize_chunk<FMT>(src, row, c, FULL || (row_ok && c < nchunks), W, a.q, a.scale);
+        }
+    } else {
+        float src[NV][8];
+        float m = 0.0f;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            cp_async_wait_group_of<NV>(v);
+            bf16x8_to_f32(ld_smem16(&stage[v * nt + threadIdx.x]), src[v]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(src[v][k]));
+        }
+        const float2 pt = per_token_scale(row_reduce<true>(m, part_amax, tpr, lrow));
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const int c = t + v * tpr;
+            quantize_chunk<FMT>(src[v], row, c, FULL || (row_ok && c < nchunks), W, a.q, a.scale, pt.x, pt.y);
         }
     }
 }

@@ -53,5 +53,6 @@ cudaError_t launch_norm(int fmt, const Plan& p, const NormArgs& a, cudaStream_t 
 // Records the CUDA error of a failed launch for sgq_launch_error() (per thread).
 void note_launch_error(cudaError_t e);
 cudaError_t launch_swiglu(int fmt, const Plan& p, const SwigluArgs& a, cudaStream_t stream);
+cudaError_t launch_quant(int fmt, const Plan& p, const QuantArgs& a, cudaStream_t stream);
 
 }  // namespace sgq

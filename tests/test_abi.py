@@ -36,8 +36,8 @@ def _header_value(name):
 
 def test_library_exports_every_declared_function(sgq_lib):
     names = _declared_functions()
-    assert set(names) == {"rmsnorm_add_quant", "swiglu_quant", "sgq_status_string", "sgq_abi_version",
-                          "sgq_launch_error"}
+    assert set(names) == {"rmsnorm_add_quant", "swiglu_quant", "rmsnorm_add", "swiglu", "quantize_fp8",
+                          "sgq_status_string", "sgq_abi_version", "sgq_launch_error"}
     for n in names:
         assert hasattr(sgq_lib, n), n
     m = re.search(r"#define SGQ_ABI_VERSION (\d+)", _header())
@@ -128,6 +128,67 @@ def test_swiglu_argument_errors(sgq_lib):
     assert swiglu(L, q=_p(0)) == INVALID              # q_out overlaps gate_up
 
 
+def norm_only(lib, flags=1, M=8, H=256, eps=1e-6, x=_p(0), r=_p(1), ro=_p(2), w=_p(3), n=_p(6)):
+    return lib.rmsnorm_add(flags, M, H, eps, x, r, ro, w, n, None)
+
+
+def act_only(lib, act=0, flags=0, M=8, I=256, alpha=1.702, beta=1.0, limit=7.0, gu=_p(0), out=_p(1)):
+    return lib.swiglu(act, flags, M, I, alpha, beta, limit, gu, out, None)
+
+
+def quant(lib, fmt=0, M=8, W=256, src=_p(0), q=_p(1), s=_p(2)):
+    return lib.quantize_fp8(fmt, M, W, src, q, s, None)
+
+
+def test_unfused_norm_argument_errors(sgq_lib):
+    L = sgq_lib
+    assert norm_only(L, M=0, x=None, n=None) == OK
+    assert norm_only(L, flags=2) == INVALID           # no quantisation, so no QUANT_FROM_FP32
+    assert norm_only(L, M=-1) == INVALID
+    assert norm_only(L, H=0) == INVALID
+    assert norm_only(L, eps=float("nan")) == INVALID
+    assert norm_only(L, H=20) == UNSUPPORTED          # H % 8 == 0 is the only width rule
+    assert norm_only(L, H=16384 + 8) == UNSUPPORTED
+    for kw in ("x", "w", "n"):
+        assert norm_only(L, **{kw: None}) == INVALID, kw
+    assert norm_only(L, r=None) == INVALID            # residual_out without residual_in
+    assert norm_only(L, n=C.c_void_p(BASE + 6 * 64 * MB + 8)) == MISALIGNED
+    assert norm_only(L, n=_p(0)) == INVALID           # normed_out overlaps x
+    assert norm_only(L, ro=_p(6)) == INVALID          # residual_out overlaps normed_out
+
+
+def test_unfused_swiglu_argument_errors(sgq_lib):
+    L = sgq_lib
+    assert act_only(L, M=0, gu=None, out=None) == OK
+    assert act_only(L, act=2) == INVALID
+    assert act_only(L, flags=2) == INVALID            # no quantisation, so no QUANT_FROM_FP32
+    assert act_only(L, flags=4) == INVALID            # ACT_ROUND_BF16 needs SiLU-and-mul
+    assert act_only(L, limit=-1.0) == INVALID
+    assert act_only(L, I=36) == UNSUPPORTED           # I % 8 == 0 is the only width rule
+    assert act_only(L, gu=None) == INVALID
+    assert act_only(L, out=None) == INVALID
+    assert act_only(L, out=C.c_void_p(BASE + 64 * MB + 2)) == MISALIGNED
+    assert act_only(L, out=C.c_void_p(BASE + 4096)) == INVALID     # out inside gate_up
+
+
+def test_quantize_argument_errors(sgq_lib):
+    L = sgq_lib
+    assert quant(L, M=0, src=None) == OK
+    assert quant(L, fmt=3) == INVALID
+    assert quant(L, M=-2) == INVALID
+    assert quant(L, W=0) == INVALID
+    assert quant(L, W=48) == UNSUPPORTED
+    assert quant(L, fmt=1, W=192) == UNSUPPORTED
+    assert quant(L, fmt=2, W=12) == UNSUPPORTED
+    assert quant(L, W=16384 + 32) == UNSUPPORTED
+    for kw in ("src", "q", "s"):
+        assert quant(L, **{kw: None}) == INVALID, kw
+    assert quant(L, src=C.c_void_p(BASE + 8)) == MISALIGNED
+    assert quant(L, fmt=2, s=C.c_void_p(BASE + 2 * 64 * MB + 2)) == MISALIGNED
+    assert quant(L, q=_p(0)) == INVALID               # q_out overlaps src
+    assert quant(L, M=1 << 45, W=16384) == INVALID
+
+
 def test_binding_rejects_wrong_tensors():
     import torch
     x = torch.zeros(4, 64, dtype=torch.float32)
@@ -136,3 +197,9 @@ def test_binding_rejects_wrong_tensors():
         binding.rmsnorm_add_quant(x, w)
     with pytest.raises(binding.SgqError):
         binding.swiglu_quant(torch.zeros(4, 64, dtype=torch.bfloat16), fmt="nope")
+    with pytest.raises(binding.SgqError):
+        binding.rmsnorm_add(x, w)
+    with pytest.raises(binding.SgqError):
+        binding.swiglu(torch.zeros(4, 63, dtype=torch.bfloat16))
+    with pytest.raises(binding.SgqError):
+        binding.quantize_fp8(torch.zeros(4, 64, dtype=torch.bfloat16), fmt="fp4")
