@@ -36,7 +36,8 @@
  *   - All tensors are contiguous and row-major. Inputs are bfloat16. Quantised
  *     values are OCP E4M3 ("e4m3fn") bytes.
  *   - Scale layouts: MXFP8 -> uint8 E8M0 codes [M, W/32] (value 2^(code-127));
- *     1x128 block -> float32 [M, W/128]; per-token -> float32 [M, 1].
+ *     1x128 block -> float32 [M, W/128]; per-token -> float32 [M, 1]; all
+ *     row-major unless a layout flag below selects another one.
  *   - Alignment: every tensor pointer must be 16-byte aligned, except a
  *     float32 scale pointer (4 bytes) and an E8M0 scale pointer (1 byte).
  *   - Width rules: MXFP8 needs W % 32 == 0, 1x128 needs W % 128 == 0,
@@ -81,6 +82,30 @@ typedef enum sgq_act {
 #define SGQ_F_QUANT_FROM_FP32 (1u << 1) /* quantise the fp32 value, not its bf16 rounding */
 #define SGQ_F_ACT_ROUND_BF16  (1u << 2) /* SiLU-and-mul: round silu(g) to bf16 before the product */
 
+/*
+ * Scale layouts for GEMM consumers other than the row-major one. [P1]'s
+ * review ("Scale layout / scheme contract") separates consumers that read
+ * row-major [M, N/32] E8M0 scales from those that want them swizzled; these
+ * flags give the layouts that Blackwell-class consumers read. Accepted by
+ * rmsnorm_add_quant, swiglu_quant and quantize_fp8.
+ *
+ * SGQ_F_SCALE_SWIZZLED (MXFP8 only): the E8M0 codes in the tiled layout of
+ *   block-scaled MMA operands (the scale-factor layout that cuBLASLt's
+ *   VEC32_UE8M0 block scaling reads). Rows are padded to Mp = M rounded up
+ *   to 128 and scale columns to Gp = W/32 rounded up to 4. The [Mp, Gp] codes
+ *   are cut into 128 x 4 tiles of 512 bytes, stored tile-row by tile-row
+ *   ((r/128) * (Gp/4) + g/4); inside a tile, row r and column g sit at byte
+ *   (r % 32) * 16 + ((r / 32) % 4) * 4 + g % 4. Buffer: Mp * Gp bytes. The
+ *   padding (rows >= M, columns >= W/32) is written as code 0.
+ * SGQ_F_SCALE_COL_MAJOR (1x128 only): the fp32 scales column-major (group-
+ *   major): scale (r, g) at g * Mp + r with Mp = M rounded up to 4, so every
+ *   column starts 16-byte aligned from the base. Buffer: (W/128) * Mp * 4
+ *   bytes. Rows >= M are written as 0.0f.
+ * Either flag with another format is SGQ_ERR_INVALID_ARG.
+ */
+#define SGQ_F_SCALE_SWIZZLED  (1u << 3)
+#define SGQ_F_SCALE_COL_MAJOR (1u << 4)
+
 typedef enum sgq_status {
     SGQ_OK = 0,
     SGQ_ERR_INVALID_ARG = 1,    /* NULL required pointer, bad enum/flag, negative size, overlap */
@@ -112,7 +137,8 @@ typedef void* sgq_stream_t;
  *
  * Arguments:
  *   fmt           sgq_format_t
- *   flags         SGQ_F_GEMMA_WEIGHT | SGQ_F_QUANT_FROM_FP32 (others rejected)
+ *   flags         SGQ_F_GEMMA_WEIGHT | SGQ_F_QUANT_FROM_FP32, and a scale layout
+ *                 flag of the format (others rejected)
  *   M, H          rows and hidden width
  *   eps           >= 0, finite
  *   x             [M, H] bf16, read
@@ -121,7 +147,7 @@ typedef void* sgq_stream_t;
  *                 is NULL; may equal residual_in
  *   weight        [H] bf16, read
  *   q_out         [M, H] E4M3, written
- *   scale_out     scales in the layout of fmt, written
+ *   scale_out     scales in the layout of fmt and flags, written
  *   normed_out    [M, H] bf16, written, or NULL
  *   stream        the stream to launch on
  */
@@ -148,14 +174,15 @@ int rmsnorm_add_quant(int fmt, uint32_t flags, int64_t M, int64_t H, float eps,
  *
  * Arguments:
  *   fmt, act      sgq_format_t, sgq_act_t
- *   flags         SGQ_F_QUANT_FROM_FP32, and SGQ_F_ACT_ROUND_BF16 with
- *                 SGQ_ACT_SILU_MUL only (others rejected)
+ *   flags         SGQ_F_QUANT_FROM_FP32, SGQ_F_ACT_ROUND_BF16 with
+ *                 SGQ_ACT_SILU_MUL only, and a scale layout flag of the
+ *                 format (others rejected)
  *   M, I          rows and intermediate width (the output width)
  *   alpha, beta, limit  OAI parameters (finite alpha and beta, limit > 0,
  *                 may be +inf); ignored for SiLU-and-mul
  *   gate_up       [M, 2I] bf16, read
  *   q_out         [M, I] E4M3, written
- *   scale_out     scales in the layout of fmt, written
+ *   scale_out     scales in the layout of fmt and flags, written
  *   stream        the stream to launch on
  */
 int swiglu_quant(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float alpha,
@@ -204,14 +231,15 @@ int swiglu(int act, uint32_t flags, int64_t M, int64_t I, float alpha, float bet
  *
  * Arguments:
  *   fmt           sgq_format_t
+ *   flags         a scale layout flag of the format, or 0 (others rejected)
  *   M, W          rows and width (W a multiple of the group, <= SGQ_MAX_WIDTH)
  *   src           [M, W] bf16, read
  *   q_out         [M, W] E4M3, written
- *   scale_out     scales in the layout of fmt, written
+ *   scale_out     scales in the layout of fmt and flags, written
  *   stream        the stream to launch on
  */
-int quantize_fp8(int fmt, int64_t M, int64_t W, const void* src, void* q_out, void* scale_out,
-                 sgq_stream_t stream);
+int quantize_fp8(int fmt, uint32_t flags, int64_t M, int64_t W, const void* src, void* q_out,
+                 void* scale_out, sgq_stream_t stream);
 
 /* A static, human-readable name of a status code. */
 const char* sgq_status_string(int status);

@@ -5,7 +5,8 @@ benchmark's CPU-baseline leg use it; the library's product path never imports
 it. It wraps `sgq_oracle.c` (plain fp64 C, scalar loops) through ctypes and
 takes and returns numpy arrays. Inputs are raw bf16 bit patterns (uint16).
 
-Every function computes the definitions stated in `sgq_oracle.c`. Parity pins
+Every function computes the definitions stated in `sgq_oracle.c`, except
+`scale_layout`, a plain Python rearrangement of finished scales. Parity pins
 (closed forms, brute force and the pages' printed statistics) are in
 tests/test_oracle_*.py.
 """
@@ -164,3 +165,49 @@ def quantize(fmt: str, src: np.ndarray, *, diagnostics: bool = True, rel: float 
     if rc != 0:
         raise ValueError(f"oracle rejected arguments (fmt={fmt}, M={M}, W={W})")
     return {"q": q, "scale": s, "t": t, "amb": amb, "gamb": gamb}
+
+
+def scale_layout(fmt: str, scale: np.ndarray, layout: str) -> np.ndarray:
+    """Rearrange row-major scales [M, G] into another consumer layout.
+
+    "row":       unchanged.
+    "swizzled":  (MXFP8) the tiled scale-factor layout of block-scaled MMA
+                 operands: rows padded to a multiple of 128 and columns to a
+                 multiple of 4 with zeros; the padded [Mp, Gp] array is cut
+                 into tiles of 128 rows x 4 columns, which are laid out one
+                 after another, tile columns fastest; inside a tile, row r
+                 and column g go to position (r % 32) * 16 + (r // 32) * 4 + g.
+                 Returned as [Mp, Gp] (the flat buffer, reshaped).
+    "col_major": (1x128) the transpose [G, Mp], rows padded to a multiple of 4
+                 with zeros.
+
+    Scale layouts are a convention of the consumer GEMM: the review section
+    "Scale layout / scheme contract" of "[ROCm][MiniMax-M3.1] Fuse MXFP8 quant
+    into the add+RMSNorm and SwiGLU epilogues" separates consumers of
+    row-major [M, N/32] E8M0 scales from consumers of swizzled ones. Written
+    as plain loops over the entries.
+    """
+    scale = np.asarray(scale)
+    M, G = scale.shape
+    if layout == "row":
+        return scale.copy()
+    if layout == "swizzled":
+        assert fmt == "mxfp8"
+        Mp, Gp = -(-M // 128) * 128, -(-G // 4) * 4
+        flat = np.zeros(Mp * Gp, dtype=scale.dtype)
+        tiles_per_band = Gp // 4
+        for r in range(M):
+            for g in range(G):
+                tile = (r // 128) * tiles_per_band + g // 4
+                rr, gg = r % 128, g % 4
+                flat[tile * 512 + (rr % 32) * 16 + (rr // 32) * 4 + gg] = scale[r, g]
+        return flat.reshape(Mp, Gp)
+    if layout == "col_major":
+        assert fmt == "block128"
+        Mp = -(-M // 4) * 4
+        out = np.zeros((G, Mp), dtype=scale.dtype)
+        for r in range(M):
+            for g in range(G):
+                out[g, r] = scale[r, g]
+        return out
+    raise ValueError(f"unknown scale layout {layout!r}")

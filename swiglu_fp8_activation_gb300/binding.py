@@ -18,7 +18,10 @@ LIB_NAME = "libsgq.so"
 FORMATS = {"mxfp8": 0, "block128": 1, "per_token": 2}
 ACTS = {"swiglu_oai": 0, "silu_mul": 1}
 F_GEMMA_WEIGHT, F_QUANT_FROM_FP32, F_ACT_ROUND_BF16 = 1, 2, 4
+F_SCALE_SWIZZLED, F_SCALE_COL_MAJOR = 8, 16
 GROUP = {"mxfp8": 32, "block128": 128}
+# scale layouts: name -> (flag, the one format it applies to, or None for all)
+SCALE_LAYOUTS = {"row": (0, None), "swizzled": (F_SCALE_SWIZZLED, "mxfp8"), "col_major": (F_SCALE_COL_MAJOR, "block128")}
 
 _lib = None
 
@@ -55,7 +58,7 @@ def library() -> C.CDLL:
         L.swiglu.restype = C.c_int
         L.swiglu.argtypes = [C.c_int, C.c_uint32, i64, i64, C.c_float, C.c_float, C.c_float, vp, vp, vp]
         L.quantize_fp8.restype = C.c_int
-        L.quantize_fp8.argtypes = [C.c_int, i64, i64, vp, vp, vp, vp]
+        L.quantize_fp8.argtypes = [C.c_int, C.c_uint32, i64, i64, vp, vp, vp, vp]
         L.sgq_status_string.restype = C.c_char_p
         L.sgq_status_string.argtypes = [C.c_int]
         L.sgq_abi_version.restype = C.c_int
@@ -86,8 +89,28 @@ def _stream(stream) -> C.c_void_p:
     return C.c_void_p(stream.cuda_stream)
 
 
-def scale_shape(fmt: str, M: int, W: int) -> tuple:
+def _round_up(v: int, m: int) -> int:
+    return (v + m - 1) // m * m
+
+
+def scale_shape(fmt: str, M: int, W: int, layout: str = "row") -> tuple:
+    """Shape of the scale tensor: row-major [M, groups] ([M, 1] per-token);
+    swizzled MXFP8 [M rounded up to 128, groups rounded up to 4] holding the
+    512-byte tiles in order; column-major 1x128 [groups, M rounded up to 4]."""
+    if layout == "swizzled":
+        return (_round_up(M, 128), _round_up(W // 32, 4))
+    if layout == "col_major":
+        return (W // 128, _round_up(M, 4))
     return (M, 1) if fmt == "per_token" else (M, W // GROUP[fmt])
+
+
+def _layout_flag(fmt: str, layout: str) -> int:
+    if layout not in SCALE_LAYOUTS:
+        raise SgqError(f"unknown scale layout {layout!r}")
+    flag, only = SCALE_LAYOUTS[layout]
+    if only is not None and fmt != only:
+        raise SgqError(f"scale layout {layout!r} applies to {only} only, not {fmt}")
+    return flag
 
 
 def scale_dtype(fmt: str) -> torch.dtype:
@@ -106,7 +129,7 @@ def rmsnorm_add_quant(x: torch.Tensor, weight: torch.Tensor, *, fmt: str = "mxfp
                       residual_out: torch.Tensor | None = None, eps: float = 1e-6,
                       gemma: bool = True, quant_from_fp32: bool = False, normed: bool = False,
                       q_out: torch.Tensor | None = None, scale_out: torch.Tensor | None = None,
-                      normed_out: torch.Tensor | None = None, stream=None):
+                      normed_out: torch.Tensor | None = None, scale_layout: str = "row", stream=None):
     """Residual add + RMSNorm + FP8 quantisation (one kernel launch).
 
     x [M,H] bf16; weight [H] bf16; residual_in [M,H] bf16 or None;
@@ -128,15 +151,16 @@ def rmsnorm_add_quant(x: torch.Tensor, weight: torch.Tensor, *, fmt: str = "mxfp
         q_out = torch.empty((M, H), dtype=torch.uint8, device=dev)
     if fmt not in FORMATS:
         raise SgqError(f"unknown format {fmt!r}")
+    lflag = _layout_flag(fmt, scale_layout)
     if scale_out is None:
-        scale_out = torch.empty(scale_shape(fmt, M, H), dtype=scale_dtype(fmt), device=dev)
+        scale_out = torch.empty(scale_shape(fmt, M, H, scale_layout), dtype=scale_dtype(fmt), device=dev)
     if normed and normed_out is None:
         normed_out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
     _want(q_out, (M, H), torch.uint8, "q_out")
-    _want(scale_out, scale_shape(fmt, M, H), scale_dtype(fmt), "scale_out")
+    _want(scale_out, scale_shape(fmt, M, H, scale_layout), scale_dtype(fmt), "scale_out")
     if normed_out is not None:
         _want(normed_out, (M, H), torch.bfloat16, "normed_out")
-    flags = (F_GEMMA_WEIGHT if gemma else 0) | (F_QUANT_FROM_FP32 if quant_from_fp32 else 0)
+    flags = (F_GEMMA_WEIGHT if gemma else 0) | (F_QUANT_FROM_FP32 if quant_from_fp32 else 0) | lflag
     st = library().rmsnorm_add_quant(FORMATS[fmt], flags, M, H, float(eps), _ptr(x),
                                      _ptr(residual_in), _ptr(residual_out), _ptr(weight),
                                      _ptr(q_out), _ptr(scale_out), _ptr(normed_out), _stream(stream))
@@ -147,7 +171,7 @@ def rmsnorm_add_quant(x: torch.Tensor, weight: torch.Tensor, *, fmt: str = "mxfp
 def swiglu_quant(gate_up: torch.Tensor, *, fmt: str = "mxfp8", act: str = "swiglu_oai",
                  quant_from_fp32: bool = True, round_act_bf16: bool = False, alpha: float = 1.702,
                  beta: float = 1.0, limit: float = 7.0, q_out: torch.Tensor | None = None,
-                 scale_out: torch.Tensor | None = None, stream=None):
+                 scale_out: torch.Tensor | None = None, scale_layout: str = "row", stream=None):
     """SwiGLU + FP8 quantisation (one kernel launch).
 
     gate_up [M, 2I] bf16 (gate = first half, up = second half). Returns
@@ -161,13 +185,14 @@ def swiglu_quant(gate_up: torch.Tensor, *, fmt: str = "mxfp8", act: str = "swigl
     if fmt not in FORMATS or act not in ACTS:
         raise SgqError(f"unknown format/activation {fmt!r}/{act!r}")
     dev = gate_up.device
+    lflag = _layout_flag(fmt, scale_layout)
     if q_out is None:
         q_out = torch.empty((M, I), dtype=torch.uint8, device=dev)
     if scale_out is None:
-        scale_out = torch.empty(scale_shape(fmt, M, I), dtype=scale_dtype(fmt), device=dev)
+        scale_out = torch.empty(scale_shape(fmt, M, I, scale_layout), dtype=scale_dtype(fmt), device=dev)
     _want(q_out, (M, I), torch.uint8, "q_out")
-    _want(scale_out, scale_shape(fmt, M, I), scale_dtype(fmt), "scale_out")
-    flags = (F_QUANT_FROM_FP32 if quant_from_fp32 else 0) | (F_ACT_ROUND_BF16 if round_act_bf16 else 0)
+    _want(scale_out, scale_shape(fmt, M, I, scale_layout), scale_dtype(fmt), "scale_out")
+    flags = (F_QUANT_FROM_FP32 if quant_from_fp32 else 0) | (F_ACT_ROUND_BF16 if round_act_bf16 else 0) | lflag
     st = library().swiglu_quant(FORMATS[fmt], ACTS[act], flags, M, I, float(alpha), float(beta),
                                 float(limit), _ptr(gate_up), _ptr(q_out), _ptr(scale_out), _stream(stream))
     _check(st, "swiglu_quant")
@@ -224,7 +249,7 @@ def swiglu(gate_up: torch.Tensor, *, act: str = "swiglu_oai", round_act_bf16: bo
 
 
 def quantize_fp8(src: torch.Tensor, *, fmt: str = "mxfp8", q_out: torch.Tensor | None = None,
-                 scale_out: torch.Tensor | None = None, stream=None):
+                 scale_out: torch.Tensor | None = None, scale_layout: str = "row", stream=None):
     """FP8 quantisation of bf16 rows (the separate quant of the unfused chain).
 
     src [M, W] bf16. Returns (q [M,W] uint8 E4M3, scale).
@@ -233,12 +258,14 @@ def quantize_fp8(src: torch.Tensor, *, fmt: str = "mxfp8", q_out: torch.Tensor |
     _want(src, (M, W), torch.bfloat16, "src")
     if fmt not in FORMATS:
         raise SgqError(f"unknown format {fmt!r}")
+    lflag = _layout_flag(fmt, scale_layout)
     if q_out is None:
         q_out = torch.empty((M, W), dtype=torch.uint8, device=src.device)
     if scale_out is None:
-        scale_out = torch.empty(scale_shape(fmt, M, W), dtype=scale_dtype(fmt), device=src.device)
+        scale_out = torch.empty(scale_shape(fmt, M, W, scale_layout), dtype=scale_dtype(fmt), device=src.device)
     _want(q_out, (M, W), torch.uint8, "q_out")
-    _want(scale_out, scale_shape(fmt, M, W), scale_dtype(fmt), "scale_out")
-    st = library().quantize_fp8(FORMATS[fmt], M, W, _ptr(src), _ptr(q_out), _ptr(scale_out), _stream(stream))
+    _want(scale_out, scale_shape(fmt, M, W, scale_layout), scale_dtype(fmt), "scale_out")
+    st = library().quantize_fp8(FORMATS[fmt], lflag, M, W, _ptr(src), _ptr(q_out), _ptr(scale_out),
+                                _stream(stream))
     _check(st, "quantize_fp8")
     return q_out, scale_out

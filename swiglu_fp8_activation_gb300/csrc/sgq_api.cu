@@ -76,10 +76,45 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
 
 int group_of(int fmt) { return fmt == SGQ_FMT_MXFP8 ? 32 : fmt == SGQ_FMT_FP8_BLOCK128 ? 128 : 8; }
 
-size_t scale_bytes(int fmt, int64_t M, int64_t W) {
-    if (fmt == SGQ_FMT_MXFP8) return (size_t)(M * (W / 32));
-    if (fmt == SGQ_FMT_FP8_BLOCK128) return (size_t)(M * (W / 128)) * 4;
-    return (size_t)M * 4;
+int sm_count();
+
+constexpr uint32_t kLayoutFlags = SGQ_F_SCALE_SWIZZLED | SGQ_F_SCALE_COL_MAJOR;
+
+int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+// The scale layout the flags select for format fmt at [M, W], and its size
+// in bytes. False when a layout flag does not belong to the format.
+bool scale_geometry(int fmt, uint32_t flags, int64_t M, int64_t W, sgq::ScaleOut* so, size_t* bytes) {
+    const bool swz = (flags & SGQ_F_SCALE_SWIZZLED) != 0, col = (flags & SGQ_F_SCALE_COL_MAJOR) != 0;
+    so->ng = (int)(fmt == SGQ_FMT_FP8_PER_TOKEN ? 1 : W / group_of(fmt));
+    so->layout = sgq::SCALE_ROW_MAJOR;
+    so->ld = so->ng;
+    so->Ms = M;
+    if (swz && (col || fmt != SGQ_FMT_MXFP8)) return false;
+    if (col && fmt != SGQ_FMT_FP8_BLOCK128) return false;
+    if (swz) {
+        so->layout = sgq::SCALE_SWIZZLED;
+        so->ld = round_up(so->ng, 4) / 4;          // 512-byte tiles per 128-row band
+        so->Ms = round_up(M, 128);
+        *bytes = (size_t)so->Ms * (size_t)round_up(so->ng, 4);
+    } else if (col) {
+        so->layout = sgq::SCALE_COL_MAJOR;
+        so->ld = round_up(M, 4);
+        so->Ms = so->ld;
+        *bytes = (size_t)so->ng * (size_t)so->ld * 4;
+    } else {
+        *bytes = (size_t)M * (size_t)so->ng * (fmt == SGQ_FMT_MXFP8 ? 1 : 4);
+    }
+    return true;
+}
+
+// Plan the rows of a launch whose scale layout covers so.Ms >= M rows: the
+// grid covers the layout's padding rows too, and the exact-fit kernels only
+// run when there are none.
+bool plan_launch(int64_t M, int W, const sgq::ScaleOut& so, sgq::Plan* p) {
+    if (!sgq::plan_rows(so.Ms, W, sm_count(), p)) return false;
+    p->full = p->full && so.Ms == M;
+    return true;
 }
 
 int sm_count() {
@@ -121,6 +156,10 @@ int norm_call(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, const vo
     if (M == 0) return SGQ_OK;
     if (!x || !weight) return SGQ_ERR_INVALID_ARG;
     if (residual_out && !residual_in) return SGQ_ERR_INVALID_ARG;
+    sgq::ScaleOut so;
+    size_t sbytes = 0;
+    if (!scale_geometry(fmt, flags, M, H, &so, &sbytes)) return SGQ_ERR_INVALID_ARG;
+    if (!q_out) sbytes = 0;
     if (!aligned(x, 16) || !aligned(residual_in, 16) || !aligned(residual_out, 16) || !aligned(weight, 16) ||
         !aligned(q_out, 16) || !aligned(normed_out, 16) || !aligned(scale_out, fmt == SGQ_FMT_MXFP8 ? 1 : 4))
         return SGQ_ERR_MISALIGNED;
@@ -131,20 +170,21 @@ int norm_call(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, const vo
                           {residual_in, act},
                           {weight, (size_t)H * 2},
                           {q_out, (size_t)M * H},
-                          {scale_out, q_out ? scale_bytes(fmt, M, H) : 0},
+                          {scale_out, sbytes},
                           {normed_out, act},
                           {r_out_span, act}};
     if (any_overlap(spans, 7)) return SGQ_ERR_INVALID_ARG;
 
     sgq::Plan plan;
-    if (!sgq::plan_rows(M, (int)H, sm_count(), &plan)) return SGQ_ERR_UNSUPPORTED;
+    if (!plan_launch(M, (int)H, so, &plan)) return SGQ_ERR_UNSUPPORTED;
     sgq::NormArgs a;
     a.x = static_cast<const uint16_t*>(x);
     a.r_in = static_cast<const uint16_t*>(residual_in);
     a.r_out = static_cast<uint16_t*>(residual_out);
     a.w = static_cast<const uint16_t*>(weight);
     a.q = static_cast<uint8_t*>(q_out);
-    a.scale = scale_out;
+    so.p = scale_out;
+    a.so = so;
     a.normed = static_cast<uint16_t*>(normed_out);
     a.M = M;
     a.H = (int)H;
@@ -168,21 +208,26 @@ int swiglu_call(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float al
     if (M > kMaxElements / (2 * I)) return SGQ_ERR_INVALID_ARG;
     if (M == 0) return SGQ_OK;
     if (!gate_up) return SGQ_ERR_INVALID_ARG;
+    sgq::ScaleOut so;
+    size_t sbytes = 0;
+    if (!scale_geometry(fmt, flags, M, I, &so, &sbytes)) return SGQ_ERR_INVALID_ARG;
+    if (!q_out) sbytes = 0;
     if (!aligned(gate_up, 16) || !aligned(q_out, 16) || !aligned(out, 16) ||
         !aligned(scale_out, fmt == SGQ_FMT_MXFP8 ? 1 : 4))
         return SGQ_ERR_MISALIGNED;
     const Span spans[] = {{gate_up, (size_t)M * I * 4},
                           {q_out, (size_t)M * I},
-                          {scale_out, q_out ? scale_bytes(fmt, M, I) : 0},
+                          {scale_out, sbytes},
                           {out, (size_t)M * I * 2}};
     if (any_overlap(spans, 4)) return SGQ_ERR_INVALID_ARG;
 
     sgq::Plan plan;
-    if (!sgq::plan_rows(M, (int)I, sm_count(), &plan)) return SGQ_ERR_UNSUPPORTED;
+    if (!plan_launch(M, (int)I, so, &plan)) return SGQ_ERR_UNSUPPORTED;
     sgq::SwigluArgs a;
     a.gu = static_cast<const uint16_t*>(gate_up);
     a.q = static_cast<uint8_t*>(q_out);
-    a.scale = scale_out;
+    so.p = scale_out;
+    a.so = so;
     a.out = static_cast<uint16_t*>(out);
     a.M = M;
     a.I = (int)I;
@@ -221,7 +266,7 @@ int rmsnorm_add_quant(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, 
                       const void* residual_in, void* residual_out, const void* weight, void* q_out,
                       void* scale_out, void* normed_out, sgq_stream_t stream) {
     if (fmt < SGQ_FMT_MXFP8 || fmt > SGQ_FMT_FP8_PER_TOKEN) return SGQ_ERR_INVALID_ARG;
-    if (flags & ~(SGQ_F_GEMMA_WEIGHT | SGQ_F_QUANT_FROM_FP32)) return SGQ_ERR_INVALID_ARG;
+    if (flags & ~(SGQ_F_GEMMA_WEIGHT | SGQ_F_QUANT_FROM_FP32 | kLayoutFlags)) return SGQ_ERR_INVALID_ARG;
     if (H > 0 && H % group_of(fmt) != 0) return SGQ_ERR_UNSUPPORTED;
     if (M > 0 && (!q_out || !scale_out)) return SGQ_ERR_INVALID_ARG;
     return norm_call(fmt, flags, M, H, eps, x, residual_in, residual_out, weight, q_out, scale_out, normed_out,
@@ -240,7 +285,7 @@ int rmsnorm_add(uint32_t flags, int64_t M, int64_t H, float eps, const void* x, 
 int swiglu_quant(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float alpha, float beta,
                  float limit, const void* gate_up, void* q_out, void* scale_out, sgq_stream_t stream) {
     if (fmt < SGQ_FMT_MXFP8 || fmt > SGQ_FMT_FP8_PER_TOKEN) return SGQ_ERR_INVALID_ARG;
-    if (flags & ~(SGQ_F_QUANT_FROM_FP32 | SGQ_F_ACT_ROUND_BF16)) return SGQ_ERR_INVALID_ARG;
+    if (flags & ~(SGQ_F_QUANT_FROM_FP32 | SGQ_F_ACT_ROUND_BF16 | kLayoutFlags)) return SGQ_ERR_INVALID_ARG;
     if (I > 0 && I % group_of(fmt) != 0) return SGQ_ERR_UNSUPPORTED;
     if (M > 0 && (!q_out || !scale_out)) return SGQ_ERR_INVALID_ARG;
     return swiglu_call(fmt, act, flags, M, I, alpha, beta, limit, gate_up, q_out, scale_out, nullptr, stream);
@@ -254,24 +299,30 @@ int swiglu(int act, uint32_t flags, int64_t M, int64_t I, float alpha, float bet
     return swiglu_call(SGQ_FMT_MXFP8, act, flags, M, I, alpha, beta, limit, gate_up, nullptr, nullptr, out, stream);
 }
 
-int quantize_fp8(int fmt, int64_t M, int64_t W, const void* src, void* q_out, void* scale_out, sgq_stream_t stream) {
+int quantize_fp8(int fmt, uint32_t flags, int64_t M, int64_t W, const void* src, void* q_out, void* scale_out,
+                 sgq_stream_t stream) {
     if (fmt < SGQ_FMT_MXFP8 || fmt > SGQ_FMT_FP8_PER_TOKEN) return SGQ_ERR_INVALID_ARG;
+    if (flags & ~kLayoutFlags) return SGQ_ERR_INVALID_ARG;
     if (M < 0 || W <= 0) return SGQ_ERR_INVALID_ARG;
     if (W % group_of(fmt) != 0 || W > SGQ_MAX_WIDTH) return SGQ_ERR_UNSUPPORTED;
     if (M > kMaxElements / W) return SGQ_ERR_INVALID_ARG;
     if (M == 0) return SGQ_OK;
     if (!src || !q_out || !scale_out) return SGQ_ERR_INVALID_ARG;
+    sgq::ScaleOut so;
+    size_t sbytes = 0;
+    if (!scale_geometry(fmt, flags, M, W, &so, &sbytes)) return SGQ_ERR_INVALID_ARG;
     if (!aligned(src, 16) || !aligned(q_out, 16) || !aligned(scale_out, fmt == SGQ_FMT_MXFP8 ? 1 : 4))
         return SGQ_ERR_MISALIGNED;
-    const Span spans[] = {{src, (size_t)M * W * 2}, {q_out, (size_t)M * W}, {scale_out, scale_bytes(fmt, M, W)}};
+    const Span spans[] = {{src, (size_t)M * W * 2}, {q_out, (size_t)M * W}, {scale_out, sbytes}};
     if (any_overlap(spans, 3)) return SGQ_ERR_INVALID_ARG;
 
     sgq::Plan plan;
-    if (!sgq::plan_rows(M, (int)W, sm_count(), &plan)) return SGQ_ERR_UNSUPPORTED;
+    if (!plan_launch(M, (int)W, so, &plan)) return SGQ_ERR_UNSUPPORTED;
     sgq::QuantArgs a;
     a.src = static_cast<const uint16_t*>(src);
     a.q = static_cast<uint8_t*>(q_out);
-    a.scale = scale_out;
+    so.p = scale_out;
+    a.so = so;
     a.M = M;
     a.W = (int)W;
     a.tpr = plan.tpr;

@@ -33,6 +33,7 @@ namespace sgq {
 
 enum Fmt : int { FMT_MX = 0, FMT_B128 = 1, FMT_PT = 2 };
 enum Act : int { ACT_OAI = 0, ACT_SILU = 1 };
+enum ScaleLayout : int { SCALE_ROW_MAJOR = 0, SCALE_SWIZZLED = 1, SCALE_COL_MAJOR = 2 };
 
 constexpr uint32_t F_GEMMA = 1u << 0;
 constexpr uint32_t F_FROM_FP32 = 1u << 1;

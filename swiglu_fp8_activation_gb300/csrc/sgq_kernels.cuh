@@ -7,13 +7,30 @@
 
 namespace sgq {
 
+// Where a kernel writes its scales. Scales of group g of row `row` go to
+// base(row) + (g / 4) * s4 + (g % 4) * s1 bytes (scale_row), which covers:
+//   SCALE_ROW_MAJOR  [M, ng] row-major;
+//   SCALE_SWIZZLED   MXFP8 E8M0 in 128 x 4 tiles of 512 bytes, tiles row-major
+//                    over (M/128 bands) x (ng/4 tile columns); inside a tile,
+//                    row r and column j at (r % 32) * 16 + (r / 32) * 4 + j;
+//   SCALE_COL_MAJOR  fp32 [ng, ld] (group-major), ld = M rounded up to 4.
+// Rows in [M, Ms) are padding of the layout: their scales are written as
+// zero (their inputs read as zero), and nothing else of them is written.
+struct ScaleOut {
+    void* p;
+    int64_t ld;       // SCALE_SWIZZLED: tiles per 128-row band; SCALE_COL_MAJOR: leading dimension
+    int64_t Ms;       // rows whose scales are written (M, or M padded to the layout's row multiple)
+    int ng;           // groups per row
+    int layout;       // SCALE_*
+};
+
 struct NormArgs {
     const uint16_t* x;       // [M, H] bf16
     const uint16_t* r_in;    // [M, H] bf16 or null
     uint16_t* r_out;         // [M, H] bf16 or null (may equal r_in)
     const uint16_t* w;       // [H] bf16
-    uint8_t* q;              // [M, H] E4M3
-    void* scale;             // format-dependent scale array
+    uint8_t* q;              // [M, H] E4M3, or null (no quantisation)
+    ScaleOut so;
     uint16_t* normed;        // [M, H] bf16 or null
     int64_t M;
     int H;
@@ -26,7 +43,7 @@ struct NormArgs {
 struct SwigluArgs {
     const uint16_t* gu;      // [M, 2I] bf16: gate = [0, I), up = [I, 2I)
     uint8_t* q;              // [M, I] E4M3 (null when `out` is set)
-    void* scale;
+    ScaleOut so;
     uint16_t* out;           // [M, I] bf16 activation instead of quantising, or null
     int64_t M;
     int I;
@@ -40,26 +57,65 @@ struct SwigluArgs {
 struct QuantArgs {
     const uint16_t* src;     // [M, W] bf16
     uint8_t* q;              // [M, W] E4M3
-    void* scale;
+    ScaleOut so;
     int64_t M;
     int W;
     int tpr;
     int rpc;
 };
 
+// One row's view of ScaleOut in layout LAYOUT (a compile-time choice, so
+// that each layout's address arithmetic is only what it needs).
+struct ScaleRow {
+    char* base;       // byte address of group 0 of the row
+    int64_t ld4;      // SCALE_COL_MAJOR: bytes from one group's column to the next
+    int pad_last;     // SCALE_SWIZZLED with ng % 4 != 0: the last real group, whose
+                      // tile row is completed with zero codes; else -1
+};
+
+template <int FMT, int LAYOUT>
+__device__ __forceinline__ ScaleRow scale_row(const ScaleOut& so, int64_t row) {
+    char* p = static_cast<char*>(so.p);
+    ScaleRow r;
+    r.ld4 = 0;
+    r.pad_last = -1;
+    if (FMT == FMT_PT) {
+        r.base = p + row * 4;
+    } else if (LAYOUT == SCALE_SWIZZLED) {
+        r.base = p + (row >> 7) * so.ld * 512 + (row & 31) * 16 + ((row >> 5) & 3) * 4;
+        if (so.ng & 3) r.pad_last = so.ng - 1;
+    } else if (LAYOUT == SCALE_COL_MAJOR) {
+        r.base = p + row * 4;
+        r.ld4 = so.ld * 4;
+    } else {
+        r.base = p + row * (int64_t)so.ng * (FMT == FMT_MX ? 1 : 4);
+    }
+    return r;
+}
+
+// Byte address of group g's scale in the row.
+template <int FMT, int LAYOUT>
+__device__ __forceinline__ char* scale_addr(const ScaleRow& r, int g) {
+    if (LAYOUT == SCALE_SWIZZLED) return r.base + ((g >> 2) << 9) + (g & 3);
+    if (LAYOUT == SCALE_COL_MAJOR) return r.base + g * r.ld4;
+    return r.base + g * (FMT == FMT_MX ? 1 : 4);
+}
+
 // Quantise one chunk (8 source values of row `row`, chunk index c) and store
 // its 8 E4M3 codes and, from the first chunk of its group, the scale. Every
 // lane of the warp must call it for MX and 1x128 (the group amax is a lane
-// shuffle); `store` is false for lanes without a valid chunk (their src is 0).
+// shuffle); `store` is false for lanes without a valid chunk (their src is 0)
+// and `sstore` likewise for the scale (true also on the layout's padding rows).
 //   MX:  code = E8M0 of the 1x32 block's amax; q = E4M3(src * 2^(127-code)),
 //        the scaling being exact (a power of two).
 //   FP8: s = amax / 448 (IEEE fp32 division); q = E4M3(src / s) with the IEEE
 //        fp32 quotient (div_rn from one correctly rounded reciprocal per
 //        group); s = 0 (all-zero group) stores s = 0 and q = 0. The per-token
 //        format passes its row scale and reciprocal in (pt_s, pt_r).
-template <int FMT>
-__device__ __forceinline__ void quantize_chunk(const float (&src)[8], int64_t row, int c, bool store, int W,
-                                               uint8_t* q, void* scale, float pt_s = 0.0f, float pt_r = 0.0f) {
+template <int FMT, int LAYOUT>
+__device__ __forceinline__ void quantize_chunk(const float (&src)[8], int64_t row, int c, bool store, bool sstore,
+                                               int W, uint8_t* q, const ScaleRow& sr, float pt_s = 0.0f,
+                                               float pt_r = 0.0f) {
     float m = 0.0f;
     if (FMT != FMT_PT) {
 #pragma unroll
@@ -76,7 +132,13 @@ __device__ __forceinline__ void quantize_chunk(const float (&src)[8], int64_t ro
             tq[k] = t.x;
             tq[k + 1] = t.y;
         }
-        st_u8_if(static_cast<uint8_t*>(scale) + row * (W >> 5) + (c >> 2), code, store && (c & 3) == 0);
+        const int g = c >> 2;
+        uint8_t* sp = reinterpret_cast<uint8_t*>(scale_addr<FMT, LAYOUT>(sr, g));
+        const bool lead = sstore && (c & 3) == 0;
+        st_u8_if(sp, code, lead);
+        if (LAYOUT == SCALE_SWIZZLED && g == sr.pad_last && lead) {   // zero codes complete the last tile row
+            for (int j = (g & 3) + 1; j < 4; ++j) sp[j - (g & 3)] = 0;
+        }
     } else {
         float s = pt_s, r = pt_r;
         if (FMT == FMT_B128) {
@@ -90,8 +152,12 @@ __device__ __forceinline__ void quantize_chunk(const float (&src)[8], int64_t ro
 #pragma unroll
             for (int k = 0; k < 8; ++k) tq[k] = __fdiv_rn(src[k], s);
         }
-        if (FMT == FMT_B128) st_f32_if(static_cast<float*>(scale) + row * (W >> 7) + (c >> 4), s, store && (c & 15) == 0);
-        else st_f32_if(static_cast<float*>(scale) + row, s, store && c == 0);
+        if (FMT == FMT_B128) {
+            const int g = c >> 4;
+            st_f32_if(reinterpret_cast<float*>(scale_addr<FMT, LAYOUT>(sr, g)), s, sstore && (c & 15) == 0);
+        } else {
+            st_f32_if(reinterpret_cast<float*>(sr.base), s, sstore && c == 0);
+        }
     }
     const uint2 packed = make_uint2(f32x4_to_e4m3x4(tq[0], tq[1], tq[2], tq[3]),
                                     f32x4_to_e4m3x4(tq[4], tq[5], tq[6], tq[7]));
@@ -117,7 +183,7 @@ __host__ __device__ constexpr int norm_stage_bytes(bool has_res, int nv, int thr
 
 // FULL: every thread's chunks lie inside the row and every row inside M (the
 // plan divides both exactly), so no bounds are checked.
-template <int FMT, int NV, bool HAS_RES, bool FULL>
+template <int FMT, int LAYOUT, int NV, bool HAS_RES, bool FULL>
 __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
     extern __shared__ uint4 stage[];
     __shared__ float2 part[32];
@@ -187,12 +253,15 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
     } else {
         ss = row_reduce<false>(ss, reinterpret_cast<float*>(part), tpr, lrow);
     }
-    const float inv = __frsqrt_rn(__fdiv_rn(ss, (float)H) + a.eps);
+    float inv = __frsqrt_rn(__fdiv_rn(ss, (float)H) + a.eps);
+    if (!FULL && !row_ok) inv = 0.0f;                          // a padding row of the scale layout: all zero
 
     // 4. y = inv * z; bf16 copy; quant source; quantise (MX and 1x128 chunk by
     //    chunk; per-token after the whole row, with the row scale from ymax).
     //    Without q (the unfused norm) only the bf16 copy is written.
     const bool quant = a.q != nullptr;
+    const bool srow_ok = FULL || row < a.so.Ms;
+    const ScaleRow sr = scale_row<FMT, LAYOUT>(a.so, row);
     float2 pt = make_float2(0.0f, 0.0f);
     if (FMT == FMT_PT) {
         const float ymax = inv * row_zmax;                     // = max |y| exactly
@@ -214,7 +283,7 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
         } else {
             bf16x8_to_f32(yb, src);
         }
-        quantize_chunk<FMT>(src, row, c, ok, H, a.q, a.scale, pt.x, pt.y);
+        quantize_chunk<FMT, LAYOUT>(src, row, c, ok, FULL || (srow_ok && c < nchunks), H, a.q, sr, pt.x, pt.y);
     }
 }
 
@@ -285,7 +354,7 @@ __host__ __device__ constexpr int swiglu_stage_bytes(int nv, int threads) { retu
 // (stage[2v][thread], stage[2v+1][thread]), one commit group per chunk, so
 // the whole row is in flight without holding registers and chunk v is
 // processed as soon as its own group has landed.
-template <int FMT, int NV, int ACT, bool FULL>
+template <int FMT, int LAYOUT, int NV, int ACT, bool FULL>
 __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs a) {
     extern __shared__ uint4 stage[];
     __shared__ float part_amax[32];
@@ -313,6 +382,8 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
 
     const bool round_silu = (a.flags & F_ACT_BF16) != 0, from32 = (a.flags & F_FROM_FP32) != 0;
     const float2 gr = oai_gate_range(a.alpha);
+    const bool srow_ok = FULL || row < a.so.Ms;
+    const ScaleRow sr = scale_row<FMT, LAYOUT>(a.so, row);
     if (FMT != FMT_PT) {               // MX and 1x128: chunk by chunk, as each lands
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
@@ -331,7 +402,8 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
                 for (int k = 0; k < 8; ++k) src[k] = round_bf16(src[k]);
             }
             // chunks past the row end loaded zeros, and every activation of 0 and 0 is 0
-            quantize_chunk<FMT>(src, row, c, FULL || (row_ok && c < nchunks), I, a.q, a.scale);
+            quantize_chunk<FMT, LAYOUT>(src, row, c, FULL || (row_ok && c < nchunks), FULL || (srow_ok && c < nchunks), I,
+                                a.q, sr);
         }
     } else {                           // per-token: the whole row, then its amax
         float src[NV][8];
@@ -353,7 +425,8 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
             const int c = t + v * tpr;
-            quantize_chunk<FMT>(src[v], row, c, FULL || (row_ok && c < nchunks), I, a.q, a.scale, pt.x, pt.y);
+            quantize_chunk<FMT, LAYOUT>(src[v], row, c, FULL || (row_ok && c < nchunks), FULL || (srow_ok && c < nchunks),
+                                I, a.q, sr, pt.x, pt.y);
         }
     }
 }
@@ -364,7 +437,7 @@ __host__ __device__ constexpr int quant_stage_bytes(int nv, int threads) { retur
 // Standalone FP8 quantisation of bf16 rows (the quant of the unfused
 // chains). Same row engine and quantiser as the fused kernels; the source is
 // the bf16 value itself.
-template <int FMT, int NV, bool FULL>
+template <int FMT, int LAYOUT, int NV, bool FULL>
 __global__ void __launch_bounds__(kMaxTPR) quant_kernel(const QuantArgs a) {
     extern __shared__ uint4 stage[];
     __shared__ float part_amax[32];
@@ -388,6 +461,8 @@ __global__ void __launch_bounds__(kMaxTPR) quant_kernel(const QuantArgs a) {
     }
     pdl_trigger();
 
+    const bool srow_ok = FULL || row < a.so.Ms;
+    const ScaleRow sr = scale_row<FMT, LAYOUT>(a.so, row);
     if (FMT != FMT_PT) {
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
@@ -395,7 +470,8 @@ __global__ void __launch_bounds__(kMaxTPR) quant_kernel(const QuantArgs a) {
             float src[8];
             cp_async_wait_group_of<NV>(v);
             bf16x8_to_f32(ld_smem16(&stage[v * nt + threadIdx.x]), src);
-            quantize_chunk<FMT>(src, row, c, FULL || (row_ok && c < nchunks), W, a.q, a.scale);
+            quantize_chunk<FMT, LAYOUT>(src, row, c, FULL || (row_ok && c < nchunks), FULL || (srow_ok && c < nchunks), W,
+                                a.q, sr);
         }
     } else {
         float src[NV][8];
@@ -411,7 +487,8 @@ __global__ void __launch_bounds__(kMaxTPR) quant_kernel(const QuantArgs a) {
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
             const int c = t + v * tpr;
-            quantize_chunk<FMT>(src[v], row, c, FULL || (row_ok && c < nchunks), W, a.q, a.scale, pt.x, pt.y);
+            quantize_chunk<FMT, LAYOUT>(src[v], row, c, FULL || (row_ok && c < nchunks), FULL || (srow_ok && c < nchunks),
+                                W, a.q, sr, pt.x, pt.y);
         }
     }
 }

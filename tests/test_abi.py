@@ -136,8 +136,8 @@ def act_only(lib, act=0, flags=0, M=8, I=256, alpha=1.702, beta=1.0, limit=7.0, 
     return lib.swiglu(act, flags, M, I, alpha, beta, limit, gu, out, None)
 
 
-def quant(lib, fmt=0, M=8, W=256, src=_p(0), q=_p(1), s=_p(2)):
-    return lib.quantize_fp8(fmt, M, W, src, q, s, None)
+def quant(lib, fmt=0, flags=0, M=8, W=256, src=_p(0), q=_p(1), s=_p(2)):
+    return lib.quantize_fp8(fmt, flags, M, W, src, q, s, None)
 
 
 def test_unfused_norm_argument_errors(sgq_lib):
@@ -187,6 +187,32 @@ def test_quantize_argument_errors(sgq_lib):
     assert quant(L, fmt=2, s=C.c_void_p(BASE + 2 * 64 * MB + 2)) == MISALIGNED
     assert quant(L, q=_p(0)) == INVALID               # q_out overlaps src
     assert quant(L, M=1 << 45, W=16384) == INVALID
+    assert quant(L, flags=1) == INVALID               # GEMMA_WEIGHT is not a quant flag
+    assert quant(L, flags=2) == INVALID               # nor QUANT_FROM_FP32 (the source is bf16)
+
+
+SWZ, COL = 1 << 3, 1 << 4
+
+
+def test_scale_layout_flags(sgq_lib):
+    L = sgq_lib
+    # each layout flag belongs to one format
+    assert quant(L, fmt=1, flags=SWZ) == INVALID
+    assert quant(L, fmt=2, flags=SWZ) == INVALID
+    assert quant(L, fmt=0, flags=COL) == INVALID
+    assert quant(L, fmt=2, flags=COL) == INVALID
+    assert quant(L, fmt=0, flags=SWZ | COL) == INVALID
+    assert norm(L, fmt=1, flags=1 | SWZ) == INVALID
+    assert norm(L, fmt=0, flags=1 | COL) == INVALID
+    assert swiglu(L, fmt=2, flags=2 | COL) == INVALID
+    assert norm_only(L, flags=1 | SWZ) == INVALID     # no quantisation, so no scale layout
+    assert act_only(L, flags=COL) == INVALID
+    # the overlap checks use the padded sizes: 8 rows swizzled take 128 * 8 scale bytes at W = 256
+    base = BASE + 2 * 64 * MB
+    assert quant(L, M=0, flags=SWZ) == OK
+    assert quant(L, flags=SWZ, s=C.c_void_p(base), q=C.c_void_p(base + 128 * 8 - 16)) == INVALID
+    # column-major 1x128 at M = 5, W = 512: 4 groups x 8 padded rows x 4 bytes
+    assert quant(L, fmt=1, flags=COL, M=5, W=512, s=C.c_void_p(base), q=C.c_void_p(base + 4 * 8 * 4 - 16)) == INVALID
 
 
 def test_binding_rejects_wrong_tensors():
