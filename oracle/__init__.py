@@ -20,7 +20,7 @@ from .build import build_oracle
 
 FORMATS = {"mxfp8": 0, "block128": 1, "per_token": 2}
 ACTS = {"swiglu_oai": 0, "silu_mul": 1}
-F_GEMMA, F_FROM_FP32, F_ACT_ROUND_BF16 = 1, 2, 4
+F_GEMMA, F_FROM_FP32, F_ACT_ROUND_BF16, F_FP16 = 1, 2, 4, 32
 AMB_SRC, AMB_CODE, AMB_TIE = 1, 2, 4
 REL_WINDOW = 2.0 ** -20
 
@@ -35,6 +35,10 @@ def lib() -> C.CDLL:
         L.ora_bf16_decode.argtypes = [C.c_uint16]
         L.ora_bf16_round.restype = C.c_uint16
         L.ora_bf16_round.argtypes = [C.c_double]
+        L.ora_f16_decode.restype = C.c_double
+        L.ora_f16_decode.argtypes = [C.c_uint16]
+        L.ora_f16_round.restype = C.c_uint16
+        L.ora_f16_round.argtypes = [C.c_double]
         L.ora_e4m3_decode.restype = C.c_double
         L.ora_e4m3_decode.argtypes = [C.c_uint8]
         L.ora_e4m3_encode.restype = C.c_uint8
@@ -49,7 +53,7 @@ def lib() -> C.CDLL:
         L.ora_swiglu_quant.argtypes = [C.c_int, C.c_int, C.c_uint, C.c_long, C.c_long, C.c_float,
                                        C.c_float, C.c_float, p, p, p, p, p, p, p, C.c_double]
         L.ora_quantize.restype = C.c_int
-        L.ora_quantize.argtypes = [C.c_int, C.c_long, C.c_long, p, p, p, p, p, p, C.c_double]
+        L.ora_quantize.argtypes = [C.c_int, C.c_uint, C.c_long, C.c_long, p, p, p, p, p, p, C.c_double]
         _lib = L
     return _lib
 
@@ -95,8 +99,9 @@ def _u16(a, shape):
 
 def rmsnorm_add_quant(fmt: str, x: np.ndarray, r: np.ndarray | None, w: np.ndarray, *,
                       eps: float, gemma: bool, from_fp32: bool, normed: bool = True,
-                      diagnostics: bool = True, rel: float = REL_WINDOW) -> dict:
-    """Residual add + RMSNorm + FP8 quantisation of rows x [M,H] (bf16 bits).
+                      diagnostics: bool = True, rel: float = REL_WINDOW, fp16: bool = False) -> dict:
+    """Residual add + RMSNorm + FP8 quantisation of rows x [M,H] (bf16 bits,
+    or fp16 bits with fp16=True, which also makes the written rows fp16).
 
     Returns q (uint8 [M,H]), scale ([M,G] uint8 E8M0 codes or float32),
     residual (uint16 bits or None), normed (uint16 bits or None) and, with
@@ -114,7 +119,7 @@ def rmsnorm_add_quant(fmt: str, x: np.ndarray, r: np.ndarray | None, w: np.ndarr
     if diagnostics:
         y, t = np.zeros((M, H)), np.zeros((M, H))
         amb, gamb = np.zeros((M, H), np.uint8), np.zeros(s.shape, np.uint8)
-    flags = (F_GEMMA if gemma else 0) | (F_FROM_FP32 if from_fp32 else 0)
+    flags = (F_GEMMA if gemma else 0) | (F_FROM_FP32 if from_fp32 else 0) | (F_FP16 if fp16 else 0)
     rc = lib().ora_rmsnorm_add_quant(FORMATS[fmt], flags, M, H, float(eps), _ptr(x), _ptr(r), _ptr(w),
                                      _ptr(r_out), _ptr(n_out), _ptr(q), _ptr(s), _ptr(y), _ptr(t),
                                      _ptr(amb), _ptr(gamb), rel)
@@ -150,10 +155,11 @@ def swiglu_quant(fmt: str, act: str, gate_up: np.ndarray, *, from_fp32: bool,
     return {"q": q, "scale": s, "a": a, "t": t, "amb": amb, "gamb": gamb}
 
 
-def quantize(fmt: str, src: np.ndarray, *, diagnostics: bool = True, rel: float = REL_WINDOW) -> dict:
-    """Standalone FP8 quantisation of bf16 rows src [M, W] (bf16 bits): the
-    quant of the unfused chains. Returns q, scale and, with diagnostics, t,
-    amb and gamb."""
+def quantize(fmt: str, src: np.ndarray, *, diagnostics: bool = True, rel: float = REL_WINDOW,
+             fp16: bool = False) -> dict:
+    """Standalone FP8 quantisation of bf16 rows src [M, W] (bf16 bits, or fp16
+    bits with fp16=True): the quant of the unfused chains. Returns q, scale
+    and, with diagnostics, t, amb and gamb."""
     M, W = src.shape
     src = _u16(src, (M, W))
     q = np.zeros((M, W), np.uint8)
@@ -161,7 +167,7 @@ def quantize(fmt: str, src: np.ndarray, *, diagnostics: bool = True, rel: float 
     t = amb = gamb = None
     if diagnostics:
         t, amb, gamb = np.zeros((M, W)), np.zeros((M, W), np.uint8), np.zeros(s.shape, np.uint8)
-    rc = lib().ora_quantize(FORMATS[fmt], M, W, _ptr(src), _ptr(q), _ptr(s), _ptr(t), _ptr(amb), _ptr(gamb), rel)
+    rc = lib().ora_quantize(FORMATS[fmt], F_FP16 if fp16 else 0, M, W, _ptr(src), _ptr(q), _ptr(s), _ptr(t), _ptr(amb), _ptr(gamb), rel)
     if rc != 0:
         raise ValueError(f"oracle rejected arguments (fmt={fmt}, M={M}, W={W})")
     return {"q": q, "scale": s, "t": t, "amb": amb, "gamb": gamb}
@@ -211,3 +217,24 @@ def scale_layout(fmt: str, scale: np.ndarray, layout: str) -> np.ndarray:
                 out[g, r] = scale[r, g]
         return out
     raise ValueError(f"unknown scale layout {layout!r}")
+
+
+def f16_decode(b: int) -> float:
+    return lib().ora_f16_decode(int(b))
+
+
+def f16_round(v: float) -> int:
+    return lib().ora_f16_round(float(v))
+
+
+def rmsnorm_dual_quant(fmt: str, xa: np.ndarray, wa: np.ndarray, xb: np.ndarray, wb: np.ndarray, *, eps: float,
+                       gemma: bool, from_fp32: bool, fp16: bool = False, **kw) -> tuple:
+    """Two independent RMSNorms (no residual) + quantisation over the same
+    rows: the q and kv latent norms of multi-head latent attention, which
+    "[ROCm] Fuse per-token activation quant into RMSNorm for per-channel
+    quantized attention" (sglang PR 34502), "Change", runs as one fused q/kv
+    RMSNorm. Each half is exactly rmsnorm_add_quant of its own rows and
+    weight; returns the two result dicts."""
+    a = rmsnorm_add_quant(fmt, xa, None, wa, eps=eps, gemma=gemma, from_fp32=from_fp32, fp16=fp16, **kw)
+    b = rmsnorm_add_quant(fmt, xb, None, wb, eps=eps, gemma=gemma, from_fp32=from_fp32, fp16=fp16, **kw)
+    return a, b

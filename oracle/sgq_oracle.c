@@ -24,7 +24,10 @@
  *    norm quantises the fp32 normed value; the fused SiLU-and-mul rounds silu
  *    to bf16 and the product to bf16, like the unfused SiLU-and-mul.
  *  - "[ROCm] Fuse per-token activation quant into RMSNorm ..." (sglang PR
- *    34502), "Change": per-token FP8 with an [m, 1] scale.
+ *    34502), "Change": per-token FP8 with an [m, 1] scale; fp16 activations
+ *    stay fp16 (the norm's input, outputs and quant source are then fp16, as
+ *    is the reviewed norm of vllm PR 65478, whose bitwise test covers bf16
+ *    and fp16).
  *  - The formulas the pages only name: RMSNorm y = h * (mean(h^2) + eps)^-1/2
  *    * (1 + w) (Gemma) or * w; OAI SwiGLU a = min(g,L) * sigmoid(alpha*min(g,L))
  *    * (clamp(u,-L,L) + beta); SiLU-and-mul a = g*sigmoid(g)*u; E4M3 and E8M0
@@ -40,7 +43,7 @@
  * tests (the two sides do not include each other). */
 enum { ORA_MXFP8 = 0, ORA_BLOCK128 = 1, ORA_PER_TOKEN = 2 };
 enum { ORA_SWIGLU_OAI = 0, ORA_SILU_MUL = 1 };
-enum { ORA_F_GEMMA = 1u << 0, ORA_F_FROM_FP32 = 1u << 1, ORA_F_ACT_ROUND_BF16 = 1u << 2 };
+enum { ORA_F_GEMMA = 1u << 0, ORA_F_FROM_FP32 = 1u << 1, ORA_F_ACT_ROUND_BF16 = 1u << 2, ORA_F_FP16 = 1u << 5 };
 
 /* Per-element ambiguity flags written to `amb`. ORA_AMB_TIE marks an
  * element of an FP8 group quantised from fp32 whose argument y/s lies within
@@ -94,6 +97,63 @@ static int near_bf16_boundary(double v, double rel) {
     double mid = (floor(a / ulp) + 0.5) * ulp;
     double lo_mid = mid - ulp;
     return fabs(a - mid) <= rel * a || fabs(a - lo_mid) <= rel * a;
+}
+
+/* ------------------------------------------------------------------ fp16 */
+
+/* IEEE binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits; exponent
+ * field 0 holds the subnormals f * 2^-24; field 31 holds inf and NaN. */
+double ora_f16_decode(uint16_t b) {
+    int e = (b >> 10) & 0x1F, f = b & 0x3FF;
+    double v;
+    if (e == 0) v = ldexp((double)f, -24);
+    else if (e == 31) v = f ? NAN : INFINITY;
+    else v = ldexp(1024.0 + (double)f, e - 25);
+    return (b & 0x8000) ? -v : v;
+}
+
+/* Distance between adjacent fp16 values at |v|. */
+static double f16_ulp(double a) {
+    int e2;
+    if (a == 0.0) return ldexp(1.0, -24);
+    frexp(a, &e2);
+    int e = e2 - 1;
+    if (e < -14) e = -14;       /* subnormals share the spacing of the smallest binade */
+    return ldexp(1.0, e - 10);
+}
+
+/* Nearest fp16 to v, ties to even; results past the largest finite value
+ * (65504, reached by everything below the midpoint 65520) are infinite. */
+uint16_t ora_f16_round(double v) {
+    if (isnan(v)) return 0x7E00;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (isinf(a)) return sign | 0x7C00;
+    double ulp = f16_ulp(a);
+    double r = nearbyint(a / ulp) * ulp;     /* exact; half to even */
+    if (r >= 65536.0) return sign | 0x7C00;
+    if (r < ldexp(1.0, -14)) return sign | (uint16_t)(r / ldexp(1.0, -24));
+    int e2;
+    frexp(r, &e2);
+    int e = e2 - 1;                          /* r in [2^e, 2^(e+1)) */
+    uint16_t frac = (uint16_t)(ldexp(r, 10 - e) - 1024.0);
+    return sign | (uint16_t)((e + 15) << 10) | frac;
+}
+
+static int near_f16_boundary(double v, double rel) {
+    double a = fabs(v);
+    if (a == 0.0) return 0;
+    double ulp = f16_ulp(a);
+    double mid = (floor(a / ulp) + 0.5) * ulp;
+    double lo_mid = mid - ulp;
+    return fabs(a - mid) <= rel * a || fabs(a - lo_mid) <= rel * a;
+}
+
+/* The 16-bit activation type: bf16, or fp16 when f16 is set. */
+static double io_decode(int f16, uint16_t b) { return f16 ? ora_f16_decode(b) : ora_bf16_decode(b); }
+static uint16_t io_round(int f16, double v) { return f16 ? ora_f16_round(v) : ora_bf16_round(v); }
+static int near_io_boundary(int f16, double v, double rel) {
+    return f16 ? near_f16_boundary(v, rel) : near_bf16_boundary(v, rel);
 }
 
 /* ------------------------------------------------------------------ E4M3 */
@@ -183,7 +243,7 @@ static void element_flags(double tj, unsigned char src_amb, double* t, unsigned 
  * scale. `pre[]` are the values before the optional bf16 rounding of the
  * source (equal to src when quantising from fp32), used only for the
  * ambiguity flags. Writes t[] = src / scale (the E4M3 rounding argument). */
-static void quant_group(int fmt, int from_fp32, const double* src, const double* pre,
+static void quant_group(int fmt, int from_fp32, int f16, const double* src, const double* pre,
                         const unsigned char* src_amb, long n, uint8_t* q, void* scale_slot,
                         double* t, unsigned char* amb, unsigned char* gamb, double rel) {
     double amax = 0.0, amax_pre = 0.0;
@@ -194,9 +254,9 @@ static void quant_group(int fmt, int from_fp32, const double* src, const double*
     /* Is the group's scale decision robust against small changes of amax? */
     int g_amb = 0;
     if (!from_fp32) {
-        /* bf16 source: amax moves only if an element near the top rounds differently. */
+        /* 16-bit source: amax moves only if an element near the top rounds differently. */
         for (long j = 0; j < n; ++j)
-            if (src_amb[j] && fabs(pre[j]) >= amax_pre * (1.0 - ldexp(1.0, -7))) g_amb = 1;
+            if (src_amb[j] && fabs(pre[j]) >= amax_pre * (1.0 - ldexp(1.0, f16 ? -10 : -7))) g_amb = 1;
     }
     if (fmt == ORA_MXFP8) {
         if (from_fp32 && near_pow2(amax, rel)) g_amb = 1;
@@ -238,17 +298,17 @@ static void* scale_at(int fmt, void* scale, long index) {
 }
 
 /* Quantise one row of `width` values. */
-static void quant_row(int fmt, int from_fp32, const double* pre, long width, long row,
+static void quant_row(int fmt, int from_fp32, int f16, const double* pre, long width, long row,
                       uint8_t* q, void* scale, double* t, unsigned char* amb, unsigned char* gamb,
                       double rel, double* src, unsigned char* src_amb) {
     for (long j = 0; j < width; ++j) {
-        src[j] = from_fp32 ? pre[j] : ora_bf16_decode(ora_bf16_round(pre[j]));
-        src_amb[j] = (unsigned char)(from_fp32 ? 0 : near_bf16_boundary(pre[j], rel));
+        src[j] = from_fp32 ? pre[j] : io_decode(f16, io_round(f16, pre[j]));
+        src_amb[j] = (unsigned char)(from_fp32 ? 0 : near_io_boundary(f16, pre[j], rel));
     }
     long gs = group_size(fmt, width), ng = width / gs;
     for (long g = 0; g < ng; ++g) {
         long off = row * width + g * gs;
-        quant_group(fmt, from_fp32, src + g * gs, pre + g * gs, src_amb + g * gs, gs, q + off,
+        quant_group(fmt, from_fp32, f16, src + g * gs, pre + g * gs, src_amb + g * gs, gs, q + off,
                     scale_at(fmt, scale, row * ng + g), t ? t + off : 0, amb ? amb + off : 0,
                     gamb ? gamb + row * ng + g : 0, rel);
     }
@@ -262,6 +322,8 @@ static void quant_row(int fmt, int from_fp32, const double* pre, long width, lon
  *   y = h / sqrt(sum(h^2)/H + eps) * (1 + w)   (Gemma) or * w (plain)
  *   normed = bf16(y)               (optional output)
  *   quant source = bf16(y), or y itself with ORA_F_FROM_FP32
+ * With ORA_F_FP16, x, r, w and the written residual and normed rows are fp16
+ * and the rounded quant source is fp16(y).
  * Outputs: q [M,H] E4M3 codes; scale [M,H/32] E8M0 codes, [M,H/128] fp32 or
  * [M,1] fp32. Optional diagnostics: y64 [M,H] (y in fp64), t64 [M,H] (the
  * E4M3 rounding argument), amb [M,H] and gamb [M,groups] flags for decisions
@@ -277,22 +339,23 @@ int ora_rmsnorm_add_quant(int fmt, unsigned flags, long M, long H, float eps,
     unsigned char* sa = (unsigned char*)malloc((size_t)H);
     if (!h || !sa) { free(h); free(sa); return -1; }
     double *y = h + H, *src = h + 2 * H;
+    const int f16 = (flags & ORA_F_FP16) != 0;
     for (long i = 0; i < M; ++i) {
         const uint16_t* xi = x + i * H;
-        for (long j = 0; j < H; ++j) h[j] = ora_bf16_decode(xi[j]) + (r ? ora_bf16_decode(r[i * H + j]) : 0.0);
+        for (long j = 0; j < H; ++j) h[j] = io_decode(f16, xi[j]) + (r ? io_decode(f16, r[i * H + j]) : 0.0);
         if (r && r_out)
-            for (long j = 0; j < H; ++j) r_out[i * H + j] = ora_bf16_round(h[j]);
+            for (long j = 0; j < H; ++j) r_out[i * H + j] = io_round(f16, h[j]);
         double ss = 0.0;
         for (long j = 0; j < H; ++j) ss += h[j] * h[j];
         double inv = 1.0 / sqrt(ss / (double)H + (double)eps);
         for (long j = 0; j < H; ++j) {
-            double wj = ora_bf16_decode(w[j]);
+            double wj = io_decode(f16, w[j]);
             y[j] = h[j] * inv * ((flags & ORA_F_GEMMA) ? 1.0 + wj : wj);
         }
         if (normed_out)
-            for (long j = 0; j < H; ++j) normed_out[i * H + j] = ora_bf16_round(y[j]);
+            for (long j = 0; j < H; ++j) normed_out[i * H + j] = io_round(f16, y[j]);
         if (y64) memcpy(y64 + i * H, y, sizeof(double) * (size_t)H);
-        quant_row(fmt, (flags & ORA_F_FROM_FP32) != 0, y, H, i, q, scale, t64, amb, gamb, rel, src, sa);
+        if (q) quant_row(fmt, (flags & ORA_F_FROM_FP32) != 0, f16, y, H, i, q, scale, t64, amb, gamb, rel, src, sa);
     }
     free(h);
     free(sa);
@@ -342,7 +405,7 @@ int ora_swiglu_quant(int fmt, int act, unsigned flags, long M, long I, float alp
             }
         }
         if (a64) memcpy(a64 + i * I, a, sizeof(double) * (size_t)I);
-        quant_row(fmt, (flags & ORA_F_FROM_FP32) != 0, a, I, i, q, scale, t64, amb, gamb, rel, src, sa);
+        quant_row(fmt, (flags & ORA_F_FROM_FP32) != 0, 0, a, I, i, q, scale, t64, amb, gamb, rel, src, sa);
         if (act_amb && (flags & ORA_F_ACT_ROUND_BF16)) {
             /* A rounding of silu(g) that may go either way also leaves the
              * element and (if it is near the top) the group scale open. */
@@ -372,17 +435,19 @@ int ora_swiglu_quant(int fmt, int act, unsigned flags, long M, long I, float alp
  * microbenchmark script (norm, then a separate MXFP8 quant); "[ROCm] Fuse
  * per-token activation quant into RMSNorm ..." (sglang PR 34502),
  * "Motivation" (the standalone per-token quant)). The source values are the
- * bf16 values themselves. Outputs and diagnostics as above.
+ * bf16 values themselves (fp16 values with ORA_F_FP16). Outputs and
+ * diagnostics as above.
  */
-int ora_quantize(int fmt, long M, long W, const uint16_t* src_bits, uint8_t* q, void* scale, double* t64,
-                 unsigned char* amb, unsigned char* gamb, double rel) {
+int ora_quantize(int fmt, unsigned flags, long M, long W, const uint16_t* src_bits, uint8_t* q, void* scale,
+                 double* t64, unsigned char* amb, unsigned char* gamb, double rel) {
     if (fmt < 0 || fmt > 2 || M < 0 || W <= 0 || W % group_size(fmt, W) != 0) return -1;
     double* v = (double*)malloc(sizeof(double) * (size_t)W * 2);
     unsigned char* sa = (unsigned char*)malloc((size_t)W);
     if (!v || !sa) { free(v); free(sa); return -1; }
     for (long i = 0; i < M; ++i) {
-        for (long j = 0; j < W; ++j) v[j] = ora_bf16_decode(src_bits[i * W + j]);
-        quant_row(fmt, 0, v, W, i, q, scale, t64, amb, gamb, rel, v + W, sa);
+        const int f16 = (flags & ORA_F_FP16) != 0;
+        for (long j = 0; j < W; ++j) v[j] = io_decode(f16, src_bits[i * W + j]);
+        quant_row(fmt, 0, f16, v, W, i, q, scale, t64, amb, gamb, rel, v + W, sa);
     }
     free(v);
     free(sa);
