@@ -357,6 +357,39 @@ def other_configs(dev):
     return res
 
 
+def qkv_norm_configs(dev):
+    """µs per launch (graph replay) of the q/kv latent norms of multi-head
+    latent attention: q [M,1536] normed + per-token FP8, kv [M,512] normed to
+    bf16, both read as column ranges of one [M,2112] projection output. One
+    two-segment launch against two single-norm launches on copies of the
+    same rows."""
+    import torch
+
+    from swiglu_fp8_activation_gb300 import rmsnorm_add_quant, rmsnorm_dual_quant
+    res = {}
+    Ha, Hb = 1536, 512
+    for M in (1, 64, 4096):
+        g = torch.Generator().manual_seed(M)
+        buf = (torch.randn(M, Ha + Hb + 64, generator=g)).to(torch.bfloat16).to(dev)
+        wa = (1 + 0.1 * torch.randn(Ha, generator=g)).to(torch.bfloat16).to(dev)
+        wb = (1 + 0.1 * torch.randn(Hb, generator=g)).to(torch.bfloat16).to(dev)
+        xa, xb = buf[:, :Ha], buf[:, Ha:Ha + Hb]
+        fn = lambda: rmsnorm_dual_quant(xa, wa, xb, wb)
+        xa_c, xb_c = xa.contiguous(), xb.contiguous()
+        qa = torch.empty(M, Ha, dtype=torch.uint8, device=dev)
+        sa = torch.empty(M, 1, dtype=torch.float32, device=dev)
+        nb = torch.empty(M, Hb, dtype=torch.bfloat16, device=dev)
+        qb = torch.empty(M, Hb, dtype=torch.uint8, device=dev)
+        sb = torch.empty(M, 1, dtype=torch.float32, device=dev)
+
+        def two():
+            rmsnorm_add_quant(xa_c, wa, fmt="per_token", gemma=False, q_out=qa, scale_out=sa)
+            rmsnorm_add_quant(xb_c, wb, fmt="per_token", gemma=False, q_out=qb, scale_out=sb, normed_out=nb)
+        res[f"M{M}"] = {"dual_us": round(graph_us_per_launch(fn, iters=100, reps=10), 3),
+                        "two_launches_us": round(graph_us_per_launch(two, iters=100, reps=10), 3)}
+    return res
+
+
 def time_e2e(pf, dev, steps, chunks=8):
     """The same step through the public API with host buffers. Every step
     copies x, r and gate_up from pinned host memory, runs both ops, and copies
@@ -515,6 +548,7 @@ def run_ours(args, world, rank, local):
         total_ms, norm_ms, swiglu_ms = time_prefill(pf, args.steps, args.warmup, world)
         decode = decode_table(dev) if rank == 0 and not args.quick else None
         others = other_configs(dev) if rank == 0 and not args.quick else None
+        qkv = qkv_norm_configs(dev) if rank == 0 and not args.quick else None
     total_ms = max_over_ranks(total_ms, world)
     e2e_ms, h2d, d2h = time_e2e(pf, dev, args.e2e_steps)
     e2e_ms = max_over_ranks(e2e_ms, world)
@@ -545,6 +579,7 @@ def run_ours(args, world, rank, local):
                     "swiglu_frac": round(swiglu_gbs / peak, 4)},
         "decode_us_per_launch": decode,
         "other_configs": others,
+        "qkv_latent_norm_us": qkv,
         "e2e": {"value": round(sb / (e2e_ms * 1e-3) / 1e9 * world, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 3),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * args.steps,

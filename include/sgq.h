@@ -33,8 +33,10 @@
  *     allocates nothing, keeps no state between calls, never synchronises and
  *     launches nothing but its one kernel, so calls may be captured into CUDA
  *     graphs.
- *   - All tensors are contiguous and row-major. Inputs are bfloat16. Quantised
- *     values are OCP E4M3 ("e4m3fn") bytes.
+ *   - All tensors are contiguous and row-major (the dual norm's inputs may
+ *     have a row stride). 16-bit activations are bfloat16, or IEEE fp16 with
+ *     SGQ_F_FP16 where an entry point accepts it. Quantised values are OCP
+ *     E4M3 ("e4m3fn") bytes.
  *   - Scale layouts: MXFP8 -> uint8 E8M0 codes [M, W/32] (value 2^(code-127));
  *     1x128 block -> float32 [M, W/128]; per-token -> float32 [M, 1]; all
  *     row-major unless a layout flag below selects another one.
@@ -61,7 +63,7 @@
 extern "C" {
 #endif
 
-#define SGQ_ABI_VERSION 1
+#define SGQ_ABI_VERSION 2
 #define SGQ_MAX_WIDTH 16384
 
 /* Quantisation format of the output activation. */
@@ -81,6 +83,9 @@ typedef enum sgq_act {
 #define SGQ_F_GEMMA_WEIGHT    (1u << 0) /* norm: scale by (1 + w) (Gemma) instead of w */
 #define SGQ_F_QUANT_FROM_FP32 (1u << 1) /* quantise the fp32 value, not its bf16 rounding */
 #define SGQ_F_ACT_ROUND_BF16  (1u << 2) /* SiLU-and-mul: round silu(g) to bf16 before the product */
+#define SGQ_F_FP16            (1u << 5) /* norms and quantize_fp8: the 16-bit activations (inputs,
+                                           weight, written residual and normed rows, and the
+                                           rounded quant source) are IEEE fp16, not bf16 */
 
 /*
  * Scale layouts for GEMM consumers other than the row-major one. [P1]'s
@@ -137,8 +142,9 @@ typedef void* sgq_stream_t;
  *
  * Arguments:
  *   fmt           sgq_format_t
- *   flags         SGQ_F_GEMMA_WEIGHT | SGQ_F_QUANT_FROM_FP32, and a scale layout
- *                 flag of the format (others rejected)
+ *   flags         SGQ_F_GEMMA_WEIGHT | SGQ_F_QUANT_FROM_FP32 | SGQ_F_FP16, and a
+ *                 scale layout flag of the format (others rejected). With
+ *                 SGQ_F_FP16 the bf16 of the formulas above reads fp16.
  *   M, H          rows and hidden width
  *   eps           >= 0, finite
  *   x             [M, H] bf16, read
@@ -199,7 +205,7 @@ int swiglu_quant(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float a
  * rmsnorm_add_quant without SGQ_F_QUANT_FROM_FP32, byte for byte.
  *
  * Arguments as for rmsnorm_add_quant, except:
- *   flags         SGQ_F_GEMMA_WEIGHT only (others rejected)
+ *   flags         SGQ_F_GEMMA_WEIGHT | SGQ_F_FP16 (others rejected)
  *   H             any multiple of 8 up to SGQ_MAX_WIDTH
  *   normed_out    [M, H] bf16, written (required)
  */
@@ -231,7 +237,8 @@ int swiglu(int act, uint32_t flags, int64_t M, int64_t I, float alpha, float bet
  *
  * Arguments:
  *   fmt           sgq_format_t
- *   flags         a scale layout flag of the format, or 0 (others rejected)
+ *   flags         SGQ_F_FP16 (src is fp16), and a scale layout flag of the
+ *                 format (others rejected)
  *   M, W          rows and width (W a multiple of the group, <= SGQ_MAX_WIDTH)
  *   src           [M, W] bf16, read
  *   q_out         [M, W] E4M3, written
@@ -240,6 +247,48 @@ int swiglu(int act, uint32_t flags, int64_t M, int64_t I, float alpha, float bet
  */
 int quantize_fp8(int fmt, uint32_t flags, int64_t M, int64_t W, const void* src, void* q_out,
                  void* scale_out, sgq_stream_t stream);
+
+/* One row set of rmsnorm_dual_quant. */
+typedef struct sgq_norm_seg {
+    int64_t H;             /* width */
+    int64_t ld;            /* row stride of x in elements: >= H, a multiple of 8 */
+    const void* x;         /* rows of x: [M, ld] 16-bit, columns [0, H) read */
+    const void* weight;    /* [H] 16-bit */
+    void* q_out;           /* [M, H] E4M3, or NULL: this segment is not quantised */
+    void* scale_out;       /* scales of fmt (row-major), NULL exactly when q_out is */
+    void* normed_out;      /* [M, H] 16-bit normed rows, or NULL (not with q_out NULL) */
+} sgq_norm_seg_t;
+
+/*
+ * Two RMSNorms over the same M rows in one launch, each with its own input
+ * rows, weight and outputs, and no residual: the q and kv latent norms of
+ * multi-head latent attention ([P4] "Change": the decode q_b_proj quant is
+ * folded into the fused q/kv RMSNorm, which emits the per-token quantised q
+ * while kv stays in the activation type). For each segment, each row:
+ *
+ *   y = x * inv * (1 + w) (SGQ_F_GEMMA_WEIGHT) or x * inv * w,
+ *   inv = 1 / sqrt(sum_j x_j^2 / H + eps)
+ *   normed_out = 16-bit(y)                  (if normed_out is not NULL)
+ *   q_out, scale_out = quantise(src)        (if q_out is not NULL)
+ *
+ * exactly as rmsnorm_add_quant computes a row without residual, so each
+ * segment's outputs equal a rmsnorm_add_quant call on its rows. The inputs
+ * may be column ranges of one tensor (x = base + column offset, ld = the
+ * tensor's row length), and may overlap each other; the outputs may overlap
+ * nothing. Scales are row-major (no layout flags).
+ *
+ * Arguments:
+ *   fmt           sgq_format_t (both segments)
+ *   flags         SGQ_F_GEMMA_WEIGHT | SGQ_F_QUANT_FROM_FP32 | SGQ_F_FP16
+ *   M             rows of both segments
+ *   eps           >= 0, finite
+ *   seg_a, seg_b  host pointers to the two segments (read during the call
+ *                 only); H a multiple of the format's group when the segment
+ *                 is quantised, else of 8; H <= SGQ_MAX_WIDTH
+ *   stream        the stream to launch on
+ */
+int rmsnorm_dual_quant(int fmt, uint32_t flags, int64_t M, float eps, const sgq_norm_seg_t* seg_a,
+                       const sgq_norm_seg_t* seg_b, sgq_stream_t stream);
 
 /* A static, human-readable name of a status code. */
 const char* sgq_status_string(int status);

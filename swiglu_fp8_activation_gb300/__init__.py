@@ -10,6 +10,8 @@ Two fused ops behind a C ABI (`libsgq.so`, declared in include/sgq.h):
 The three steps of the unfused chains they replace are exported too, one
 launch each, to run and time beside them: `rmsnorm_add` (norm to bf16),
 `swiglu` (activation to bf16) and `quantize_fp8` (FP8 quant of bf16 rows).
+`rmsnorm_dual_quant` norms two row sets (the q and kv latent norms) in one
+launch. The norms and the quant also take fp16 activations.
 
 Formats: MXFP8 (E4M3 + one E8M0 scale per 1x32 block), 1x128 block FP8 with
 fp32 scales, and per-token FP8 with an [M,1] fp32 scale.
@@ -21,5 +23,5 @@ from .binding import (  # noqa: F401
     FORMATS, ACTS, F_GEMMA_WEIGHT, F_QUANT_FROM_FP32, F_ACT_ROUND_BF16, F_SCALE_SWIZZLED, F_SCALE_COL_MAJOR,
     SCALE_LAYOUTS, scale_shape,
     SgqError, library, library_path, rmsnorm_add_quant, swiglu_quant, status_string,
-    rmsnorm_add, swiglu, quantize_fp8,
+    rmsnorm_add, swiglu, quantize_fp8, rmsnorm_dual_quant, NormSeg, F_FP16,
 )

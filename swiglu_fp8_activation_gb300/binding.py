@@ -19,11 +19,19 @@ FORMATS = {"mxfp8": 0, "block128": 1, "per_token": 2}
 ACTS = {"swiglu_oai": 0, "silu_mul": 1}
 F_GEMMA_WEIGHT, F_QUANT_FROM_FP32, F_ACT_ROUND_BF16 = 1, 2, 4
 F_SCALE_SWIZZLED, F_SCALE_COL_MAJOR = 8, 16
+F_FP16 = 32
+ACT_DTYPES = (torch.bfloat16, torch.float16)   # the 16-bit activation types of the norms and the quant
 GROUP = {"mxfp8": 32, "block128": 128}
 # scale layouts: name -> (flag, the one format it applies to, or None for all)
 SCALE_LAYOUTS = {"row": (0, None), "swizzled": (F_SCALE_SWIZZLED, "mxfp8"), "col_major": (F_SCALE_COL_MAJOR, "block128")}
 
 _lib = None
+
+
+class NormSeg(C.Structure):
+    """sgq_norm_seg_t: one row set of rmsnorm_dual_quant."""
+    _fields_ = [("H", C.c_int64), ("ld", C.c_int64), ("x", C.c_void_p), ("weight", C.c_void_p),
+                ("q_out", C.c_void_p), ("scale_out", C.c_void_p), ("normed_out", C.c_void_p)]
 
 
 class SgqError(RuntimeError):
@@ -59,6 +67,9 @@ def library() -> C.CDLL:
         L.swiglu.argtypes = [C.c_int, C.c_uint32, i64, i64, C.c_float, C.c_float, C.c_float, vp, vp, vp]
         L.quantize_fp8.restype = C.c_int
         L.quantize_fp8.argtypes = [C.c_int, C.c_uint32, i64, i64, vp, vp, vp, vp]
+        L.rmsnorm_dual_quant.restype = C.c_int
+        L.rmsnorm_dual_quant.argtypes = [C.c_int, C.c_uint32, i64, C.c_float, C.POINTER(NormSeg),
+                                         C.POINTER(NormSeg), vp]
         L.sgq_status_string.restype = C.c_char_p
         L.sgq_status_string.argtypes = [C.c_int]
         L.sgq_abi_version.restype = C.c_int
@@ -117,6 +128,12 @@ def scale_dtype(fmt: str) -> torch.dtype:
     return torch.uint8 if fmt == "mxfp8" else torch.float32
 
 
+def _act_dtype(t: torch.Tensor, name: str) -> torch.dtype:
+    if t.dtype not in ACT_DTYPES:
+        raise SgqError(f"{name}: expected bfloat16 or float16, got {t.dtype}")
+    return t.dtype
+
+
 def _want(t: torch.Tensor, shape, dtype, name):
     if tuple(t.shape) != tuple(shape) or t.dtype != dtype:
         raise SgqError(f"{name}: expected {dtype} {tuple(shape)}, got {t.dtype} {tuple(t.shape)}")
@@ -134,18 +151,20 @@ def rmsnorm_add_quant(x: torch.Tensor, weight: torch.Tensor, *, fmt: str = "mxfp
 
     x [M,H] bf16; weight [H] bf16; residual_in [M,H] bf16 or None;
     residual_out defaults to residual_in (in-place update) when residual_in is
-    given. Returns (q [M,H] uint8 E4M3, scale, normed [M,H] bf16 or None,
-    residual_out or None).
+    given. x, weight and the residual are all bfloat16 or all float16 (the
+    written rows then have the same type). Returns (q [M,H] uint8 E4M3,
+    scale, normed [M,H] or None, residual_out or None).
     """
     M, H = x.shape
-    _want(x, (M, H), torch.bfloat16, "x")
-    _want(weight, (H,), torch.bfloat16, "weight")
+    dt = _act_dtype(x, "x")
+    _want(x, (M, H), dt, "x")
+    _want(weight, (H,), dt, "weight")
     if residual_in is not None:
-        _want(residual_in, (M, H), torch.bfloat16, "residual_in")
+        _want(residual_in, (M, H), dt, "residual_in")
         if residual_out is None:
             residual_out = residual_in
     if residual_out is not None:
-        _want(residual_out, (M, H), torch.bfloat16, "residual_out")
+        _want(residual_out, (M, H), dt, "residual_out")
     dev = x.device
     if q_out is None:
         q_out = torch.empty((M, H), dtype=torch.uint8, device=dev)
@@ -155,12 +174,13 @@ def rmsnorm_add_quant(x: torch.Tensor, weight: torch.Tensor, *, fmt: str = "mxfp
     if scale_out is None:
         scale_out = torch.empty(scale_shape(fmt, M, H, scale_layout), dtype=scale_dtype(fmt), device=dev)
     if normed and normed_out is None:
-        normed_out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+        normed_out = torch.empty((M, H), dtype=dt, device=dev)
     _want(q_out, (M, H), torch.uint8, "q_out")
     _want(scale_out, scale_shape(fmt, M, H, scale_layout), scale_dtype(fmt), "scale_out")
     if normed_out is not None:
-        _want(normed_out, (M, H), torch.bfloat16, "normed_out")
+        _want(normed_out, (M, H), dt, "normed_out")
     flags = (F_GEMMA_WEIGHT if gemma else 0) | (F_QUANT_FROM_FP32 if quant_from_fp32 else 0) | lflag
+    flags |= F_FP16 if dt == torch.float16 else 0
     st = library().rmsnorm_add_quant(FORMATS[fmt], flags, M, H, float(eps), _ptr(x),
                                      _ptr(residual_in), _ptr(residual_out), _ptr(weight),
                                      _ptr(q_out), _ptr(scale_out), _ptr(normed_out), _stream(stream))
@@ -204,22 +224,24 @@ def rmsnorm_add(x: torch.Tensor, weight: torch.Tensor, *, residual_in: torch.Ten
                 normed_out: torch.Tensor | None = None, stream=None):
     """Residual add + RMSNorm to bf16 (the norm step of the unfused chain).
 
-    Returns (normed [M,H] bf16, residual_out or None); residual_out defaults
-    to residual_in (in-place update) when residual_in is given.
+    Returns (normed [M,H] in x's type, residual_out or None); residual_out
+    defaults to residual_in (in-place update) when residual_in is given.
     """
     M, H = x.shape
-    _want(x, (M, H), torch.bfloat16, "x")
-    _want(weight, (H,), torch.bfloat16, "weight")
+    dt = _act_dtype(x, "x")
+    _want(x, (M, H), dt, "x")
+    _want(weight, (H,), dt, "weight")
     if residual_in is not None:
-        _want(residual_in, (M, H), torch.bfloat16, "residual_in")
+        _want(residual_in, (M, H), dt, "residual_in")
         if residual_out is None:
             residual_out = residual_in
     if residual_out is not None:
-        _want(residual_out, (M, H), torch.bfloat16, "residual_out")
+        _want(residual_out, (M, H), dt, "residual_out")
     if normed_out is None:
-        normed_out = torch.empty((M, H), dtype=torch.bfloat16, device=x.device)
-    _want(normed_out, (M, H), torch.bfloat16, "normed_out")
-    st = library().rmsnorm_add(F_GEMMA_WEIGHT if gemma else 0, M, H, float(eps), _ptr(x), _ptr(residual_in),
+        normed_out = torch.empty((M, H), dtype=dt, device=x.device)
+    _want(normed_out, (M, H), dt, "normed_out")
+    flags = (F_GEMMA_WEIGHT if gemma else 0) | (F_FP16 if dt == torch.float16 else 0)
+    st = library().rmsnorm_add(flags, M, H, float(eps), _ptr(x), _ptr(residual_in),
                                _ptr(residual_out), _ptr(weight), _ptr(normed_out), _stream(stream))
     _check(st, "rmsnorm_add")
     return normed_out, residual_out
@@ -252,10 +274,11 @@ def quantize_fp8(src: torch.Tensor, *, fmt: str = "mxfp8", q_out: torch.Tensor |
                  scale_out: torch.Tensor | None = None, scale_layout: str = "row", stream=None):
     """FP8 quantisation of bf16 rows (the separate quant of the unfused chain).
 
-    src [M, W] bf16. Returns (q [M,W] uint8 E4M3, scale).
+    src [M, W] bfloat16 or float16. Returns (q [M,W] uint8 E4M3, scale).
     """
     M, W = src.shape
-    _want(src, (M, W), torch.bfloat16, "src")
+    dt = _act_dtype(src, "src")
+    _want(src, (M, W), dt, "src")
     if fmt not in FORMATS:
         raise SgqError(f"unknown format {fmt!r}")
     lflag = _layout_flag(fmt, scale_layout)
@@ -265,7 +288,58 @@ def quantize_fp8(src: torch.Tensor, *, fmt: str = "mxfp8", q_out: torch.Tensor |
         scale_out = torch.empty(scale_shape(fmt, M, W, scale_layout), dtype=scale_dtype(fmt), device=src.device)
     _want(q_out, (M, W), torch.uint8, "q_out")
     _want(scale_out, scale_shape(fmt, M, W, scale_layout), scale_dtype(fmt), "scale_out")
+    lflag |= F_FP16 if dt == torch.float16 else 0
     st = library().quantize_fp8(FORMATS[fmt], lflag, M, W, _ptr(src), _ptr(q_out), _ptr(scale_out),
                                 _stream(stream))
     _check(st, "quantize_fp8")
     return q_out, scale_out
+
+
+def _seg_input(x: torch.Tensor, name: str):
+    """A 2-D activation whose rows may be strided (a column range of a wider
+    tensor): unit column stride, row stride ld >= width."""
+    if x.dim() != 2 or (x.shape[0] > 1 and x.stride(1) != 1) or (x.shape[1] > 1 and x.stride(1) != 1):
+        raise SgqError(f"{name}: expected a 2-D tensor with unit column stride")
+    ld = x.stride(0) if x.shape[0] > 1 else x.shape[1]
+    if ld < x.shape[1]:
+        raise SgqError(f"{name}: row stride {ld} below the width {x.shape[1]}")
+    return ld
+
+
+def rmsnorm_dual_quant(xa: torch.Tensor, wa: torch.Tensor, xb: torch.Tensor, wb: torch.Tensor, *,
+                       fmt: str = "per_token", eps: float = 1e-6, gemma: bool = False,
+                       quant_from_fp32: bool = False, quant_a: bool = True, quant_b: bool = False,
+                       normed_a: bool = False, normed_b: bool = True, stream=None):
+    """Two RMSNorms over the same rows in one launch (the q and kv latent
+    norms): segment a (xa [M,Ha], wa [Ha]) and b (xb [M,Hb], wb [Hb]). xa and
+    xb may be column ranges of one tensor (strided rows). Each segment is
+    quantised (quant_*) and/or written in its activation type (normed_*).
+    Returns ((qa, sa, na), (qb, sb, nb)) with None for what was not asked.
+    """
+    M = xa.shape[0]
+    if xb.shape[0] != M:
+        raise SgqError("xa and xb must have the same number of rows")
+    if fmt not in FORMATS:
+        raise SgqError(f"unknown format {fmt!r}")
+    dt = _act_dtype(xa, "xa")
+    segs, outs = [], []
+    for name, x, w, quant, normed in (("a", xa, wa, quant_a, normed_a), ("b", xb, wb, quant_b, normed_b)):
+        if x.dtype != dt:
+            raise SgqError(f"x{name}: expected {dt}, got {x.dtype}")
+        H = x.shape[1]
+        ld = _seg_input(x, f"x{name}")
+        _want(w, (H,), dt, f"w{name}")
+        if not (quant or normed):
+            raise SgqError(f"segment {name}: nothing to write")
+        q = torch.empty((M, H), dtype=torch.uint8, device=x.device) if quant else None
+        s = torch.empty(scale_shape(fmt, M, H), dtype=scale_dtype(fmt), device=x.device) if quant else None
+        n = torch.empty((M, H), dtype=dt, device=x.device) if normed else None
+        segs.append(NormSeg(H, ld, x.data_ptr(), w.data_ptr(), q.data_ptr() if quant else None,
+                            s.data_ptr() if quant else None, n.data_ptr() if normed else None))
+        outs.append((q, s, n))
+    flags = (F_GEMMA_WEIGHT if gemma else 0) | (F_QUANT_FROM_FP32 if quant_from_fp32 else 0)
+    flags |= F_FP16 if dt == torch.float16 else 0
+    st = library().rmsnorm_dual_quant(FORMATS[fmt], flags, M, float(eps), C.byref(segs[0]), C.byref(segs[1]),
+                                      _stream(stream))
+    _check(st, "rmsnorm_dual_quant")
+    return outs[0], outs[1]

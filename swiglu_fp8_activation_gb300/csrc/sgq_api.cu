@@ -78,6 +78,8 @@ int group_of(int fmt) { return fmt == SGQ_FMT_MXFP8 ? 32 : fmt == SGQ_FMT_FP8_BL
 
 int sm_count();
 
+int dt_of(uint32_t flags) { return (flags & SGQ_F_FP16) ? sgq::DT_F16 : sgq::DT_BF16; }
+
 constexpr uint32_t kLayoutFlags = SGQ_F_SCALE_SWIZZLED | SGQ_F_SCALE_COL_MAJOR;
 
 int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
@@ -187,12 +189,13 @@ int norm_call(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, const vo
     a.so = so;
     a.normed = static_cast<uint16_t*>(normed_out);
     a.M = M;
+    a.ldx = H;
     a.H = (int)H;
     a.tpr = plan.tpr;
     a.rpc = plan.rpc;
     a.eps = eps;
     a.flags = flags;
-    return launched(sgq::launch_norm(fmt, plan, a, static_cast<cudaStream_t>(stream)));
+    return launched(sgq::launch_norm(fmt, dt_of(flags), plan, a, static_cast<cudaStream_t>(stream)));
 }
 
 // The SwiGLU launch behind swiglu_quant (q_out set) and swiglu (out set:
@@ -241,6 +244,43 @@ int swiglu_call(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float al
     return launched(sgq::launch_swiglu(fmt, plan, a, static_cast<cudaStream_t>(stream)));
 }
 
+int gcd(int a, int b) { return b == 0 ? a : gcd(b, a % b); }
+
+// Plan of the two-segment norm: one chunk count per thread (NV) for both
+// segments, each segment's threads per row (a multiple of 32), and a common
+// CTA size T that both divide, so every CTA holds whole rows of its segment.
+// T is the least common multiple of the two, grown towards kTargetCTA at
+// large M; when that exceeds kMaxTPR both segments take the wider one's
+// threads per row. NV order and the small-M rule follow plan_rows.
+bool plan_dual(int64_t M, int Ha, int Hb, int sms, sgq::Plan* p, int tpr[2], int rpc[2], int64_t* grid0) {
+    const int n[2] = {Ha / 8, Hb / 8};
+    const bool small = sms > 0 && M * (int64_t)(n[0] + n[1]) <= (int64_t)sms * 1024;
+    for (int i = 0; i < sgq::kMaxNV; ++i) {
+        const int nv = small ? 1 + i : sgq::kMaxNV - i;
+        int t[2];
+        for (int s = 0; s < 2; ++s) t[s] = ((n[s] + nv - 1) / nv + 31) / 32 * 32;
+        if (t[0] > sgq::kMaxTPR || t[1] > sgq::kMaxTPR) continue;
+        int T = t[0] / gcd(t[0], t[1]) * t[1];
+        if (T > sgq::kMaxTPR) {                     // both take the wider segment's threads per row
+            T = t[0] > t[1] ? t[0] : t[1];
+            t[0] = t[1] = T;
+        }
+        if (!small && T < sgq::kTargetCTA) T *= sgq::kTargetCTA / T;
+        for (int s = 0; s < 2; ++s) {
+            tpr[s] = t[s];
+            rpc[s] = T / t[s];
+        }
+        *grid0 = (M + rpc[0] - 1) / rpc[0];
+        p->nv = nv;
+        p->tpr = T;
+        p->rpc = 1;
+        p->grid = *grid0 + (M + rpc[1] - 1) / rpc[1];
+        p->full = false;
+        return p->grid <= 0x7FFFFFFF;
+    }
+    return false;
+}
+
 }  // namespace
 
 extern "C" {
@@ -266,7 +306,7 @@ int rmsnorm_add_quant(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, 
                       const void* residual_in, void* residual_out, const void* weight, void* q_out,
                       void* scale_out, void* normed_out, sgq_stream_t stream) {
     if (fmt < SGQ_FMT_MXFP8 || fmt > SGQ_FMT_FP8_PER_TOKEN) return SGQ_ERR_INVALID_ARG;
-    if (flags & ~(SGQ_F_GEMMA_WEIGHT | SGQ_F_QUANT_FROM_FP32 | kLayoutFlags)) return SGQ_ERR_INVALID_ARG;
+    if (flags & ~(SGQ_F_GEMMA_WEIGHT | SGQ_F_QUANT_FROM_FP32 | SGQ_F_FP16 | kLayoutFlags)) return SGQ_ERR_INVALID_ARG;
     if (H > 0 && H % group_of(fmt) != 0) return SGQ_ERR_UNSUPPORTED;
     if (M > 0 && (!q_out || !scale_out)) return SGQ_ERR_INVALID_ARG;
     return norm_call(fmt, flags, M, H, eps, x, residual_in, residual_out, weight, q_out, scale_out, normed_out,
@@ -275,7 +315,7 @@ int rmsnorm_add_quant(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, 
 
 int rmsnorm_add(uint32_t flags, int64_t M, int64_t H, float eps, const void* x, const void* residual_in,
                 void* residual_out, const void* weight, void* normed_out, sgq_stream_t stream) {
-    if (flags & ~SGQ_F_GEMMA_WEIGHT) return SGQ_ERR_INVALID_ARG;
+    if (flags & ~(SGQ_F_GEMMA_WEIGHT | SGQ_F_FP16)) return SGQ_ERR_INVALID_ARG;
     if (H > 0 && H % 8 != 0) return SGQ_ERR_UNSUPPORTED;
     if (M > 0 && !normed_out) return SGQ_ERR_INVALID_ARG;
     return norm_call(SGQ_FMT_MXFP8, flags, M, H, eps, x, residual_in, residual_out, weight, nullptr, nullptr,
@@ -302,7 +342,7 @@ int swiglu(int act, uint32_t flags, int64_t M, int64_t I, float alpha, float bet
 int quantize_fp8(int fmt, uint32_t flags, int64_t M, int64_t W, const void* src, void* q_out, void* scale_out,
                  sgq_stream_t stream) {
     if (fmt < SGQ_FMT_MXFP8 || fmt > SGQ_FMT_FP8_PER_TOKEN) return SGQ_ERR_INVALID_ARG;
-    if (flags & ~kLayoutFlags) return SGQ_ERR_INVALID_ARG;
+    if (flags & ~(kLayoutFlags | SGQ_F_FP16)) return SGQ_ERR_INVALID_ARG;
     if (M < 0 || W <= 0) return SGQ_ERR_INVALID_ARG;
     if (W % group_of(fmt) != 0 || W > SGQ_MAX_WIDTH) return SGQ_ERR_UNSUPPORTED;
     if (M > kMaxElements / W) return SGQ_ERR_INVALID_ARG;
@@ -327,7 +367,73 @@ int quantize_fp8(int fmt, uint32_t flags, int64_t M, int64_t W, const void* src,
     a.W = (int)W;
     a.tpr = plan.tpr;
     a.rpc = plan.rpc;
-    return launched(sgq::launch_quant(fmt, plan, a, static_cast<cudaStream_t>(stream)));
+    return launched(sgq::launch_quant(fmt, dt_of(flags), plan, a, static_cast<cudaStream_t>(stream)));
+}
+
+int rmsnorm_dual_quant(int fmt, uint32_t flags, int64_t M, float eps, const sgq_norm_seg_t* seg_a,
+                       const sgq_norm_seg_t* seg_b, sgq_stream_t stream) {
+    if (fmt < SGQ_FMT_MXFP8 || fmt > SGQ_FMT_FP8_PER_TOKEN) return SGQ_ERR_INVALID_ARG;
+    if (flags & ~(SGQ_F_GEMMA_WEIGHT | SGQ_F_QUANT_FROM_FP32 | SGQ_F_FP16)) return SGQ_ERR_INVALID_ARG;
+    if (!seg_a || !seg_b || M < 0 || !(eps >= 0.0f) || isinf(eps)) return SGQ_ERR_INVALID_ARG;
+    const sgq_norm_seg_t* sg[2] = {seg_a, seg_b};
+    for (int i = 0; i < 2; ++i) {
+        const sgq_norm_seg_t& s = *sg[i];
+        if (s.H <= 0 || s.ld < s.H) return SGQ_ERR_INVALID_ARG;
+        if (s.H % (s.q_out ? group_of(fmt) : 8) != 0 || s.H > SGQ_MAX_WIDTH) return SGQ_ERR_UNSUPPORTED;
+        if (M > kMaxElements / s.ld) return SGQ_ERR_INVALID_ARG;
+    }
+    if (M == 0) return SGQ_OK;
+    Span in[4], out[6];
+    for (int i = 0; i < 2; ++i) {
+        const sgq_norm_seg_t& s = *sg[i];
+        if (!s.x || !s.weight || (!s.q_out) != (!s.scale_out) || (!s.q_out && !s.normed_out))
+            return SGQ_ERR_INVALID_ARG;
+        if (s.ld % 8 != 0 || !aligned(s.x, 16) || !aligned(s.weight, 16) || !aligned(s.q_out, 16) ||
+            !aligned(s.normed_out, 16) || !aligned(s.scale_out, fmt == SGQ_FMT_MXFP8 ? 1 : 4))
+            return SGQ_ERR_MISALIGNED;
+        sgq::ScaleOut so;
+        size_t sbytes = 0;
+        scale_geometry(fmt, 0, M, s.H, &so, &sbytes);
+        in[2 * i] = {s.x, (size_t)((M - 1) * s.ld + s.H) * 2};
+        in[2 * i + 1] = {s.weight, (size_t)s.H * 2};
+        out[3 * i] = {s.q_out, (size_t)(M * s.H)};
+        out[3 * i + 1] = {s.scale_out, s.q_out ? sbytes : 0};
+        out[3 * i + 2] = {s.normed_out, (size_t)(M * s.H) * 2};
+    }
+    // outputs may overlap neither each other nor any input; the inputs may
+    // overlap (q and kv are often column ranges of one projection output)
+    if (any_overlap(out, 6)) return SGQ_ERR_INVALID_ARG;
+    for (int i = 0; i < 6; ++i)
+        for (int j = 0; j < 4; ++j)
+            if (overlap(out[i].p, out[i].n, in[j].p, in[j].n)) return SGQ_ERR_INVALID_ARG;
+
+    sgq::Plan plan;
+    int tpr[2], rpc[2];
+    int64_t grid0 = 0;
+    if (!plan_dual(M, (int)seg_a->H, (int)seg_b->H, sm_count(), &plan, tpr, rpc, &grid0)) return SGQ_ERR_UNSUPPORTED;
+    sgq::DualArgs d;
+    for (int i = 0; i < 2; ++i) {
+        const sgq_norm_seg_t& s = *sg[i];
+        sgq::NormArgs& a = d.seg[i];
+        a.x = static_cast<const uint16_t*>(s.x);
+        a.r_in = nullptr;
+        a.r_out = nullptr;
+        a.w = static_cast<const uint16_t*>(s.weight);
+        a.q = static_cast<uint8_t*>(s.q_out);
+        size_t sbytes = 0;
+        scale_geometry(fmt, 0, M, s.H, &a.so, &sbytes);
+        a.so.p = s.scale_out;
+        a.normed = static_cast<uint16_t*>(s.normed_out);
+        a.M = M;
+        a.ldx = s.ld;
+        a.H = (int)s.H;
+        a.tpr = tpr[i];
+        a.rpc = rpc[i];
+        a.eps = eps;
+        a.flags = flags;
+    }
+    d.grid0 = grid0;
+    return launched(sgq::launch_norm_dual(fmt, dt_of(flags), plan, d, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -34,6 +34,7 @@ namespace sgq {
 enum Fmt : int { FMT_MX = 0, FMT_B128 = 1, FMT_PT = 2 };
 enum Act : int { ACT_OAI = 0, ACT_SILU = 1 };
 enum ScaleLayout : int { SCALE_ROW_MAJOR = 0, SCALE_SWIZZLED = 1, SCALE_COL_MAJOR = 2 };
+enum IoType : int { DT_BF16 = 0, DT_F16 = 1 };   // the 16-bit activation type
 
 constexpr uint32_t F_GEMMA = 1u << 0;
 constexpr uint32_t F_FROM_FP32 = 1u << 1;
@@ -133,6 +134,52 @@ __device__ __forceinline__ uint4 f32x8_to_bf16x8(const float f[8]) {
 // Round a float to the nearest bf16 (ties to even) and widen it back.
 __device__ __forceinline__ float round_bf16(float v) {
     return __uint_as_float(f32x2_to_bf16x2(v, 0.0f) << 16);
+}
+
+// fp16x2 (low half first) -> two floats (exact).
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t w) {
+    float lo, hi;
+    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w));
+    return make_float2(lo, hi);
+}
+
+// Two floats -> fp16x2 with round-to-nearest-even; `lo` goes to the low half.
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// Eight 16-bit values of type DT (one 16-byte chunk) -> floats, and back
+// with round-to-nearest-even; round_io rounds one float to DT and widens it.
+template <int DT>
+__device__ __forceinline__ void load8(const uint4 v, float f[8]) {
+    if (DT == DT_BF16) {
+        bf16x8_to_f32(v, f);
+    } else {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 t = f16x2_to_f32x2(w[i]);
+            f[2 * i] = t.x;
+            f[2 * i + 1] = t.y;
+        }
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 pack8(const float f[8]) {
+    if (DT == DT_BF16) return f32x8_to_bf16x8(f);
+    return make_uint4(f32x2_to_f16x2(f[0], f[1]), f32x2_to_f16x2(f[2], f[3]), f32x2_to_f16x2(f[4], f[5]),
+                      f32x2_to_f16x2(f[6], f[7]));
+}
+
+template <int DT>
+__device__ __forceinline__ float round_io(float v) {
+    if (DT == DT_BF16) return round_bf16(v);
+    return f16x2_to_f32x2(f32x2_to_f16x2(v, 0.0f)).x;
 }
 
 // Four floats -> four E4M3 bytes (round to nearest even, saturate to +-448);

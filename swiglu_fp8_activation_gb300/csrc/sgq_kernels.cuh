@@ -25,7 +25,7 @@ struct ScaleOut {
 };
 
 struct NormArgs {
-    const uint16_t* x;       // [M, H] bf16
+    const uint16_t* x;       // [M, ldx] 16-bit (bf16 or fp16), rows read from column 0 to H
     const uint16_t* r_in;    // [M, H] bf16 or null
     uint16_t* r_out;         // [M, H] bf16 or null (may equal r_in)
     const uint16_t* w;       // [H] bf16
@@ -33,6 +33,7 @@ struct NormArgs {
     ScaleOut so;
     uint16_t* normed;        // [M, H] bf16 or null
     int64_t M;
+    int64_t ldx;             // row stride of x in elements (H for contiguous rows)
     int H;
     int tpr;                 // threads per row (multiple of 32)
     int rpc;                 // rows per CTA
@@ -55,7 +56,7 @@ struct SwigluArgs {
 };
 
 struct QuantArgs {
-    const uint16_t* src;     // [M, W] bf16
+    const uint16_t* src;     // [M, W] bf16 or fp16
     uint8_t* q;              // [M, W] E4M3
     ScaleOut so;
     int64_t M;
@@ -181,10 +182,12 @@ __host__ __device__ constexpr int norm_stage_bytes(bool has_res, int nv, int thr
     return nv * norm_stage_inputs(has_res) * threads * 16;
 }
 
+// The rows of CTA `blk` of one norm launch (blockDim.x = a.rpc * a.tpr).
 // FULL: every thread's chunks lie inside the row and every row inside M (the
-// plan divides both exactly), so no bounds are checked.
-template <int FMT, int LAYOUT, int NV, bool HAS_RES, bool FULL>
-__global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
+// plan divides both exactly), so no bounds are checked. DT is the 16-bit
+// type of x, r, w and the written rows.
+template <int FMT, int LAYOUT, int NV, bool HAS_RES, bool FULL, int DT>
+__device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
     extern __shared__ uint4 stage[];
     __shared__ float2 part[32];
     constexpr int NIN = norm_stage_inputs(HAS_RES);
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
     const int nt = blockDim.x;
     const int lrow = threadIdx.x / tpr;
     const int t = threadIdx.x - lrow * tpr;
-    const int64_t row = (int64_t)blockIdx.x * a.rpc + lrow;
+    const int64_t row = blk * a.rpc + lrow;
     const bool row_ok = FULL || row < a.M;
     const int H = a.H, nchunks = H >> 3;
     const int64_t base = row * (int64_t)H;
@@ -209,7 +212,7 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
         const int c = t + v * tpr;
         const bool ok = FULL || (row_ok && c < nchunks);   // else zero-fill, reading nothing
         const int nb = ok ? 16 : 0;
-        cp_async16(slot(v, 0), ok ? (const void*)(a.x + base + (int64_t)c * 8) : (const void*)a.x, nb);
+        cp_async16(slot(v, 0), ok ? (const void*)(a.x + row * a.ldx + (int64_t)c * 8) : (const void*)a.x, nb);
         if (HAS_RES)
             cp_async16(slot(v, 1), ok ? (const void*)(a.r_in + base + (int64_t)c * 8) : (const void*)a.x, nb);
         cp_async16_cached(slot(v, NIN - 1), ok ? (const void*)(a.w + (int64_t)c * 8) : (const void*)a.x, nb);
@@ -227,15 +230,15 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
         const int c = t + v * tpr;
         float h[8], wf[8];
         cp_async_wait_group_of<NV>(v);
-        bf16x8_to_f32(ld_smem16(slot(v, 0)), h);
+        load8<DT>(ld_smem16(slot(v, 0)), h);
         if (HAS_RES) {
             float rf[8];
-            bf16x8_to_f32(ld_smem16(slot(v, 1)), rf);
+            load8<DT>(ld_smem16(slot(v, 1)), rf);
 #pragma unroll
             for (int k = 0; k < 8; ++k) h[k] += rf[k];
-            if (a.r_out) st16_if(a.r_out + base + (int64_t)c * 8, f32x8_to_bf16x8(h), FULL || (row_ok && c < nchunks));
+            if (a.r_out) st16_if(a.r_out + base + (int64_t)c * 8, pack8<DT>(h), FULL || (row_ok && c < nchunks));
         }
-        bf16x8_to_f32(ld_smem16(slot(v, NIN - 1)), wf);
+        load8<DT>(ld_smem16(slot(v, NIN - 1)), wf);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             ss = fmaf(h[k], h[k], ss);
@@ -256,7 +259,7 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
     float inv = __frsqrt_rn(__fdiv_rn(ss, (float)H) + a.eps);
     if (!FULL && !row_ok) inv = 0.0f;                          // a padding row of the scale layout: all zero
 
-    // 4. y = inv * z; bf16 copy; quant source; quantise (MX and 1x128 chunk by
+    // 4. y = inv * z; 16-bit copy; quant source; quantise (MX and 1x128 chunk by
     //    chunk; per-token after the whole row, with the row scale from ymax).
     //    Without q (the unfused norm) only the bf16 copy is written.
     const bool quant = a.q != nullptr;
@@ -265,7 +268,7 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
     float2 pt = make_float2(0.0f, 0.0f);
     if (FMT == FMT_PT) {
         const float ymax = inv * row_zmax;                     // = max |y| exactly
-        pt = per_token_scale(from32 ? ymax : round_bf16(ymax));
+        pt = per_token_scale(from32 ? ymax : round_io<DT>(ymax));
     }
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
@@ -274,17 +277,38 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
         float y[8], src[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) y[k] = inv * z[v][k];     // z = 0 past the row end (zero-filled copies)
-        const uint4 yb = f32x8_to_bf16x8(y);
+        const uint4 yb = pack8<DT>(y);
         if (a.normed) st16_if(a.normed + base + (int64_t)c * 8, yb, ok);
         if (!quant) continue;
         if (from32) {
 #pragma unroll
             for (int k = 0; k < 8; ++k) src[k] = y[k];
         } else {
-            bf16x8_to_f32(yb, src);
+            load8<DT>(yb, src);
         }
         quantize_chunk<FMT, LAYOUT>(src, row, c, ok, FULL || (srow_ok && c < nchunks), H, a.q, sr, pt.x, pt.y);
     }
+}
+
+template <int FMT, int LAYOUT, int NV, bool HAS_RES, bool FULL, int DT>
+__global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
+    norm_rows<FMT, LAYOUT, NV, HAS_RES, FULL, DT>(a, blockIdx.x);
+}
+
+// Two independent row sets normed in one launch (the q and kv latent norms
+// of multi-head latent attention): CTAs [0, grid0) run seg[0], the rest
+// seg[1]. Both segments use the CTA size blockDim.x = rpc * tpr of their own
+// plan; no residual; bounds always checked.
+struct DualArgs {
+    NormArgs seg[2];
+    int64_t grid0;
+};
+
+template <int FMT, int NV, int DT>
+__global__ void __launch_bounds__(kMaxTPR) norm_dual_kernel(const DualArgs d) {
+    const bool second = blockIdx.x >= d.grid0;
+    const NormArgs a = second ? d.seg[1] : d.seg[0];
+    norm_rows<FMT, SCALE_ROW_MAJOR, NV, false, false, DT>(a, second ? blockIdx.x - d.grid0 : blockIdx.x);
 }
 
 // The activation of one chunk of 8 (gate, up) values, in fp32:
@@ -434,10 +458,10 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
 // Bytes of dynamic shared memory the standalone quant kernel stages its loads in.
 __host__ __device__ constexpr int quant_stage_bytes(int nv, int threads) { return nv * threads * 16; }
 
-// Standalone FP8 quantisation of bf16 rows (the quant of the unfused
+// Standalone FP8 quantisation of 16-bit rows (the quant of the unfused
 // chains). Same row engine and quantiser as the fused kernels; the source is
-// the bf16 value itself.
-template <int FMT, int LAYOUT, int NV, bool FULL>
+// the bf16 (DT_BF16) or fp16 (DT_F16) value itself.
+template <int FMT, int LAYOUT, int NV, bool FULL, int DT>
 __global__ void __launch_bounds__(kMaxTPR) quant_kernel(const QuantArgs a) {
     extern __shared__ uint4 stage[];
     __shared__ float part_amax[32];
@@ -469,7 +493,7 @@ __global__ void __launch_bounds__(kMaxTPR) quant_kernel(const QuantArgs a) {
             const int c = t + v * tpr;
             float src[8];
             cp_async_wait_group_of<NV>(v);
-            bf16x8_to_f32(ld_smem16(&stage[v * nt + threadIdx.x]), src);
+            load8<DT>(ld_smem16(&stage[v * nt + threadIdx.x]), src);
             quantize_chunk<FMT, LAYOUT>(src, row, c, FULL || (row_ok && c < nchunks), FULL || (srow_ok && c < nchunks), W,
                                 a.q, sr);
         }
@@ -479,7 +503,7 @@ __global__ void __launch_bounds__(kMaxTPR) quant_kernel(const QuantArgs a) {
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
             cp_async_wait_group_of<NV>(v);
-            bf16x8_to_f32(ld_smem16(&stage[v * nt + threadIdx.x]), src[v]);
+            load8<DT>(ld_smem16(&stage[v * nt + threadIdx.x]), src[v]);
 #pragma unroll
             for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(src[v][k]));
         }

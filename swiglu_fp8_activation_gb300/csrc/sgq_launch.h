@@ -48,11 +48,15 @@ cudaError_t launch_pdl(void (*k)(const Args), const Plan& p, const Args& a, cuda
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-cudaError_t launch_norm(int fmt, const Plan& p, const NormArgs& a, cudaStream_t stream);
+// dt: DT_BF16 or DT_F16, the 16-bit activation type.
+cudaError_t launch_norm(int fmt, int dt, const Plan& p, const NormArgs& a, cudaStream_t stream);
+cudaError_t launch_norm_f16(int fmt, const Plan& p, const NormArgs& a, cudaStream_t stream);
+// p.grid covers both segments; p.rpc * p.tpr is the common CTA size.
+cudaError_t launch_norm_dual(int fmt, int dt, const Plan& p, const DualArgs& d, cudaStream_t stream);
 
 // Records the CUDA error of a failed launch for sgq_launch_error() (per thread).
 void note_launch_error(cudaError_t e);
 cudaError_t launch_swiglu(int fmt, const Plan& p, const SwigluArgs& a, cudaStream_t stream);
-cudaError_t launch_quant(int fmt, const Plan& p, const QuantArgs& a, cudaStream_t stream);
+cudaError_t launch_quant(int fmt, int dt, const Plan& p, const QuantArgs& a, cudaStream_t stream);
 
 }  // namespace sgq

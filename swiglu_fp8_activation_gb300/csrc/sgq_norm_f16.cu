@@ -1,0 +1,10 @@
+// sgq_norm_f16.cu -- the add + RMSNorm + quant kernel on fp16 activations.
+#include "sgq_norm_impl.cuh"
+
+namespace sgq {
+
+cudaError_t launch_norm_f16(int fmt, const Plan& p, const NormArgs& a, cudaStream_t stream) {
+    return NormPick<DT_F16>::launch(fmt, p, a, stream);
+}
+
+}  // namespace sgq

@@ -37,7 +37,7 @@ def _header_value(name):
 def test_library_exports_every_declared_function(sgq_lib):
     names = _declared_functions()
     assert set(names) == {"rmsnorm_add_quant", "swiglu_quant", "rmsnorm_add", "swiglu", "quantize_fp8",
-                          "sgq_status_string", "sgq_abi_version", "sgq_launch_error"}
+                          "rmsnorm_dual_quant", "sgq_status_string", "sgq_abi_version", "sgq_launch_error"}
     for n in names:
         assert hasattr(sgq_lib, n), n
     m = re.search(r"#define SGQ_ABI_VERSION (\d+)", _header())
@@ -53,6 +53,9 @@ def test_enum_and_flag_values_agree():
     assert _header_value("SGQ_F_GEMMA_WEIGHT") == binding.F_GEMMA_WEIGHT == oracle.F_GEMMA
     assert _header_value("SGQ_F_QUANT_FROM_FP32") == binding.F_QUANT_FROM_FP32 == oracle.F_FROM_FP32
     assert _header_value("SGQ_F_ACT_ROUND_BF16") == binding.F_ACT_ROUND_BF16 == oracle.F_ACT_ROUND_BF16
+    assert _header_value("SGQ_F_FP16") == binding.F_FP16 == oracle.F_FP16
+    assert _header_value("SGQ_F_SCALE_SWIZZLED") == binding.F_SCALE_SWIZZLED
+    assert _header_value("SGQ_F_SCALE_COL_MAJOR") == binding.F_SCALE_COL_MAJOR
 
 
 def test_launch_error_text_without_a_failure(sgq_lib):
@@ -69,13 +72,21 @@ def _p(i):
     return C.c_void_p(BASE + i * 64 * MB)
 
 
+def _host_checked(status):
+    """Every call here passes fake pointers, so it must be refused (or be
+    empty) before anything launches: a launch status means a case got past
+    the host checks and would touch fake addresses on a GPU."""
+    assert status != 4, "a fake-pointer call passed the host checks"
+    return status
+
+
 def norm(lib, fmt=0, flags=1, M=8, H=256, eps=1e-6, x=_p(0), r=_p(1), ro=_p(2), w=_p(3), q=_p(4), s=_p(5),
          n=_p(6)):
-    return lib.rmsnorm_add_quant(fmt, flags, M, H, eps, x, r, ro, w, q, s, n, None)
+    return _host_checked(lib.rmsnorm_add_quant(fmt, flags, M, H, eps, x, r, ro, w, q, s, n, None))
 
 
 def swiglu(lib, fmt=0, act=0, flags=2, M=8, I=256, alpha=1.702, beta=1.0, limit=7.0, gu=_p(0), q=_p(1), s=_p(2)):
-    return lib.swiglu_quant(fmt, act, flags, M, I, alpha, beta, limit, gu, q, s, None)
+    return _host_checked(lib.swiglu_quant(fmt, act, flags, M, I, alpha, beta, limit, gu, q, s, None))
 
 
 def test_norm_argument_errors(sgq_lib):
@@ -129,15 +140,15 @@ def test_swiglu_argument_errors(sgq_lib):
 
 
 def norm_only(lib, flags=1, M=8, H=256, eps=1e-6, x=_p(0), r=_p(1), ro=_p(2), w=_p(3), n=_p(6)):
-    return lib.rmsnorm_add(flags, M, H, eps, x, r, ro, w, n, None)
+    return _host_checked(lib.rmsnorm_add(flags, M, H, eps, x, r, ro, w, n, None))
 
 
 def act_only(lib, act=0, flags=0, M=8, I=256, alpha=1.702, beta=1.0, limit=7.0, gu=_p(0), out=_p(1)):
-    return lib.swiglu(act, flags, M, I, alpha, beta, limit, gu, out, None)
+    return _host_checked(lib.swiglu(act, flags, M, I, alpha, beta, limit, gu, out, None))
 
 
 def quant(lib, fmt=0, flags=0, M=8, W=256, src=_p(0), q=_p(1), s=_p(2)):
-    return lib.quantize_fp8(fmt, flags, M, W, src, q, s, None)
+    return _host_checked(lib.quantize_fp8(fmt, flags, M, W, src, q, s, None))
 
 
 def test_unfused_norm_argument_errors(sgq_lib):
@@ -229,3 +240,53 @@ def test_binding_rejects_wrong_tensors():
         binding.swiglu(torch.zeros(4, 63, dtype=torch.bfloat16))
     with pytest.raises(binding.SgqError):
         binding.quantize_fp8(torch.zeros(4, 64, dtype=torch.bfloat16), fmt="fp4")
+
+
+FP16 = 1 << 5
+
+
+def test_fp16_flag_is_taken_by_the_norms_and_the_quant_only(sgq_lib):
+    L = sgq_lib
+    assert swiglu(L, flags=2 | FP16) == INVALID       # SwiGLU is bf16 only
+    assert act_only(L, flags=FP16) == INVALID
+    assert norm(L, M=0, flags=1 | FP16) == OK
+    assert norm_only(L, M=0, flags=1 | FP16) == OK
+    assert quant(L, M=0, flags=FP16) == OK
+
+
+def _seg(H=512, ld=None, x=0, w=1, q=2, s=3, n=4):
+    f = lambda i: None if i is None else BASE + i * 64 * MB
+    return binding.NormSeg(H, H if ld is None else ld, f(x), f(w), f(q), f(s), f(n))
+
+
+def dual(lib, a=None, b=None, fmt=2, flags=0, M=8, eps=1e-6):
+    a = a or _seg()
+    b = b or _seg(x=5, w=6, q=None, s=None, n=7)
+    return _host_checked(lib.rmsnorm_dual_quant(fmt, flags, M, eps, C.byref(a), C.byref(b), None))
+
+
+def test_dual_norm_argument_errors(sgq_lib):
+    L = sgq_lib
+    assert dual(L, M=0) == OK
+    assert dual(L, fmt=3) == INVALID
+    assert dual(L, flags=4) == INVALID                # ACT_ROUND_BF16 is not a norm flag
+    assert dual(L, flags=1 << 3) == INVALID           # no scale layouts
+    assert dual(L, M=-1) == INVALID
+    assert dual(L, eps=float("nan")) == INVALID
+    assert _host_checked(L.rmsnorm_dual_quant(2, 0, 8, 1e-6, None, C.byref(_seg()), None)) == INVALID
+    assert dual(L, a=_seg(H=0)) == INVALID
+    assert dual(L, a=_seg(ld=256)) == INVALID         # row stride below the width
+    assert dual(L, fmt=0, a=_seg(H=520)) == UNSUPPORTED              # quantised: MX group of 32
+    # an unquantised segment needs H % 8 only: H = 520 passes the width rule and fails later on the overlap
+    assert dual(L, fmt=0, b=_seg(H=520, x=5, w=6, q=None, s=None, n=0)) == INVALID
+    assert dual(L, b=_seg(H=20, x=5, w=6, q=None, s=None, n=7)) == UNSUPPORTED
+    assert dual(L, a=_seg(H=16384 + 8)) == UNSUPPORTED
+    assert dual(L, a=_seg(x=None)) == INVALID
+    assert dual(L, a=_seg(w=None)) == INVALID
+    assert dual(L, a=_seg(s=None)) == INVALID         # q_out without scale_out
+    assert dual(L, a=_seg(q=None)) == INVALID         # scale_out without q_out
+    assert dual(L, b=_seg(x=5, w=6, q=None, s=None, n=None)) == INVALID   # nothing to write
+    assert dual(L, a=_seg(ld=516)) == MISALIGNED      # rows must start 16-byte aligned
+    assert dual(L, a=_seg(n=7)) == INVALID            # two outputs in one place
+    assert dual(L, a=_seg(q=5)) == INVALID            # an output over an input
+    assert dual(L, M=1 << 45, a=_seg(H=16384)) == INVALID
