@@ -313,6 +313,14 @@ __device__ __forceinline__ float div_rn(float a, float b, float r) {
     return fmaf(rem, r, q0);
 }
 
+// Two quotients at once, as div_rn, given nb = -b and r = RN(1/b) for the
+// same b (one FP8 group's scale): q0 = a*r; rem = a - b*q0 (exact); q0 + rem*r.
+__device__ __forceinline__ float2 div2_rn(float2 a, float2 nb, float2 r) {
+    const float2 q0 = __fmul2_rn(a, r);
+    const float2 rem = __ffma2_rn(q0, nb, a);
+    return __ffma2_rn(rem, r, q0);
+}
+
 // ------------------------------------------------------------- reductions
 
 __device__ __forceinline__ float warp_sum(float v) {

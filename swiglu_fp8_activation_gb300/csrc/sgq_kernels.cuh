@@ -148,7 +148,11 @@ __device__ __forceinline__ void quantize_chunk(const float (&src)[8], int64_t ro
         }
         if (s >= 0x1p-126f || s == 0.0f) {              // r = 0 for s = 0: every code is 0
 #pragma unroll
-            for (int k = 0; k < 8; ++k) tq[k] = div_rn(src[k], s, r);
+            for (int k = 0; k < 8; k += 2) {
+                const float2 t = div2_rn(make_float2(src[k], src[k + 1]), f2(-s), f2(r));
+                tq[k] = t.x;
+                tq[k + 1] = t.y;
+            }
         } else {                                         // subnormal scale (amax < 5.3e-36)
 #pragma unroll
             for (int k = 0; k < 8; ++k) tq[k] = __fdiv_rn(src[k], s);
@@ -224,7 +228,8 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
     //    sum of squares (and max |z| for the per-token format)
     const bool gemma = (a.flags & F_GEMMA) != 0, from32 = (a.flags & F_FROM_FP32) != 0;
     float z[NV][8];
-    float ss = 0.0f, zmax = 0.0f;
+    float2 ss2 = make_float2(0.0f, 0.0f);
+    float zmax = 0.0f;
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
         const int c = t + v * tpr;
@@ -235,17 +240,27 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
             float rf[8];
             load8<DT>(ld_smem16(slot(v, 1)), rf);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) h[k] += rf[k];
+            for (int k = 0; k < 8; k += 2) {
+                const float2 hs = __fadd2_rn(make_float2(h[k], h[k + 1]), make_float2(rf[k], rf[k + 1]));
+                h[k] = hs.x;
+                h[k + 1] = hs.y;
+            }
             if (a.r_out) st16_if(a.r_out + base + (int64_t)c * 8, pack8<DT>(h), FULL || (row_ok && c < nchunks));
         }
         load8<DT>(ld_smem16(slot(v, NIN - 1)), wf);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            ss = fmaf(h[k], h[k], ss);
-            z[v][k] = h[k] * (gemma ? 1.0f + wf[k] : wf[k]);
-            if (FMT == FMT_PT) zmax = fmaxf(zmax, fabsf(z[v][k]));
+        for (int k = 0; k < 8; k += 2) {
+            const float2 hp = make_float2(h[k], h[k + 1]);
+            float2 wp = make_float2(wf[k], wf[k + 1]);
+            if (gemma) wp = __fadd2_rn(wp, f2(1.0f));              // 1 + w
+            ss2 = __ffma2_rn(hp, hp, ss2);
+            const float2 zp = __fmul2_rn(hp, wp);
+            z[v][k] = zp.x;
+            z[v][k + 1] = zp.y;
+            if (FMT == FMT_PT) zmax = fmaxf(zmax, fmaxf(fabsf(zp.x), fabsf(zp.y)));
         }
     }
+    float ss = ss2.x + ss2.y;
 
     // 3. inv = 1/sqrt(mean(h^2) + eps), each step correctly rounded
     float row_zmax = 0.0f;
@@ -276,7 +291,11 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
         const bool ok = FULL || (row_ok && c < nchunks);
         float y[8], src[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) y[k] = inv * z[v][k];     // z = 0 past the row end (zero-filled copies)
+        for (int k = 0; k < 8; k += 2) {                       // z = 0 past the row end (zero-filled copies)
+            const float2 yp = __fmul2_rn(f2(inv), make_float2(z[v][k], z[v][k + 1]));
+            y[k] = yp.x;
+            y[k + 1] = yp.y;
+        }
         const uint4 yb = pack8<DT>(y);
         if (a.normed) st16_if(a.normed + base + (int64_t)c * 8, yb, ok);
         if (!quant) continue;

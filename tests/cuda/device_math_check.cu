@@ -1,5 +1,5 @@
 // Test-only kernels around the library's device arithmetic (sigmoid8,
-// activation8, div_rn),
+// activation8, div_rn and its packed form div2_rn),
 // compiled by tests/test_gpu_device_math.py and compared there against fp64
 // and against CUDA's own correctly rounded division.
 #include <cuda_runtime.h>
@@ -34,12 +34,19 @@ __global__ void oai_kernel(const float* g, const float* u, float* out, int n, fl
     }
 }
 
-__global__ void div_kernel(const float* a, const float* b, float* q_fast, float* q_ieee, int n) {
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+// n must be even: pairs (i, i+1) go through the packed form, each with its
+// own divisor, and every element also through the scalar form.
+__global__ void div_kernel(const float* a, const float* b, float* q_fast, float* q_pack, float* q_ieee, int n) {
+    const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
     if (i < n) {
-        const float r = __frcp_rn(b[i]);
-        q_fast[i] = sgq::div_rn(a[i], b[i], r);
+        const float r0 = __frcp_rn(b[i]), r1 = __frcp_rn(b[i + 1]);
+        q_fast[i] = sgq::div_rn(a[i], b[i], r0);
+        q_fast[i + 1] = sgq::div_rn(a[i + 1], b[i + 1], r1);
+        const float2 qp = sgq::div2_rn(make_float2(a[i], a[i + 1]), make_float2(-b[i], -b[i + 1]), make_float2(r0, r1));
+        q_pack[i] = qp.x;
+        q_pack[i + 1] = qp.y;
         q_ieee[i] = __fdiv_rn(a[i], b[i]);
+        q_ieee[i + 1] = __fdiv_rn(a[i + 1], b[i + 1]);
     }
 }
 
@@ -55,7 +62,7 @@ extern "C" int run_oai(const float* g, const float* u, float* out, int n, float 
     return (int)cudaDeviceSynchronize();
 }
 
-extern "C" int run_div(const float* a, const float* b, float* q_fast, float* q_ieee, int n) {
-    div_kernel<<<(n + 255) / 256, 256>>>(a, b, q_fast, q_ieee, n);
+extern "C" int run_div(const float* a, const float* b, float* q_fast, float* q_pack, float* q_ieee, int n) {
+    div_kernel<<<(n / 2 + 255) / 256, 256>>>(a, b, q_fast, q_pack, q_ieee, n);
     return (int)cudaDeviceSynchronize();
 }

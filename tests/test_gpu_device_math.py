@@ -79,7 +79,7 @@ def test_oai_activation_accuracy(devlib):
     assert got[0] > 0.2265625          # exact value 0.22656257..., the boundary is 29/128
 
 
-def test_div_rn_matches_ieee_division(devlib):
+def test_div_rn_and_packed_form_match_ieee_division(devlib):
     rng = np.random.default_rng(1)
     n = 4_000_000
     # the kernels' case: b = amax / 448, |a| <= amax
@@ -95,8 +95,9 @@ def test_div_rn_matches_ieee_division(devlib):
     b2 = (np.abs(rng.standard_normal(n)) * 2.0 ** rng.integers(-60, 60, n) + 2.0 ** -100).astype(np.float32)
     for aa, bb in ((a, b), (a2, b2)):
         at, bt = torch.from_numpy(aa).cuda(), torch.from_numpy(bb).cuda()
-        qf, qi = torch.empty_like(at), torch.empty_like(at)
-        assert devlib.run_div(_p(at), _p(bt), _p(qf), _p(qi), n) == 0
-        qf, qi = qf.cpu().numpy(), qi.cpu().numpy()
+        qf, qp, qi = torch.empty_like(at), torch.empty_like(at), torch.empty_like(at)
+        assert devlib.run_div(_p(at), _p(bt), _p(qf), _p(qp), _p(qi), n) == 0
+        qf, qp, qi = qf.cpu().numpy(), qp.cpu().numpy(), qi.cpu().numpy()
         normal = (np.abs(qi) >= 2.0 ** -126) & np.isfinite(qi)     # overflowing pairs never occur in the kernels
         np.testing.assert_array_equal(qf.view(np.uint32)[normal], qi.view(np.uint32)[normal])
+        np.testing.assert_array_equal(qp.view(np.uint32)[normal], qi.view(np.uint32)[normal])
