@@ -217,9 +217,7 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // the remainder.
 constexpr float kLog2eHi = 1.44269502162933349609375f;   // 0x3FB8AA3B
 constexpr float kLog2eLo = 1.925963033500011e-08f;       // log2(e) - kLog2eHi
-// 1.5 * 2^23: adding it to |x| < 2^22 rounds x to an integer (to nearest even)
-// held in the low mantissa bits.
-constexpr float kRoundMagic = 12582912.0f;
+constexpr float kLn2 = 0.693147180559945309f;        // ln 2, rounded to fp32
 
 __device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
 
@@ -240,21 +238,20 @@ constexpr float kSigLo = -104.0f, kSigHi = 20.0f;
 // fp32x2 arithmetic:
 //   * E = 2^q, q = -z log2 e carried as head qh = RN(-z log2e_hi) plus tail
 //     (the FMA residual of that product, z log2e_lo and the residual of z),
-//     in the manner of Cody and Waite's argument reduction;
-//   * q = n + f with n = round(qh) and |f| <= 0.5005: the hardware 2^x
-//     approximation only ever sees |f| <= 0.5005 (where it is accurate to
-//     about 2 ulp), and 2^n is added to the exponent field; the
-//     round-to-integer constant's bit pattern shifted left by 23 is zero mod
-//     2^32, so the rounded head's bits shifted left by 23 are n << 23;
+//     in the manner of Cody and Waite's argument reduction, so q = qh - tail
+//     with |tail| < 2^-16;
+//   * the hardware 2^x takes the head, whose every value it evaluates to
+//     about 2 ulp, and the tail enters to first order:
+//     2^q = 2^qh (1 - tail ln 2), the dropped second-order term being below
+//     2^-33 relative;
 //   * sigmoid = 1/(1+E), the hardware reciprocal refined by one
-//     Newton-Raphson step. With z in [-104, 20], n lies in [-29, 150]; where
-//     n > 126 (z < -87.7, a branch taken once per chunk) E would overflow and
-//     the sigmoid, which is then 2^-q to within 2^-126 relative, is formed as
-//     2^-f * 2^-n in two exact scaling steps.
+//     Newton-Raphson step. Where qh > 125 (z < -86.6, a branch taken once
+//     per chunk) 1/(1+E) would leave the normal range, and the sigmoid, then
+//     2^-q to within 2^-125 relative, is formed as 2^(126-qh) (1 + tail ln 2)
+//     scaled by 2^-126.
 template <bool TAIL>
 __device__ __forceinline__ void sigmoid8(const float (&zh)[8], const float (&nzl)[8], float (&out)[8]) {
-    float2 e[4], fr[4];
-    uint32_t nb[8];
+    float2 e[4], m[4];
     float qmax = -1.0e30f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -263,20 +260,13 @@ __device__ __forceinline__ void sigmoid8(const float (&zh)[8], const float (&nzl
         float2 tail = __ffma2_rn(z, f2(kLog2eHi), qh);                   // z log2e_hi + qh, exact
         tail = __ffma2_rn(z, f2(kLog2eLo), tail);
         if (TAIL) tail = __ffma2_rn(make_float2(nzl[2 * i], nzl[2 * i + 1]), f2(-kLog2eHi), tail);   // q = qh - tail
-        const float2 big = __fadd2_rn(qh, f2(kRoundMagic));              // round(qh) in the low bits
-        const float2 n = __fadd2_rn(big, f2(-kRoundMagic));
-        float2 f = __ffma2_rn(n, f2(-1.0f), qh);                         // qh - n, exact
-        f = __ffma2_rn(tail, f2(-1.0f), f);                              // |f| <= 0.5005
-        fr[i] = f;
-        e[i] = make_float2(ex2_approx(f.x), ex2_approx(f.y));            // 2^f in [0.7, 1.42]
-        nb[2 * i] = __float_as_uint(big.x) << 23;                        // n << 23 (mod 2^32)
-        nb[2 * i + 1] = __float_as_uint(big.y) << 23;
+        m[i] = __fmul2_rn(tail, f2(-kLn2));                              // 2^q = 2^qh (1 + m)
+        e[i] = make_float2(ex2_approx(qh.x), ex2_approx(qh.y));
         qmax = fmaxf(qmax, fmaxf(qh.x, qh.y));
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float2 E = make_float2(__uint_as_float(__float_as_uint(e[i].x) + nb[2 * i]),
-                                     __uint_as_float(__float_as_uint(e[i].y) + nb[2 * i + 1]));
+        const float2 E = __ffma2_rn(e[i], m[i], e[i]);
         const float2 d = __fadd2_rn(E, f2(1.0f));
         const float2 nd = __ffma2_rn(E, f2(-1.0f), f2(-1.0f));             // -(1 + E)
         const float2 r0 = make_float2(rcp_approx(d.x), rcp_approx(d.y));
@@ -285,16 +275,16 @@ __device__ __forceinline__ void sigmoid8(const float (&zh)[8], const float (&nzl
         out[2 * i] = r.x;
         out[2 * i + 1] = r.y;
     }
-    if (qmax >= 126.5f) {        // some n > 126: sigmoid = 2^-f * 2^-n for those
+    if (qmax > 125.0f) {         // sigmoid = 2^-q for those past qh = 125
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                const int n = (int)nb[2 * i + j] >> 23;
-                if (n > 126) {
-                    const float mf = j ? fr[i].y : fr[i].x;
-                    const float g = ex2_approx(-mf) * 0x1p-126f;        // 2^-f * 2^-126, normal
-                    out[2 * i + j] = g * __uint_as_float((uint32_t)(127 - (n - 126)) << 23);
+                const float qh = zh[2 * i + j] * -kLog2eHi;
+                if (qh > 125.0f) {
+                    const float mj = j ? m[i].y : m[i].x;
+                    const float v = ex2_approx(126.0f - qh);             // 2^(126 - qh), in [2^-24, 2]
+                    out[2 * i + j] = fmaf(v, -mj, v) * 0x1p-126f;
                 }
             }
         }
