@@ -3,6 +3,7 @@
 // allocates, synchronises or keeps state between calls.
 #include <math.h>
 #include <stdint.h>
+#include <string.h>
 
 #include <cuda_runtime.h>
 
@@ -79,6 +80,20 @@ int group_of(int fmt) { return fmt == SGQ_FMT_MXFP8 ? 32 : fmt == SGQ_FMT_FP8_BL
 int sm_count();
 
 int dt_of(uint32_t flags) { return (flags & SGQ_F_FP16) ? sgq::DT_F16 : sgq::DT_BF16; }
+
+// bf16 bit pattern nearest to a finite float (ties to even), and back.
+uint32_t bf16_bits_rn(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+}
+
+float bf16_value(uint32_t b) {
+    const uint32_t u = b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
 
 constexpr uint32_t kLayoutFlags = SGQ_F_SCALE_SWIZZLED | SGQ_F_SCALE_COL_MAJOR;
 
@@ -241,7 +256,14 @@ int swiglu_call(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float al
     a.alpha = alpha;
     a.beta = beta;
     a.limit = limit;
-    return launched(sgq::launch_swiglu(fmt, plan, a, static_cast<cudaStream_t>(stream)));
+    // The OAI clamps run on packed bf16 when the limit is a bf16 value and
+    // alpha * limit stays in the range where the sigmoid needs no upper clamp.
+    const uint32_t lb = bf16_bits_rn(limit);
+    const bool clamp16 = act == SGQ_ACT_SWIGLU_OAI && alpha > 0.0f && isfinite(limit) &&
+                         alpha * limit <= 0x1p100f && bf16_value(lb) == limit;
+    a.lim2 = lb | (lb << 16);
+    a.nlim2 = a.lim2 ^ 0x80008000u;
+    return launched(sgq::launch_swiglu(fmt, plan, a, clamp16, static_cast<cudaStream_t>(stream)));
 }
 
 int gcd(int a, int b) { return b == 0 ? a : gcd(b, a % b); }

@@ -119,6 +119,19 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float f[8]) {
     }
 }
 
+// Elementwise min / max of two bf16x2 pairs (finite values: exact).
+__device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // Two floats -> bf16x2 with round-to-nearest-even; `lo` goes to the low half.
 __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
     uint32_t d;

@@ -53,6 +53,7 @@ struct SwigluArgs {
     uint32_t flags;
     int act;
     float alpha, beta, limit;
+    uint32_t lim2, nlim2;    // bf16x2 of limit and -limit (the CLAMP16 kernels)
 };
 
 struct QuantArgs {
@@ -339,7 +340,11 @@ __global__ void __launch_bounds__(kMaxTPR) norm_dual_kernel(const DualArgs d) {
 //         fp32: 0 or 1), carried with its exact FMA residual;
 //   SiLU: a = (g * sigmoid(g)) * u, the first factor rounded to bf16 when
 //         round_silu is set.
-template <int ACT>
+// CLAMPED (OAI only): g and u arrive already clamped to limit (g' and u'),
+// and alpha > 0 with alpha * limit <= 2^100, so g' bounds the sigmoid's
+// argument from above (sigmoid8 is exact there for any argument below
+// 2^120) and only the lower clamp remains.
+template <int ACT, bool CLAMPED = false>
 __device__ __forceinline__ void activation8(const float (&g)[8], const float (&u)[8], float alpha, float beta,
                                             float limit, float glo, float ghi, bool round_silu, float (&a)[8]) {
     float sg[8];
@@ -347,9 +352,10 @@ __device__ __forceinline__ void activation8(const float (&g)[8], const float (&u
         float gc[8], zh[8], nzl[8];
 #pragma unroll
         for (int k = 0; k < 8; k += 2) {
-            gc[k] = fminf(g[k], limit);
-            gc[k + 1] = fminf(g[k + 1], limit);
-            const float2 gs = make_float2(fmaxf(fminf(gc[k], ghi), glo), fmaxf(fminf(gc[k + 1], ghi), glo));
+            gc[k] = CLAMPED ? g[k] : fminf(g[k], limit);
+            gc[k + 1] = CLAMPED ? g[k + 1] : fminf(g[k + 1], limit);
+            const float2 gs = CLAMPED ? make_float2(fmaxf(gc[k], glo), fmaxf(gc[k + 1], glo))
+                                      : make_float2(fmaxf(fminf(gc[k], ghi), glo), fmaxf(fminf(gc[k + 1], ghi), glo));
             const float2 z = __fmul2_rn(f2(alpha), gs);
             const float2 nz = __ffma2_rn(f2(-alpha), gs, z);               // -(residual of alpha * gs)
             zh[k] = z.x;
@@ -360,7 +366,8 @@ __device__ __forceinline__ void activation8(const float (&g)[8], const float (&u
         sigmoid8<true>(zh, nzl, sg);
 #pragma unroll
         for (int k = 0; k < 8; k += 2) {
-            const float2 uc = make_float2(fminf(fmaxf(u[k], -limit), limit), fminf(fmaxf(u[k + 1], -limit), limit));
+            const float2 uc = CLAMPED ? make_float2(u[k], u[k + 1])
+                                      : make_float2(fminf(fmaxf(u[k], -limit), limit), fminf(fmaxf(u[k + 1], -limit), limit));
             const float2 r = __fmul2_rn(__fmul2_rn(make_float2(gc[k], gc[k + 1]), make_float2(sg[k], sg[k + 1])),
                                         __fadd2_rn(uc, f2(beta)));
             a[k] = r.x;
@@ -389,6 +396,23 @@ __device__ __forceinline__ float2 oai_gate_range(float alpha) {
     return make_float2(-INFINITY, INFINITY);
 }
 
+// One chunk of gate and up from their shared-memory slots, widened to fp32;
+// with CLAMP16, g = min(g, limit) and u = clamp(u, -limit, limit) first, on
+// the packed bf16 pairs (exact: limit is a bf16 value).
+template <bool CLAMP16>
+__device__ __forceinline__ void load_gate_up(const uint4* gs, const uint4* us, const SwigluArgs& a, float (&g)[8],
+                                             float (&u)[8]) {
+    uint4 gw = ld_smem16(gs), uw = ld_smem16(us);
+    if (CLAMP16) {
+        gw = make_uint4(bf16x2_min(gw.x, a.lim2), bf16x2_min(gw.y, a.lim2), bf16x2_min(gw.z, a.lim2),
+                        bf16x2_min(gw.w, a.lim2));
+        uw = make_uint4(bf16x2_max(bf16x2_min(uw.x, a.lim2), a.nlim2), bf16x2_max(bf16x2_min(uw.y, a.lim2), a.nlim2),
+                        bf16x2_max(bf16x2_min(uw.z, a.lim2), a.nlim2), bf16x2_max(bf16x2_min(uw.w, a.lim2), a.nlim2));
+    }
+    bf16x8_to_f32(gw, g);
+    bf16x8_to_f32(uw, u);
+}
+
 // Bytes of dynamic shared memory the SwiGLU kernel stages its loads in.
 __host__ __device__ constexpr int swiglu_stage_bytes(int nv, int threads) { return nv * 2 * threads * 16; }
 
@@ -397,7 +421,9 @@ __host__ __device__ constexpr int swiglu_stage_bytes(int nv, int threads) { retu
 // (stage[2v][thread], stage[2v+1][thread]), one commit group per chunk, so
 // the whole row is in flight without holding registers and chunk v is
 // processed as soon as its own group has landed.
-template <int FMT, int LAYOUT, int NV, int ACT, bool FULL>
+// CLAMP16 (OAI only, see activation8): the limit is a bf16 value and the
+// clamps of g and u run on the packed bf16 pairs before widening.
+template <int FMT, int LAYOUT, int NV, int ACT, bool FULL, bool CLAMP16>
 __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs a) {
     extern __shared__ uint4 stage[];
     __shared__ float part_amax[32];
@@ -433,9 +459,8 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
             const int c = t + v * tpr;
             float g[8], u[8], src[8];
             cp_async_wait_group_of<NV>(v);
-            bf16x8_to_f32(ld_smem16(&stage[(2 * v) * nt + threadIdx.x]), g);
-            bf16x8_to_f32(ld_smem16(&stage[(2 * v + 1) * nt + threadIdx.x]), u);
-            activation8<ACT>(g, u, a.alpha, a.beta, a.limit, gr.x, gr.y, round_silu, src);
+            load_gate_up<CLAMP16>(&stage[(2 * v) * nt + threadIdx.x], &stage[(2 * v + 1) * nt + threadIdx.x], a, g, u);
+            activation8<ACT, CLAMP16>(g, u, a.alpha, a.beta, a.limit, gr.x, gr.y, round_silu, src);
             if (a.out) {                   // the unfused activation: bf16 out, no quantisation
                 st16_if(a.out + row * I + (int64_t)c * 8, f32x8_to_bf16x8(src), FULL || (row_ok && c < nchunks));
                 continue;
@@ -455,9 +480,8 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
         for (int v = 0; v < NV; ++v) {
             float g[8], u[8];
             cp_async_wait_group_of<NV>(v);
-            bf16x8_to_f32(ld_smem16(&stage[(2 * v) * nt + threadIdx.x]), g);
-            bf16x8_to_f32(ld_smem16(&stage[(2 * v + 1) * nt + threadIdx.x]), u);
-            activation8<ACT>(g, u, a.alpha, a.beta, a.limit, gr.x, gr.y, round_silu, src[v]);
+            load_gate_up<CLAMP16>(&stage[(2 * v) * nt + threadIdx.x], &stage[(2 * v + 1) * nt + threadIdx.x], a, g, u);
+            activation8<ACT, CLAMP16>(g, u, a.alpha, a.beta, a.limit, gr.x, gr.y, round_silu, src[v]);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 if (!from32) src[v][k] = round_bf16(src[v][k]);

@@ -56,7 +56,9 @@ cudaError_t launch_norm_dual(int fmt, int dt, const Plan& p, const DualArgs& d, 
 
 // Records the CUDA error of a failed launch for sgq_launch_error() (per thread).
 void note_launch_error(cudaError_t e);
-cudaError_t launch_swiglu(int fmt, const Plan& p, const SwigluArgs& a, cudaStream_t stream);
+// clamp16: the OAI kernels that clamp on packed bf16 (see swiglu_quant_kernel).
+cudaError_t launch_swiglu(int fmt, const Plan& p, const SwigluArgs& a, bool clamp16, cudaStream_t stream);
+cudaError_t launch_swiglu_silu(int fmt, const Plan& p, const SwigluArgs& a, cudaStream_t stream);
 cudaError_t launch_quant(int fmt, int dt, const Plan& p, const QuantArgs& a, cudaStream_t stream);
 
 }  // namespace sgq

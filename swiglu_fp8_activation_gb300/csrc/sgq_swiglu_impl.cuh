@@ -1,0 +1,44 @@
+// sgq_swiglu_impl.cuh -- kernel selection and launch of the SwiGLU + quant
+// kernel for one activation; included by the two translation units that
+// instantiate it (OAI and SiLU-and-mul), which compile in parallel.
+#pragma once
+
+#include "sgq_launch.h"
+
+namespace sgq {
+namespace {
+
+template <int ACT, bool CLAMP16>
+struct SwigluPick {
+    using Kernel = void (*)(const SwigluArgs);
+
+    template <int FMT, int LAYOUT, bool FULL>
+    static Kernel pick(int nv) {
+        switch (nv) {
+            case 1: return swiglu_quant_kernel<FMT, LAYOUT, 1, ACT, FULL, CLAMP16>;
+            case 2: return swiglu_quant_kernel<FMT, LAYOUT, 2, ACT, FULL, CLAMP16>;
+            case 3: return swiglu_quant_kernel<FMT, LAYOUT, 3, ACT, FULL, CLAMP16>;
+            default: return swiglu_quant_kernel<FMT, LAYOUT, 4, ACT, FULL, CLAMP16>;
+        }
+    }
+
+    // The instantiated (format, scale layout) pairs, as for the norm.
+    template <bool FULL>
+    static Kernel pick_fmt(int fmt, int layout, int nv) {
+        if (fmt == FMT_MX)
+            return layout == SCALE_SWIZZLED ? pick<FMT_MX, SCALE_SWIZZLED, FULL>(nv)
+                                            : pick<FMT_MX, SCALE_ROW_MAJOR, FULL>(nv);
+        if (fmt == FMT_B128)
+            return layout == SCALE_COL_MAJOR ? pick<FMT_B128, SCALE_COL_MAJOR, FULL>(nv)
+                                             : pick<FMT_B128, SCALE_ROW_MAJOR, FULL>(nv);
+        return pick<FMT_PT, SCALE_ROW_MAJOR, FULL>(nv);
+    }
+
+    static cudaError_t launch(int fmt, const Plan& p, const SwigluArgs& a, cudaStream_t stream) {
+        Kernel k = p.full ? pick_fmt<true>(fmt, a.so.layout, p.nv) : pick_fmt<false>(fmt, a.so.layout, p.nv);
+        return launch_pdl(k, p, a, stream, swiglu_stage_bytes(p.nv, p.rpc * p.tpr));
+    }
+};
+
+}  // namespace
+}  // namespace sgq

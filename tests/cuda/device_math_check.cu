@@ -34,6 +34,23 @@ __global__ void oai_kernel(const float* g, const float* u, float* out, int n, fl
     }
 }
 
+// The same through the pre-clamped form the packed-bf16 kernels use: g and u
+// clamped to limit first, then activation8<ACT_OAI, true>.
+__global__ void oai_clamped_kernel(const float* g, const float* u, float* out, int n, float alpha, float beta,
+                                   float limit) {
+    const int i = 8 * (blockIdx.x * blockDim.x + threadIdx.x);
+    if (i < n) {
+        float gg[8], uu[8], r[8];
+        for (int k = 0; k < 8; ++k) {
+            gg[k] = fminf(g[i + k], limit);
+            uu[k] = fminf(fmaxf(u[i + k], -limit), limit);
+        }
+        const float2 gr = sgq::oai_gate_range(alpha);
+        sgq::activation8<sgq::ACT_OAI, true>(gg, uu, alpha, beta, limit, gr.x, gr.y, false, r);
+        for (int k = 0; k < 8; ++k) out[i + k] = r[k];
+    }
+}
+
 // n must be even: pairs (i, i+1) go through the packed form, each with its
 // own divisor, and every element also through the scalar form.
 __global__ void div_kernel(const float* a, const float* b, float* q_fast, float* q_pack, float* q_ieee, int n) {
@@ -59,6 +76,12 @@ extern "C" int run_sigmoid(const float* z, float* out, int n) {
 
 extern "C" int run_oai(const float* g, const float* u, float* out, int n, float alpha, float beta, float limit) {
     oai_kernel<<<(n / 8 + 256) / 256, 256>>>(g, u, out, n, alpha, beta, limit);
+    return (int)cudaDeviceSynchronize();
+}
+
+extern "C" int run_oai_clamped(const float* g, const float* u, float* out, int n, float alpha, float beta,
+                               float limit) {
+    oai_clamped_kernel<<<(n / 8 + 256) / 256, 256>>>(g, u, out, n, alpha, beta, limit);
     return (int)cudaDeviceSynchronize();
 }
 

@@ -31,7 +31,7 @@ def devlib():
            "-o", so, os.path.join(ROOT, "tests", "cuda", "device_math_check.cu")]
     subprocess.run(cmd, check=True)
     L = C.CDLL(so)
-    for f in (L.run_sigmoid, L.run_div, L.run_oai):
+    for f in (L.run_sigmoid, L.run_div, L.run_oai, L.run_oai_clamped):
         f.restype = C.c_int
     return L
 
@@ -58,7 +58,8 @@ def test_sigmoid_accuracy(devlib):
     assert (got[z == 0] == 0.5).all()
 
 
-def test_oai_activation_accuracy(devlib):
+@pytest.mark.parametrize("clamped", [False, True])
+def test_oai_activation_accuracy(devlib, clamped):
     rng = np.random.default_rng(2)
     n = 2_000_000
     g = torch.from_numpy(rng.standard_normal(n) * 4.0).bfloat16().float().numpy()
@@ -68,7 +69,8 @@ def test_oai_activation_accuracy(devlib):
     alpha, beta, limit = np.float32(1.702), 1.0, 7.0
     gt, ut = torch.from_numpy(g).cuda(), torch.from_numpy(u).cuda()
     out = torch.empty_like(gt)
-    assert devlib.run_oai(_p(gt), _p(ut), _p(out), n, C.c_float(alpha), C.c_float(beta), C.c_float(limit)) == 0
+    run = devlib.run_oai_clamped if clamped else devlib.run_oai
+    assert run(_p(gt), _p(ut), _p(out), n, C.c_float(alpha), C.c_float(beta), C.c_float(limit)) == 0
     got = out.cpu().numpy().astype(np.float64)
     gc = np.minimum(g.astype(np.float64), limit)
     uc = np.clip(u.astype(np.float64), -limit, limit)

@@ -156,8 +156,13 @@ def test_swiglu_formats_ragged(fmt, act, from_fp32, round_bf16):
 
 def test_oai_parameters_and_unclamped_limit():
     gu = inputs.swiglu_inputs(16, 1024, seed=9, std=4.0)
+    # limits that are bf16 values take the packed-bf16 clamps; the others
+    # (7.1, inf), a negative alpha and a huge alpha * limit take the general path
     run_swiglu("mxfp8", "swiglu_oai", gu, from_fp32=True, alpha=1.0, beta=0.5, limit=3.0)
     run_swiglu("block128", "swiglu_oai", gu, from_fp32=True, limit=float("inf"))
+    run_swiglu("mxfp8", "swiglu_oai", gu, from_fp32=True, limit=float(np.float32(7.1)))
+    run_swiglu("per_token", "swiglu_oai", gu, from_fp32=False, alpha=-1.5, limit=5.0)
+    run_swiglu("mxfp8", "swiglu_oai", gu, from_fp32=True, alpha=2.0 ** 90, limit=2.0 ** 14)
 
 
 # ------------------------------------------------------------ edge rows
