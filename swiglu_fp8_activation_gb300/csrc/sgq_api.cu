@@ -261,6 +261,10 @@ int swiglu_call(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float al
     const uint32_t lb = bf16_bits_rn(limit);
     const bool clamp16 = act == SGQ_ACT_SWIGLU_OAI && alpha > 0.0f && isfinite(limit) &&
                          alpha * limit <= 0x1p100f && bf16_value(lb) == limit;
+    // -alpha log2(e) in two fp32 parts (head rounded, then the rest)
+    const double k = -(double)alpha * 1.4426950408889634074;
+    a.khi = (float)k;
+    a.klo = (float)(k - (double)a.khi);
     a.lim2 = lb | (lb << 16);
     a.nlim2 = a.lim2 ^ 0x80008000u;
     return launched(sgq::launch_swiglu(fmt, plan, a, clamp16, static_cast<cudaStream_t>(stream)));

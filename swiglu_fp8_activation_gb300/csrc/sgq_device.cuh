@@ -240,40 +240,39 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-// Arguments of sigmoid8() must lie in [kSigLo, kSigHi]. Past kSigHi the
-// sigmoid is 1.0 in fp32 (1 - e^-20 rounds to 1); below kSigLo it is 0
-// (e^-104 is below half the smallest fp32 subnormal), so callers clamp first.
+// Arguments z of the sigmoid must lie in [kSigLo, kSigHi] (callers clamp).
+// Past kSigHi the sigmoid is 1.0 in fp32 (1 - e^-20 rounds to 1); below
+// kSigLo it is 0 (e^-104 is below half the smallest fp32 subnormal).
 constexpr float kSigLo = -104.0f, kSigHi = 20.0f;
 
-// Logistic sigmoid 1/(1 + E), E = e^-z, of the 8 values of one chunk, with
-// z = zh - nzl (nzl: the negated exact residual of the fp32 product that
-// formed zh, used when TAIL is set). Written from the mathematics on packed
+// Logistic sigmoid 1/(1 + E), E = e^-z, of the 8 values of one chunk, for
+// z = kz * x given as x and the negated scaled log2(e) split in fp32 parts:
+// khi + klo = -kz log2(e) (kz = 1 for the plain sigmoid, alpha for OAI), so
+// that E = 2^q with q = (khi + klo) x. Written from the mathematics on packed
 // fp32x2 arithmetic:
-//   * E = 2^q, q = -z log2 e carried as head qh = RN(-z log2e_hi) plus tail
-//     (the FMA residual of that product, z log2e_lo and the residual of z),
-//     in the manner of Cody and Waite's argument reduction, so q = qh - tail
-//     with |tail| < 2^-16;
+//   * q is carried as the head qh = RN(khi x) plus a tail: the exact FMA
+//     residual of that product and klo x, in the manner of Cody and Waite's
+//     argument reduction; |tail| < 2^-16;
 //   * the hardware 2^x takes the head, whose every value it evaluates to
 //     about 2 ulp, and the tail enters to first order:
-//     2^q = 2^qh (1 - tail ln 2), the dropped second-order term being below
+//     2^q = 2^qh (1 + tail ln 2), the dropped second-order term being below
 //     2^-33 relative;
 //   * sigmoid = 1/(1+E), the hardware reciprocal refined by one
 //     Newton-Raphson step. Where qh > 125 (z < -86.6, a branch taken once
 //     per chunk) 1/(1+E) would leave the normal range, and the sigmoid, then
-//     2^-q to within 2^-125 relative, is formed as 2^(126-qh) (1 + tail ln 2)
+//     2^-q to within 2^-125 relative, is formed as 2^(126-qh) (1 - tail ln 2)
 //     scaled by 2^-126.
-template <bool TAIL>
-__device__ __forceinline__ void sigmoid8(const float (&zh)[8], const float (&nzl)[8], float (&out)[8]) {
+// Valid for any x with |q| below 2^120 whose z is at least kSigLo.
+__device__ __forceinline__ void sigmoid8(const float (&x)[8], float khi, float klo, float (&out)[8]) {
     float2 e[4], m[4];
     float qmax = -1.0e30f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float2 z = make_float2(zh[2 * i], zh[2 * i + 1]);
-        const float2 qh = __fmul2_rn(z, f2(-kLog2eHi));                  // -z log2e, rounded
-        float2 tail = __ffma2_rn(z, f2(kLog2eHi), qh);                   // z log2e_hi + qh, exact
-        tail = __ffma2_rn(z, f2(kLog2eLo), tail);
-        if (TAIL) tail = __ffma2_rn(make_float2(nzl[2 * i], nzl[2 * i + 1]), f2(-kLog2eHi), tail);   // q = qh - tail
-        m[i] = __fmul2_rn(tail, f2(-kLn2));                              // 2^q = 2^qh (1 + m)
+        const float2 xv = make_float2(x[2 * i], x[2 * i + 1]);
+        const float2 qh = __fmul2_rn(xv, f2(khi));                       // head, rounded
+        const float2 nr = __ffma2_rn(xv, f2(-khi), qh);                  // -(khi x - qh), exact
+        const float2 nt = __ffma2_rn(xv, f2(-klo), nr);                  // -tail
+        m[i] = __fmul2_rn(nt, f2(-kLn2));                                // 2^q = 2^qh (1 + m)
         e[i] = make_float2(ex2_approx(qh.x), ex2_approx(qh.y));
         qmax = fmaxf(qmax, fmaxf(qh.x, qh.y));
     }
@@ -293,7 +292,7 @@ __device__ __forceinline__ void sigmoid8(const float (&zh)[8], const float (&nzl
         for (int i = 0; i < 4; ++i) {
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                const float qh = zh[2 * i + j] * -kLog2eHi;
+                const float qh = x[2 * i + j] * khi;
                 if (qh > 125.0f) {
                     const float mj = j ? m[i].y : m[i].x;
                     const float v = ex2_approx(126.0f - qh);             // 2^(126 - qh), in [2^-24, 2]

@@ -54,6 +54,7 @@ struct SwigluArgs {
     int act;
     float alpha, beta, limit;
     uint32_t lim2, nlim2;    // bf16x2 of limit and -limit (the CLAMP16 kernels)
+    float khi, klo;          // -alpha log2(e) in two fp32 parts (OAI)
 };
 
 struct QuantArgs {
@@ -337,7 +338,8 @@ __global__ void __launch_bounds__(kMaxTPR) norm_dual_kernel(const DualArgs d) {
 //         argument is alpha * clamp(g', glo, ghi), with [glo, ghi] the g'
 //         that alpha maps into [kSigLo, kSigHi] (where the clamp acts, the
 //         sigmoid of the clamped argument already equals the true one in
-//         fp32: 0 or 1), carried with its exact FMA residual;
+//         fp32: 0 or 1); alpha enters the sigmoid's exponent through
+//         khi + klo = -alpha log2(e) (two fp32 parts from the host);
 //   SiLU: a = (g * sigmoid(g)) * u, the first factor rounded to bf16 when
 //         round_silu is set.
 // CLAMPED (OAI only): g and u arrive already clamped to limit (g' and u'),
@@ -345,25 +347,18 @@ __global__ void __launch_bounds__(kMaxTPR) norm_dual_kernel(const DualArgs d) {
 // argument from above (sigmoid8 is exact there for any argument below
 // 2^120) and only the lower clamp remains.
 template <int ACT, bool CLAMPED = false>
-__device__ __forceinline__ void activation8(const float (&g)[8], const float (&u)[8], float alpha, float beta,
-                                            float limit, float glo, float ghi, bool round_silu, float (&a)[8]) {
+__device__ __forceinline__ void activation8(const float (&g)[8], const float (&u)[8], float khi, float klo,
+                                            float beta, float limit, float glo, float ghi, bool round_silu,
+                                            float (&a)[8]) {
     float sg[8];
     if (ACT == ACT_OAI) {
-        float gc[8], zh[8], nzl[8];
+        float gc[8], gs[8];
 #pragma unroll
-        for (int k = 0; k < 8; k += 2) {
+        for (int k = 0; k < 8; ++k) {
             gc[k] = CLAMPED ? g[k] : fminf(g[k], limit);
-            gc[k + 1] = CLAMPED ? g[k + 1] : fminf(g[k + 1], limit);
-            const float2 gs = CLAMPED ? make_float2(fmaxf(gc[k], glo), fmaxf(gc[k + 1], glo))
-                                      : make_float2(fmaxf(fminf(gc[k], ghi), glo), fmaxf(fminf(gc[k + 1], ghi), glo));
-            const float2 z = __fmul2_rn(f2(alpha), gs);
-            const float2 nz = __ffma2_rn(f2(-alpha), gs, z);               // -(residual of alpha * gs)
-            zh[k] = z.x;
-            zh[k + 1] = z.y;
-            nzl[k] = nz.x;
-            nzl[k + 1] = nz.y;
+            gs[k] = CLAMPED ? fmaxf(gc[k], glo) : fmaxf(fminf(gc[k], ghi), glo);
         }
-        sigmoid8<true>(zh, nzl, sg);
+        sigmoid8(gs, khi, klo, sg);                                     // sigmoid(alpha * gs)
 #pragma unroll
         for (int k = 0; k < 8; k += 2) {
             const float2 uc = CLAMPED ? make_float2(u[k], u[k + 1])
@@ -377,7 +372,7 @@ __device__ __forceinline__ void activation8(const float (&g)[8], const float (&u
         float zc[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) zc[k] = fmaxf(fminf(g[k], kSigHi), kSigLo);
-        sigmoid8<false>(zc, zc, sg);
+        sigmoid8(zc, -kLog2eHi, -kLog2eLo, sg);
 #pragma unroll
         for (int k = 0; k < 8; k += 2) {
             float2 s = __fmul2_rn(make_float2(g[k], g[k + 1]), make_float2(sg[k], sg[k + 1]));
@@ -460,7 +455,7 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
             float g[8], u[8], src[8];
             cp_async_wait_group_of<NV>(v);
             load_gate_up<CLAMP16>(&stage[(2 * v) * nt + threadIdx.x], &stage[(2 * v + 1) * nt + threadIdx.x], a, g, u);
-            activation8<ACT, CLAMP16>(g, u, a.alpha, a.beta, a.limit, gr.x, gr.y, round_silu, src);
+            activation8<ACT, CLAMP16>(g, u, a.khi, a.klo, a.beta, a.limit, gr.x, gr.y, round_silu, src);
             if (a.out) {                   // the unfused activation: bf16 out, no quantisation
                 st16_if(a.out + row * I + (int64_t)c * 8, f32x8_to_bf16x8(src), FULL || (row_ok && c < nchunks));
                 continue;
@@ -481,7 +476,7 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
             float g[8], u[8];
             cp_async_wait_group_of<NV>(v);
             load_gate_up<CLAMP16>(&stage[(2 * v) * nt + threadIdx.x], &stage[(2 * v + 1) * nt + threadIdx.x], a, g, u);
-            activation8<ACT, CLAMP16>(g, u, a.alpha, a.beta, a.limit, gr.x, gr.y, round_silu, src[v]);
+            activation8<ACT, CLAMP16>(g, u, a.khi, a.klo, a.beta, a.limit, gr.x, gr.y, round_silu, src[v]);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 if (!from32) src[v][k] = round_bf16(src[v][k]);

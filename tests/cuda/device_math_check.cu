@@ -14,7 +14,7 @@ __global__ void sigmoid_kernel(const float* z, float* out, int n) {
     if (i < n) {
         float zz[8], r[8];
         for (int k = 0; k < 8; ++k) zz[k] = fmaxf(fminf(z[i + k], sgq::kSigHi), sgq::kSigLo);
-        sgq::sigmoid8<false>(zz, zz, r);
+        sgq::sigmoid8(zz, -sgq::kLog2eHi, -sgq::kLog2eLo, r);
         for (int k = 0; k < 8; ++k) out[i + k] = r[k];
     }
 }
@@ -29,7 +29,9 @@ __global__ void oai_kernel(const float* g, const float* u, float* out, int n, fl
             uu[k] = u[i + k];
         }
         const float2 gr = sgq::oai_gate_range(alpha);
-        sgq::activation8<sgq::ACT_OAI>(gg, uu, alpha, beta, limit, gr.x, gr.y, false, r);
+        const double kk = -(double)alpha * 1.4426950408889634074;
+        const float khi = (float)kk, klo = (float)(kk - (double)khi);
+        sgq::activation8<sgq::ACT_OAI>(gg, uu, khi, klo, beta, limit, gr.x, gr.y, false, r);
         for (int k = 0; k < 8; ++k) out[i + k] = r[k];
     }
 }
@@ -46,7 +48,9 @@ __global__ void oai_clamped_kernel(const float* g, const float* u, float* out, i
             uu[k] = fminf(fmaxf(u[i + k], -limit), limit);
         }
         const float2 gr = sgq::oai_gate_range(alpha);
-        sgq::activation8<sgq::ACT_OAI, true>(gg, uu, alpha, beta, limit, gr.x, gr.y, false, r);
+        const double kk = -(double)alpha * 1.4426950408889634074;
+        const float khi = (float)kk, klo = (float)(kk - (double)khi);
+        sgq::activation8<sgq::ACT_OAI, true>(gg, uu, khi, klo, beta, limit, gr.x, gr.y, false, r);
         for (int k = 0; k < 8; ++k) out[i + k] = r[k];
     }
 }

@@ -1,13 +1,16 @@
 """The two arithmetic shortcuts of the kernels, checked on the GPU:
 
-* sigmoid8() (split exponent, fitted 2^x polynomial, refined reciprocal)
-  against fp64 over |z| <= 130, within 2^-22 relative;
-* activation8() (the OAI SwiGLU of the kernels) against fp64, within 2^-21
-  relative, including an element whose exact value lies 3.1e-7 relative
-  above an E4M3 rounding boundary;
-* div_rn() (one reciprocal per group + Markstein's FMA correction) against
-  CUDA's correctly rounded __fdiv_rn, bit for bit, for the FP8 quotients the
-  kernels form (|a| <= b * 448 * (1 + 2^-20), b normal) and for random pairs.
+* sigmoid8() (head/tail split exponent, hardware 2^x with a first-order
+  tail correction, refined reciprocal) against fp64 over |z| <= 130, within
+  2^-22 relative;
+* activation8() (the OAI SwiGLU of the kernels, in its general and its
+  pre-clamped form) against fp64, within 2^-21 relative, including an
+  element whose exact value lies 3.1e-7 relative above an E4M3 rounding
+  boundary;
+* div_rn() and div2_rn() (one reciprocal per group + Markstein's FMA
+  correction) against CUDA's correctly rounded __fdiv_rn, bit for bit, for
+  the FP8 quotients the kernels form (|a| <= b * 448 * (1 + 2^-20), b
+  normal) and for random pairs.
 """
 import ctypes as C
 import os
