@@ -3,6 +3,8 @@
 // the thread-to-data mapping.
 #pragma once
 
+#include <type_traits>
+
 #include "sgq_device.cuh"
 
 namespace sgq {
@@ -228,7 +230,9 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
 
     // 2. h = x + r in fp32; write the updated residual; z = h * w'; partial
     //    sum of squares (and max |z| for the per-token format)
-    const bool gemma = (a.flags & F_GEMMA) != 0, from32 = (a.flags & F_FROM_FP32) != 0;
+    const bool from32 = (a.flags & F_FROM_FP32) != 0;
+    // w' = w + 1 (Gemma) or w + (-0), which is w exactly, signed zeros included
+    const float w_add = (a.flags & F_GEMMA) ? 1.0f : -0.0f;
     float z[NV][8];
     float2 ss2 = make_float2(0.0f, 0.0f);
     float zmax = 0.0f;
@@ -253,8 +257,7 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
 #pragma unroll
         for (int k = 0; k < 8; k += 2) {
             const float2 hp = make_float2(h[k], h[k + 1]);
-            float2 wp = make_float2(wf[k], wf[k + 1]);
-            if (gemma) wp = __fadd2_rn(wp, f2(1.0f));              // 1 + w
+            const float2 wp = __fadd2_rn(make_float2(wf[k], wf[k + 1]), f2(w_add));
             ss2 = __ffma2_rn(hp, hp, ss2);
             const float2 zp = __fmul2_rn(hp, wp);
             z[v][k] = zp.x;
@@ -287,28 +290,39 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
         const float ymax = inv * row_zmax;                     // = max |y| exactly
         pt = per_token_scale(from32 ? ymax : round_io<DT>(ymax));
     }
+    const bool normed = a.normed != nullptr;
+    // the chunk loop, specialised for the three cases (no quantisation; a
+    // 16-bit or an fp32 quant source) so that no per-chunk branch remains
+    auto emit = [&](auto quant_tag, auto from32_tag) {
+        constexpr bool QUANT = decltype(quant_tag)::value, FROM32 = decltype(from32_tag)::value;
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
-        const int c = t + v * tpr;
-        const bool ok = FULL || (row_ok && c < nchunks);
-        float y[8], src[8];
+        for (int v = 0; v < NV; ++v) {
+            const int c = t + v * tpr;
+            const bool ok = FULL || (row_ok && c < nchunks);
+            float y[8], src[8];
 #pragma unroll
-        for (int k = 0; k < 8; k += 2) {                       // z = 0 past the row end (zero-filled copies)
-            const float2 yp = __fmul2_rn(f2(inv), make_float2(z[v][k], z[v][k + 1]));
-            y[k] = yp.x;
-            y[k + 1] = yp.y;
+            for (int k = 0; k < 8; k += 2) {                   // z = 0 past the row end (zero-filled copies)
+                const float2 yp = __fmul2_rn(f2(inv), make_float2(z[v][k], z[v][k + 1]));
+                y[k] = yp.x;
+                y[k + 1] = yp.y;
+            }
+            const uint4 yb = pack8<DT>(y);
+            st16_if(a.normed + base + (int64_t)c * 8, yb, normed && ok);
+            if (QUANT) {
+                if (FROM32) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) src[k] = y[k];
+                } else {
+                    load8<DT>(yb, src);
+                }
+                quantize_chunk<FMT, LAYOUT>(src, row, c, ok, FULL || (srow_ok && c < nchunks), H, a.q, sr, pt.x,
+                                            pt.y);
+            }
         }
-        const uint4 yb = pack8<DT>(y);
-        if (a.normed) st16_if(a.normed + base + (int64_t)c * 8, yb, ok);
-        if (!quant) continue;
-        if (from32) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) src[k] = y[k];
-        } else {
-            load8<DT>(yb, src);
-        }
-        quantize_chunk<FMT, LAYOUT>(src, row, c, ok, FULL || (srow_ok && c < nchunks), H, a.q, sr, pt.x, pt.y);
-    }
+    };
+    if (!quant) emit(std::false_type{}, std::false_type{});
+    else if (from32) emit(std::true_type{}, std::true_type{});
+    else emit(std::true_type{}, std::false_type{});
 }
 
 template <int FMT, int LAYOUT, int NV, bool HAS_RES, bool FULL, int DT>
@@ -341,15 +355,14 @@ __global__ void __launch_bounds__(kMaxTPR) norm_dual_kernel(const DualArgs d) {
 //         fp32: 0 or 1); alpha enters the sigmoid's exponent through
 //         khi + klo = -alpha log2(e) (two fp32 parts from the host);
 //   SiLU: a = (g * sigmoid(g)) * u, the first factor rounded to bf16 when
-//         round_silu is set.
+//         ROUND is set.
 // CLAMPED (OAI only): g and u arrive already clamped to limit (g' and u'),
 // and alpha > 0 with alpha * limit <= 2^100, so g' bounds the sigmoid's
 // argument from above (sigmoid8 is exact there for any argument below
 // 2^120) and only the lower clamp remains.
-template <int ACT, bool CLAMPED = false>
+template <int ACT, bool CLAMPED = false, bool ROUND = false>
 __device__ __forceinline__ void activation8(const float (&g)[8], const float (&u)[8], float khi, float klo,
-                                            float beta, float limit, float glo, float ghi, bool round_silu,
-                                            float (&a)[8]) {
+                                            float beta, float limit, float glo, float ghi, float (&a)[8]) {
     float sg[8];
     if (ACT == ACT_OAI) {
         float gc[8], gs[8];
@@ -376,7 +389,7 @@ __device__ __forceinline__ void activation8(const float (&g)[8], const float (&u
 #pragma unroll
         for (int k = 0; k < 8; k += 2) {
             float2 s = __fmul2_rn(make_float2(g[k], g[k + 1]), make_float2(sg[k], sg[k + 1]));
-            if (round_silu) s = make_float2(round_bf16(s.x), round_bf16(s.y));
+            if (ROUND) s = make_float2(round_bf16(s.x), round_bf16(s.y));
             const float2 r = __fmul2_rn(s, make_float2(u[k], u[k + 1]));
             a[k] = r.x;
             a[k + 1] = r.y;
@@ -448,48 +461,76 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
     const float2 gr = oai_gate_range(a.alpha);
     const bool srow_ok = FULL || row < a.so.Ms;
     const ScaleRow sr = scale_row<FMT, LAYOUT>(a.so, row);
-    if (FMT != FMT_PT) {               // MX and 1x128: chunk by chunk, as each lands
+    // The chunk loops, specialised by output mode (0: the bf16 activation,
+    // no quantisation; 1: quantise the fp32 activation; 2: quantise its bf16
+    // rounding) and SiLU's bf16 rounding, so that no per-chunk branch remains.
+    auto body = [&](auto mode_tag, auto round_tag) {
+        constexpr int MODE = decltype(mode_tag)::value;
+        constexpr bool ROUND = decltype(round_tag)::value;
+        if (FMT != FMT_PT) {           // MX and 1x128: chunk by chunk, as each lands
 #pragma unroll
-        for (int v = 0; v < NV; ++v) {
-            const int c = t + v * tpr;
-            float g[8], u[8], src[8];
-            cp_async_wait_group_of<NV>(v);
-            load_gate_up<CLAMP16>(&stage[(2 * v) * nt + threadIdx.x], &stage[(2 * v + 1) * nt + threadIdx.x], a, g, u);
-            activation8<ACT, CLAMP16>(g, u, a.khi, a.klo, a.beta, a.limit, gr.x, gr.y, round_silu, src);
-            if (a.out) {                   // the unfused activation: bf16 out, no quantisation
-                st16_if(a.out + row * I + (int64_t)c * 8, f32x8_to_bf16x8(src), FULL || (row_ok && c < nchunks));
-                continue;
+            for (int v = 0; v < NV; ++v) {
+                const int c = t + v * tpr;
+                const bool ok = FULL || (row_ok && c < nchunks);
+                float g[8], u[8], src[8];
+                cp_async_wait_group_of<NV>(v);
+                load_gate_up<CLAMP16>(&stage[(2 * v) * nt + threadIdx.x], &stage[(2 * v + 1) * nt + threadIdx.x], a,
+                                      g, u);
+                activation8<ACT, CLAMP16, ROUND>(g, u, a.khi, a.klo, a.beta, a.limit, gr.x, gr.y, src);
+                if (MODE == 0) {
+                    st16_if(a.out + row * I + (int64_t)c * 8, f32x8_to_bf16x8(src), ok);
+                } else {
+                    if (MODE == 2) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) src[k] = round_bf16(src[k]);
+                    }
+                    // chunks past the row end loaded zeros, and every activation of 0 and 0 is 0
+                    quantize_chunk<FMT, LAYOUT>(src, row, c, ok, FULL || (srow_ok && c < nchunks), I, a.q, sr);
+                }
             }
-            if (!from32) {
+        } else {                       // per-token: the whole row, then its amax
+            float src[NV][8];
+            float m = 0.0f;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) src[k] = round_bf16(src[k]);
+            for (int v = 0; v < NV; ++v) {
+                float g[8], u[8];
+                cp_async_wait_group_of<NV>(v);
+                load_gate_up<CLAMP16>(&stage[(2 * v) * nt + threadIdx.x], &stage[(2 * v + 1) * nt + threadIdx.x], a,
+                                      g, u);
+                activation8<ACT, CLAMP16, ROUND>(g, u, a.khi, a.klo, a.beta, a.limit, gr.x, gr.y, src[v]);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    if (MODE == 2) src[v][k] = round_bf16(src[v][k]);
+                    m = fmaxf(m, fabsf(src[v][k]));
+                }
             }
-            // chunks past the row end loaded zeros, and every activation of 0 and 0 is 0
-            quantize_chunk<FMT, LAYOUT>(src, row, c, FULL || (row_ok && c < nchunks), FULL || (srow_ok && c < nchunks), I,
-                                a.q, sr);
-        }
-    } else {                           // per-token: the whole row, then its amax
-        float src[NV][8];
-        float m = 0.0f;
+            if (MODE == 0) {           // (the bf16-out launches use the MX kernels; kept complete here)
 #pragma unroll
-        for (int v = 0; v < NV; ++v) {
-            float g[8], u[8];
-            cp_async_wait_group_of<NV>(v);
-            load_gate_up<CLAMP16>(&stage[(2 * v) * nt + threadIdx.x], &stage[(2 * v + 1) * nt + threadIdx.x], a, g, u);
-            activation8<ACT, CLAMP16>(g, u, a.khi, a.klo, a.beta, a.limit, gr.x, gr.y, round_silu, src[v]);
+                for (int v = 0; v < NV; ++v) {
+                    const int c = t + v * tpr;
+                    st16_if(a.out + row * I + (int64_t)c * 8, f32x8_to_bf16x8(src[v]), FULL || (row_ok && c < nchunks));
+                }
+                return;
+            }
+            const float2 pt = per_token_scale(row_reduce<true>(m, part_amax, tpr, lrow));
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                if (!from32) src[v][k] = round_bf16(src[v][k]);
-                m = fmaxf(m, fabsf(src[v][k]));
+            for (int v = 0; v < NV; ++v) {
+                const int c = t + v * tpr;
+                quantize_chunk<FMT, LAYOUT>(src[v], row, c, FULL || (row_ok && c < nchunks),
+                                            FULL || (srow_ok && c < nchunks), I, a.q, sr, pt.x, pt.y);
             }
         }
-        const float2 pt = per_token_scale(row_reduce<true>(m, part_amax, tpr, lrow));
-#pragma unroll
-        for (int v = 0; v < NV; ++v) {
-            const int c = t + v * tpr;
-            quantize_chunk<FMT, LAYOUT>(src[v], row, c, FULL || (row_ok && c < nchunks), FULL || (srow_ok && c < nchunks),
-                                I, a.q, sr, pt.x, pt.y);
-        }
+    };
+    auto by_mode = [&](auto round_tag) {
+        if (a.out) body(std::integral_constant<int, 0>{}, round_tag);
+        else if (from32) body(std::integral_constant<int, 1>{}, round_tag);
+        else body(std::integral_constant<int, 2>{}, round_tag);
+    };
+    if constexpr (ACT == ACT_SILU) {
+        if (round_silu) by_mode(std::true_type{});
+        else by_mode(std::false_type{});
+    } else {
+        by_mode(std::false_type{});
     }
 }
 

@@ -58,7 +58,10 @@ cudaError_t launch_norm_dual(int fmt, int dt, const Plan& p, const DualArgs& d, 
 void note_launch_error(cudaError_t e);
 // clamp16: the OAI kernels that clamp on packed bf16 (see swiglu_quant_kernel).
 cudaError_t launch_swiglu(int fmt, const Plan& p, const SwigluArgs& a, bool clamp16, cudaStream_t stream);
-cudaError_t launch_swiglu_silu(int fmt, const Plan& p, const SwigluArgs& a, cudaStream_t stream);
+cudaError_t launch_swiglu_oai_full(int fmt, const Plan& p, const SwigluArgs& a, bool clamp16, cudaStream_t stream);
+cudaError_t launch_swiglu_oai_part(int fmt, const Plan& p, const SwigluArgs& a, bool clamp16, cudaStream_t stream);
+cudaError_t launch_swiglu_silu_full(int fmt, const Plan& p, const SwigluArgs& a, cudaStream_t stream);
+cudaError_t launch_swiglu_silu_part(int fmt, const Plan& p, const SwigluArgs& a, cudaStream_t stream);
 cudaError_t launch_quant(int fmt, int dt, const Plan& p, const QuantArgs& a, cudaStream_t stream);
 
 }  // namespace sgq

@@ -1,6 +1,7 @@
 // sgq_swiglu_impl.cuh -- kernel selection and launch of the SwiGLU + quant
-// kernel for one activation; included by the two translation units that
-// instantiate it (OAI and SiLU-and-mul), which compile in parallel.
+// kernel; included by the translation units that instantiate it (OAI and
+// SiLU-and-mul, each exact-fit and bounds-checked), which compile in
+// parallel.
 #pragma once
 
 #include "sgq_launch.h"
@@ -34,8 +35,11 @@ struct SwigluPick {
         return pick<FMT_PT, SCALE_ROW_MAJOR, FULL>(nv);
     }
 
+    // The exact-fit (FULL) and the bounds-checked kernels are instantiated in
+    // separate translation units, which compile in parallel.
+    template <bool FULL>
     static cudaError_t launch(int fmt, const Plan& p, const SwigluArgs& a, cudaStream_t stream) {
-        Kernel k = p.full ? pick_fmt<true>(fmt, a.so.layout, p.nv) : pick_fmt<false>(fmt, a.so.layout, p.nv);
+        Kernel k = pick_fmt<FULL>(fmt, a.so.layout, p.nv);
         return launch_pdl(k, p, a, stream, swiglu_stage_bytes(p.nv, p.rpc * p.tpr));
     }
 };

@@ -1,10 +1,10 @@
-// sgq_swiglu_silu.cu -- the SwiGLU + quant kernel for SiLU-and-mul.
+// sgq_swiglu_silu.cu -- the exact-fit SwiGLU + quant kernels for SiLU-and-mul.
 #include "sgq_swiglu_impl.cuh"
 
 namespace sgq {
 
-cudaError_t launch_swiglu_silu(int fmt, const Plan& p, const SwigluArgs& a, cudaStream_t stream) {
-    return SwigluPick<ACT_SILU, false>::launch(fmt, p, a, stream);
+cudaError_t launch_swiglu_silu_full(int fmt, const Plan& p, const SwigluArgs& a, cudaStream_t stream) {
+    return SwigluPick<ACT_SILU, false>::launch<true>(fmt, p, a, stream);
 }
 
 }  // namespace sgq

@@ -31,7 +31,7 @@ __global__ void oai_kernel(const float* g, const float* u, float* out, int n, fl
         const float2 gr = sgq::oai_gate_range(alpha);
         const double kk = -(double)alpha * 1.4426950408889634074;
         const float khi = (float)kk, klo = (float)(kk - (double)khi);
-        sgq::activation8<sgq::ACT_OAI>(gg, uu, khi, klo, beta, limit, gr.x, gr.y, false, r);
+        sgq::activation8<sgq::ACT_OAI>(gg, uu, khi, klo, beta, limit, gr.x, gr.y, r);
         for (int k = 0; k < 8; ++k) out[i + k] = r[k];
     }
 }
@@ -50,7 +50,7 @@ __global__ void oai_clamped_kernel(const float* g, const float* u, float* out, i
         const float2 gr = sgq::oai_gate_range(alpha);
         const double kk = -(double)alpha * 1.4426950408889634074;
         const float khi = (float)kk, klo = (float)(kk - (double)khi);
-        sgq::activation8<sgq::ACT_OAI, true>(gg, uu, khi, klo, beta, limit, gr.x, gr.y, false, r);
+        sgq::activation8<sgq::ACT_OAI, true>(gg, uu, khi, klo, beta, limit, gr.x, gr.y, r);
         for (int k = 0; k < 8; ++k) out[i + k] = r[k];
     }
 }
