@@ -144,6 +144,13 @@ __device__ __forceinline__ uint4 f32x8_to_bf16x8(const float f[8]) {
                       f32x2_to_bf16x2(f[4], f[5]), f32x2_to_bf16x2(f[6], f[7]));
 }
 
+// Round two floats to the nearest bf16 (ties to even) and widen them back:
+// one conversion for the pair.
+__device__ __forceinline__ float2 round_bf16x2(float2 v) {
+    const uint32_t p = f32x2_to_bf16x2(v.x, v.y);
+    return make_float2(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u));
+}
+
 // Round a float to the nearest bf16 (ties to even) and widen it back.
 __device__ __forceinline__ float round_bf16(float v) {
     return __uint_as_float(f32x2_to_bf16x2(v, 0.0f) << 16);

@@ -389,7 +389,7 @@ __device__ __forceinline__ void activation8(const float (&g)[8], const float (&u
 #pragma unroll
         for (int k = 0; k < 8; k += 2) {
             float2 s = __fmul2_rn(make_float2(g[k], g[k + 1]), make_float2(sg[k], sg[k + 1]));
-            if (ROUND) s = make_float2(round_bf16(s.x), round_bf16(s.y));
+            if (ROUND) s = round_bf16x2(s);
             const float2 r = __fmul2_rn(s, make_float2(u[k], u[k + 1]));
             a[k] = r.x;
             a[k + 1] = r.y;
@@ -482,7 +482,11 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
                 } else {
                     if (MODE == 2) {
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) src[k] = round_bf16(src[k]);
+                        for (int k = 0; k < 8; k += 2) {
+                            const float2 r = round_bf16x2(make_float2(src[k], src[k + 1]));
+                            src[k] = r.x;
+                            src[k + 1] = r.y;
+                        }
                     }
                     // chunks past the row end loaded zeros, and every activation of 0 and 0 is 0
                     quantize_chunk<FMT, LAYOUT>(src, row, c, ok, FULL || (srow_ok && c < nchunks), I, a.q, sr);
@@ -499,9 +503,13 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
                                       g, u);
                 activation8<ACT, CLAMP16, ROUND>(g, u, a.khi, a.klo, a.beta, a.limit, gr.x, gr.y, src[v]);
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    if (MODE == 2) src[v][k] = round_bf16(src[v][k]);
-                    m = fmaxf(m, fabsf(src[v][k]));
+                for (int k = 0; k < 8; k += 2) {
+                    if (MODE == 2) {
+                        const float2 r = round_bf16x2(make_float2(src[v][k], src[v][k + 1]));
+                        src[v][k] = r.x;
+                        src[v][k + 1] = r.y;
+                    }
+                    m = fmaxf(m, fmaxf(fabsf(src[v][k]), fabsf(src[v][k + 1])));
                 }
             }
             if (MODE == 0) {           // (the bf16-out launches use the MX kernels; kept complete here)
