@@ -36,15 +36,16 @@ __global__ void oai_kernel(const float* g, const float* u, float* out, int n, fl
     }
 }
 
-// The same through the pre-clamped form the packed-bf16 kernels use: g and u
-// clamped to limit first, then activation8<ACT_OAI, true>.
+// The same through the pre-clamped form the packed-bf16 kernels use: g
+// clamped to [glo_clamp, limit] and u to limit first, then
+// activation8<ACT_OAI, true>.
 __global__ void oai_clamped_kernel(const float* g, const float* u, float* out, int n, float alpha, float beta,
-                                   float limit) {
+                                   float limit, float glo_clamp) {
     const int i = 8 * (blockIdx.x * blockDim.x + threadIdx.x);
     if (i < n) {
         float gg[8], uu[8], r[8];
         for (int k = 0; k < 8; ++k) {
-            gg[k] = fminf(g[i + k], limit);
+            gg[k] = fmaxf(fminf(g[i + k], limit), glo_clamp);
             uu[k] = fminf(fmaxf(u[i + k], -limit), limit);
         }
         const float2 gr = sgq::oai_gate_range(alpha);
@@ -84,8 +85,8 @@ extern "C" int run_oai(const float* g, const float* u, float* out, int n, float 
 }
 
 extern "C" int run_oai_clamped(const float* g, const float* u, float* out, int n, float alpha, float beta,
-                               float limit) {
-    oai_clamped_kernel<<<(n / 8 + 256) / 256, 256>>>(g, u, out, n, alpha, beta, limit);
+                               float limit, float glo_clamp) {
+    oai_clamped_kernel<<<(n / 8 + 256) / 256, 256>>>(g, u, out, n, alpha, beta, limit, glo_clamp);
     return (int)cudaDeviceSynchronize();
 }
 

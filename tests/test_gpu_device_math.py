@@ -69,18 +69,27 @@ def test_oai_activation_accuracy(devlib, clamped):
     u = torch.from_numpy(rng.standard_normal(n) * 4.0).bfloat16().float().numpy()
     # the element that an error of 2.8e-7 pushed across an E4M3 boundary
     g[:2], u[:2] = -1.578125, -3.25
+    # gates far below zero, where the sigmoid leaves the normal range and
+    # the packed-bf16 kernels clamp from below
+    g[8:8 + 4096] = torch.from_numpy(-np.geomspace(30.0, 3.0e4, 4096)).bfloat16().float().numpy()
     alpha, beta, limit = np.float32(1.702), 1.0, 7.0
     gt, ut = torch.from_numpy(g).cuda(), torch.from_numpy(u).cuda()
     out = torch.empty_like(gt)
-    run = devlib.run_oai_clamped if clamped else devlib.run_oai
-    assert run(_p(gt), _p(ut), _p(out), n, C.c_float(alpha), C.c_float(beta), C.c_float(limit)) == 0
+    if clamped:      # the packed-bf16 kernels' lower gate bound: the bf16 value nearest -139 / alpha
+        glo = float(torch.tensor(-139.0 / float(alpha)).bfloat16().float())
+        assert devlib.run_oai_clamped(_p(gt), _p(ut), _p(out), n, C.c_float(alpha), C.c_float(beta),
+                                      C.c_float(limit), C.c_float(glo)) == 0
+    else:
+        assert devlib.run_oai(_p(gt), _p(ut), _p(out), n, C.c_float(alpha), C.c_float(beta), C.c_float(limit)) == 0
     got = out.cpu().numpy().astype(np.float64)
     gc = np.minimum(g.astype(np.float64), limit)
     uc = np.clip(u.astype(np.float64), -limit, limit)
-    want = gc / (1.0 + np.exp(-float(alpha) * gc)) * (uc + beta)
+    with np.errstate(over="ignore"):            # exp overflows to inf far below zero: want = 0 there
+        want = gc / (1.0 + np.exp(-float(alpha) * gc)) * (uc + beta)
     ok = np.abs(want) > 2.0 ** -100
     rel = np.abs(got - want)[ok] / np.abs(want)[ok]
     assert rel.max() <= 2.0 ** -21, rel.max()
+    assert np.abs(got[~ok]).max(initial=0) <= 2.0 ** -100
     assert got[0] > 0.2265625          # exact value 0.22656257..., the boundary is 29/128
 
 

@@ -165,6 +165,22 @@ def test_oai_parameters_and_unclamped_limit():
     run_swiglu("mxfp8", "swiglu_oai", gu, from_fp32=True, alpha=2.0 ** 90, limit=2.0 ** 14)
 
 
+@pytest.mark.parametrize("fmt", ["mxfp8", "block128", "per_token"])
+def test_oai_large_negative_gates(fmt):
+    # whole blocks of gates far below zero (the sigmoid leaves the normal
+    # range, or underflows to zero) beside ordinary blocks
+    M, I = 8, 1024
+    rng = np.random.default_rng(12)
+    g = rng.standard_normal((M, I)) * 4.0
+    u = rng.uniform(-10, 10, (M, I))
+    for r in range(M):
+        for blk in range(r % 3, I // 128, 3):
+            g[r, blk * 128:(blk + 1) * 128] = -rng.uniform(30.0, 300.0, 128)
+    gu = torch.from_numpy(np.concatenate([g, u], axis=1)).to(torch.bfloat16)
+    run_swiglu(fmt, "swiglu_oai", gu, from_fp32=True)
+    run_swiglu(fmt, "swiglu_oai", gu, from_fp32=False)
+
+
 # ------------------------------------------------------------ edge rows
 
 def _bf16(a):
