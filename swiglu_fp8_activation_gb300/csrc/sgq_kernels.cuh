@@ -435,7 +435,7 @@ __host__ __device__ constexpr int swiglu_stage_bytes(int nv, int threads) { retu
 // CLAMP16 (OAI only, see activation8): the limit is a bf16 value and the
 // clamps of g and u run on the packed bf16 pairs before widening.
 template <int FMT, int LAYOUT, int NV, int ACT, bool FULL, bool CLAMP16>
-__global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs a) {
+__device__ __forceinline__ void swiglu_rows(const SwigluArgs& a) {
     extern __shared__ uint4 stage[];
     __shared__ float part_amax[32];
     const int tpr = a.tpr;
@@ -543,6 +543,20 @@ __global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs 
     } else {
         by_mode(std::false_type{});
     }
+}
+
+template <int FMT, int LAYOUT, int NV, int ACT, bool FULL, bool CLAMP16>
+__global__ void __launch_bounds__(kMaxTPR) swiglu_quant_kernel(const SwigluArgs a) {
+    swiglu_rows<FMT, LAYOUT, NV, ACT, FULL, CLAMP16>(a);
+}
+
+// The same with at most 56 registers a thread, which lets three 384-thread
+// CTAs share an SM: SiLU-and-mul + 1x128 at I = 12288 measured 11% faster.
+// (The OAI kernels measured no better capped inside the prefill step, and
+// the per-token kernels keep the whole row in registers.)
+template <int FMT, int LAYOUT, int NV, int ACT, bool FULL, bool CLAMP16>
+__global__ void __maxnreg__(56) swiglu_quant_kernel_r56(const SwigluArgs a) {
+    swiglu_rows<FMT, LAYOUT, NV, ACT, FULL, CLAMP16>(a);
 }
 
 // Bytes of dynamic shared memory the standalone quant kernel stages its loads in.

@@ -13,13 +13,22 @@ template <int ACT, bool CLAMP16>
 struct SwigluPick {
     using Kernel = void (*)(const SwigluArgs);
 
+    // SiLU-and-mul in the MX and 1x128 formats takes the register-capped kernels.
+    template <int FMT, int LAYOUT, int NV, bool FULL>
+    static Kernel kernel() {
+        if constexpr (ACT == ACT_SILU && FMT != FMT_PT)
+            return swiglu_quant_kernel_r56<FMT, LAYOUT, NV, ACT, FULL, CLAMP16>;
+        else
+            return swiglu_quant_kernel<FMT, LAYOUT, NV, ACT, FULL, CLAMP16>;
+    }
+
     template <int FMT, int LAYOUT, bool FULL>
     static Kernel pick(int nv) {
         switch (nv) {
-            case 1: return swiglu_quant_kernel<FMT, LAYOUT, 1, ACT, FULL, CLAMP16>;
-            case 2: return swiglu_quant_kernel<FMT, LAYOUT, 2, ACT, FULL, CLAMP16>;
-            case 3: return swiglu_quant_kernel<FMT, LAYOUT, 3, ACT, FULL, CLAMP16>;
-            default: return swiglu_quant_kernel<FMT, LAYOUT, 4, ACT, FULL, CLAMP16>;
+            case 1: return kernel<FMT, LAYOUT, 1, FULL>();
+            case 2: return kernel<FMT, LAYOUT, 2, FULL>();
+            case 3: return kernel<FMT, LAYOUT, 3, FULL>();
+            default: return kernel<FMT, LAYOUT, 4, FULL>();
         }
     }
 
