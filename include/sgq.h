@@ -29,8 +29,11 @@
  *        34502): "Change" (per-token FP8, [m, 1] scale).
  *
  * Conventions shared by all entry points
- *   - All pointers are DEVICE pointers owned by the caller. The library
- *     allocates nothing, keeps no state between calls, never synchronises and
+ *   - All tensor pointers are DEVICE pointers owned by the caller (the dual
+ *     norm's two segment descriptors are host structs, read during the call
+ *     only). The library
+ *     allocates nothing, keeps no state between calls (but the calling
+ *     thread's last launch error, see sgq_launch_error), never synchronises and
  *     launches nothing but its one kernel, so calls may be captured into CUDA
  *     graphs.
  *   - All tensors are contiguous and row-major (the dual norm's inputs may

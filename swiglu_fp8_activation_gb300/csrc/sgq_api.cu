@@ -1,6 +1,7 @@
 // sgq_api.cu -- the C ABI declared in include/sgq.h: host-side argument
 // checks, launch planning and one kernel launch per call. Nothing here
-// allocates, synchronises or keeps state between calls.
+// allocates or synchronises; the only state kept between calls is the
+// calling thread's last launch error, for sgq_launch_error().
 #include <math.h>
 #include <stdint.h>
 #include <string.h>

@@ -1,8 +1,8 @@
 // sgq_device.cuh -- device code of the fused norm / SwiGLU + FP8 quantisation
 // kernels for sm_103a.
 //
-// One "row engine" serves both operations. A row of W elements is split into
-// 16-byte chunks of 8 bf16 values; `tpr` threads (a multiple of 32) own one
+// One "row engine" serves every operation. A row of W elements is split into
+// 16-byte chunks of 8 16-bit values; `tpr` threads (a multiple of 32) own one
 // row, and thread t owns chunks t, t + tpr, ..., t + (NV-1)*tpr, so every
 // warp-wide copy is 512 contiguous bytes. All NV chunks of a thread are copied
 // asynchronously into its own shared-memory slots before any arithmetic (one
@@ -17,8 +17,9 @@
 // of the group size: chunk c lives in lane c % 32 of its warp, so a 32-block
 // (4 chunks) or a 128-block (16 chunks) never straddles a lane group.
 //
-// Numeric formats: bf16 = upper half of IEEE binary32; E4M3 = OCP "e4m3fn";
-// E8M0 = OCP MX scale byte, value 2^(code-127). The operations follow
+// Numeric formats: bf16 = upper half of IEEE binary32; fp16 = IEEE binary16;
+// E4M3 = OCP "e4m3fn"; E8M0 = OCP MX scale byte, value 2^(code-127). The
+// operations follow
 // "[ROCm][MiniMax-M3.1] Fuse MXFP8 quant into the add+RMSNorm and SwiGLU
 // epilogues" (vllm PR 65478, "Purpose"), "[Perf] [AMD] qwen3: Fuse the 1x128
 // FP8 input quant into RMSNorm and SiLU-and-mul" (sglang PR 48043,

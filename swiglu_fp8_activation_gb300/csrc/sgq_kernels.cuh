@@ -1,6 +1,7 @@
-// sgq_kernels.cuh -- the two row-engine kernels (add + RMSNorm, SwiGLU), each
-// fused with FP8 quantisation in one of three formats. See sgq_device.cuh for
-// the thread-to-data mapping.
+// sgq_kernels.cuh -- the row-engine kernels: add + RMSNorm (one row set, or
+// two in one launch) and SwiGLU, each fused with FP8 quantisation in one of
+// three formats, and the standalone quantisation of the unfused chains. See
+// sgq_device.cuh for the thread-to-data mapping.
 #pragma once
 
 #include <type_traits>
