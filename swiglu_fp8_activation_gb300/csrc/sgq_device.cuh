@@ -239,6 +239,7 @@ __device__ __forceinline__ float rcp_approx(float x) {
 constexpr float kLog2eHi = 1.44269502162933349609375f;   // 0x3FB8AA3B
 constexpr float kLog2eLo = 1.925963033500011e-08f;       // log2(e) - kLog2eHi
 constexpr float kLn2 = 0.693147180559945309f;        // ln 2, rounded to fp32
+constexpr float kInv448 = 0x1.24924ap-9f;             // 1/448 rounded to nearest fp32 (the FP8 scale divisor)
 
 __device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
 

@@ -108,6 +108,12 @@ __device__ __forceinline__ char* scale_addr(const ScaleRow& r, int g) {
     return r.base + g * (FMT == FMT_MX ? 1 : 4);
 }
 
+// The FP8 scale amax / 448, correctly rounded: the Markstein quotient with
+// RN(1/448) where the quotient is normal, IEEE division below.
+__device__ __forceinline__ float fp8_scale(float amax) {
+    return amax >= 0x1p-100f ? div_rn(amax, 448.0f, kInv448) : __fdiv_rn(amax, 448.0f);
+}
+
 // Quantise one chunk (8 source values of row `row`, chunk index c) and store
 // its 8 E4M3 codes and, from the first chunk of its group, the scale. Every
 // lane of the warp must call it for MX and 1x128 (the group amax is a lane
@@ -149,7 +155,7 @@ __device__ __forceinline__ void quantize_chunk(const float (&src)[8], int64_t ro
     } else {
         float s = pt_s, r = pt_r;
         if (FMT == FMT_B128) {
-            s = __fdiv_rn(m, 448.0f);
+            s = fp8_scale(m);
             r = s >= 0x1p-126f ? __frcp_rn(s) : 0.0f;   // once per group
         }
         if (s >= 0x1p-126f || s == 0.0f) {              // r = 0 for s = 0: every code is 0
@@ -177,7 +183,7 @@ __device__ __forceinline__ void quantize_chunk(const float (&src)[8], int64_t ro
 
 // Per-token scale and its reciprocal from the row amax (one per row).
 __device__ __forceinline__ float2 per_token_scale(float row_amax) {
-    const float s = __fdiv_rn(row_amax, 448.0f);
+    const float s = fp8_scale(row_amax);
     return make_float2(s, s >= 0x1p-126f ? __frcp_rn(s) : 0.0f);
 }
 

@@ -107,7 +107,12 @@ def test_div_rn_and_packed_form_match_ieee_division(devlib):
     # unrelated random pairs
     a2 = (rng.standard_normal(n) * 2.0 ** rng.integers(-60, 60, n)).astype(np.float32)
     b2 = (np.abs(rng.standard_normal(n)) * 2.0 ** rng.integers(-60, 60, n) + 2.0 ** -100).astype(np.float32)
-    for aa, bb in ((a, b), (a2, b2)):
+    # the FP8 scale itself: amax / 448 for amax >= 2^-100 (bf16 values and
+    # arbitrary fp32 values), where the kernels use RN(1/448) = __frcp_rn(448)
+    a3 = np.abs(rng.standard_normal(n) * 2.0 ** rng.integers(-100, 120, n)).astype(np.float32) + np.float32(2.0 ** -100)
+    a3[: n // 2] = torch.from_numpy(a3[: n // 2]).bfloat16().float().numpy()
+    b3 = np.full(n, 448.0, np.float32)
+    for aa, bb in ((a, b), (a2, b2), (a3, b3)):
         at, bt = torch.from_numpy(aa).cuda(), torch.from_numpy(bb).cuda()
         qf, qp, qi = torch.empty_like(at), torch.empty_like(at), torch.empty_like(at)
         assert devlib.run_div(_p(at), _p(bt), _p(qf), _p(qp), _p(qi), n) == 0
