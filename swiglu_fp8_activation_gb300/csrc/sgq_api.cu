@@ -50,6 +50,7 @@ bool plan_rows(int64_t M, int W, int sm_count, Plan* p) {
     p->rpc = rpc;
     p->grid = (M + rpc - 1) / rpc;
     p->full = nchunks == tpr * nv && M % rpc == 0;
+    p->sms = sm_count;
     return p->grid <= 0x7FFFFFFF;
 }
 
@@ -309,6 +310,7 @@ bool plan_dual(int64_t M, int Ha, int Hb, int sms, sgq::Plan* p, int tpr[2], int
         p->rpc = 1;
         p->grid = *grid0 + (M + rpc[1] - 1) / rpc[1];
         p->full = false;
+        p->sms = sms;
         return p->grid <= 0x7FFFFFFF;
     }
     return false;

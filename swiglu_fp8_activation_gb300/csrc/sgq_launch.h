@@ -16,6 +16,7 @@ struct Plan {
     int rpc;
     int64_t grid;
     bool full;   // W/8 == tpr * nv and M % rpc == 0: no bounds checks needed
+    int sms;     // multiprocessors of the device (0 if unknown)
 };
 
 // Pick a plan for M rows of width W (W % 8 == 0). Returns false when W needs
