@@ -106,9 +106,12 @@ def test_swiglu_bf16_matches_oracle(act, round_bf16, M, I):
 
 @pytest.mark.parametrize("fmt", ["mxfp8", "block128", "per_token"])
 @pytest.mark.parametrize("M", [1, 37, 512])
-def test_norm_then_quant_equals_fused_bitwise(fmt, M):
-    H = 6144 if fmt != "per_token" else 7168
+@pytest.mark.parametrize("H", [2048, 6144])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_norm_then_quant_equals_fused_bitwise(fmt, M, H, dtype):
+    # [P1] review: the bitwise test covers bf16 / fp16 and N in {2048, 6144}
     t = inputs.norm_inputs(M, H, seed=7 + M, x_std=3.0, r_std=1.0, w_mean=0.0, w_std=0.1)
+    t = {k: v.float().to(dtype) for k, v in t.items()}
     xd, rd, wd = t["x"].to(DEV), t["r"].to(DEV), t["w"].to(DEV)
     q_f, s_f, n_f, r_f = rmsnorm_add_quant(xd, wd, fmt=fmt, residual_in=rd, residual_out=torch.empty_like(rd),
                                            gemma=True, quant_from_fp32=False, normed=True)
@@ -121,7 +124,7 @@ def test_norm_then_quant_equals_fused_bitwise(fmt, M):
 
 @pytest.mark.parametrize("fmt,act,round_bf16", [("block128", "silu_mul", True), ("mxfp8", "swiglu_oai", False),
                                                 ("per_token", "silu_mul", False)])
-@pytest.mark.parametrize("M", [1, 37, 256])
+@pytest.mark.parametrize("M", [1, 37, 256, 512])
 def test_activation_then_quant_equals_fused_bitwise(fmt, act, round_bf16, M):
     I = 12288 if fmt == "block128" else 3072
     gu = inputs.swiglu_inputs(M, I, seed=11 + M, std=2.0).to(DEV)
