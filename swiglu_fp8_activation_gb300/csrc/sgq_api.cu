@@ -260,15 +260,9 @@ int swiglu_call(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float al
     a.limit = limit;
     // The OAI clamps run on packed bf16 when the limit is a bf16 value and
     // alpha * limit stays in the range where the sigmoid needs no upper clamp.
-    // The lower gate bound is then the bf16 value nearest -139 / alpha, which
-    // alpha maps into [-174, -104] (bf16 spacing is 2^-8 relative).
     const uint32_t lb = bf16_bits_rn(limit);
-    const uint32_t gb = alpha > 0.0f ? bf16_bits_rn(-139.0f / alpha) : 0u;
-    const float zlo = alpha * bf16_value(gb);
     const bool clamp16 = act == SGQ_ACT_SWIGLU_OAI && alpha > 0.0f && isfinite(limit) &&
-                         alpha * limit <= 0x1p100f && bf16_value(lb) == limit && isfinite(-139.0f / alpha) &&
-                         zlo >= -174.0f && zlo <= -104.0f;
-    a.glo2 = gb | (gb << 16);
+                         alpha * limit <= 0x1p100f && bf16_value(lb) == limit;
     // -alpha log2(e) in two fp32 parts (head rounded, then the rest)
     const double k = -(double)alpha * 1.4426950408889634074;
     a.khi = (float)k;

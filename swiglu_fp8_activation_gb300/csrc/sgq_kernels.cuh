@@ -57,7 +57,6 @@ struct SwigluArgs {
     int act;
     float alpha, beta, limit;
     uint32_t lim2, nlim2;    // bf16x2 of limit and -limit (the CLAMP16 kernels)
-    uint32_t glo2;           // bf16x2 of the CLAMP16 kernels' lower gate bound
     float khi, klo;          // -alpha log2(e) in two fp32 parts (OAI)
 };
 
@@ -364,12 +363,12 @@ __global__ void __launch_bounds__(kMaxTPR) norm_dual_kernel(const DualArgs d) {
 //         khi + klo = -alpha log2(e) (two fp32 parts from the host);
 //   SiLU: a = (g * sigmoid(g)) * u, the first factor rounded to bf16 when
 //         ROUND is set.
-// CLAMPED (OAI only): g arrives as max(min(g, limit), glo') and u as u', with
-// alpha > 0, alpha * limit <= 2^100 and glo' a bound where alpha * glo' lies
-// in [-174, -104]: below -104 the sigmoid is 0 in fp32, so g' * sigmoid(alpha
-// g') is a signed zero for every g' <= glo' and the lower clamp changes
-// nothing; above, sigmoid8 is exact for any argument down to -174 and up to
-// 2^120. The clamped gate then serves both the sigmoid and the product.
+// CLAMPED (OAI only): g and u arrive already clamped to limit (g' and u'),
+// and alpha > 0 with alpha * limit <= 2^100, so g' bounds the sigmoid's
+// argument from above (sigmoid8 is exact there for any argument below
+// 2^120) and only the lower clamp remains. (Clamping g from below on the
+// packed bf16 words as well measured 8-17% slower at decode sizes: the
+// second dependent bf16x2 min/max lengthens the critical path.)
 template <int ACT, bool CLAMPED = false, bool ROUND = false>
 __device__ __forceinline__ void activation8(const float (&g)[8], const float (&u)[8], float khi, float klo,
                                             float beta, float limit, float glo, float ghi, float (&a)[8]) {
@@ -379,7 +378,7 @@ __device__ __forceinline__ void activation8(const float (&g)[8], const float (&u
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             gc[k] = CLAMPED ? g[k] : fminf(g[k], limit);
-            gs[k] = CLAMPED ? g[k] : fmaxf(fminf(gc[k], ghi), glo);
+            gs[k] = CLAMPED ? fmaxf(gc[k], glo) : fmaxf(fminf(gc[k], ghi), glo);
         }
         sigmoid8(gs, khi, klo, sg);                                     // sigmoid(alpha * gs)
 #pragma unroll
@@ -415,15 +414,15 @@ __device__ __forceinline__ float2 oai_gate_range(float alpha) {
 }
 
 // One chunk of gate and up from their shared-memory slots, widened to fp32;
-// with CLAMP16, g = max(min(g, limit), glo') and u = clamp(u, -limit, limit)
-// first, on the packed bf16 pairs (exact: the bounds are bf16 values).
+// with CLAMP16, g = min(g, limit) and u = clamp(u, -limit, limit) first, on
+// the packed bf16 pairs (exact: limit is a bf16 value).
 template <bool CLAMP16>
 __device__ __forceinline__ void load_gate_up(const uint4* gs, const uint4* us, const SwigluArgs& a, float (&g)[8],
                                              float (&u)[8]) {
     uint4 gw = ld_smem16(gs), uw = ld_smem16(us);
     if (CLAMP16) {
-        gw = make_uint4(bf16x2_max(bf16x2_min(gw.x, a.lim2), a.glo2), bf16x2_max(bf16x2_min(gw.y, a.lim2), a.glo2),
-                        bf16x2_max(bf16x2_min(gw.z, a.lim2), a.glo2), bf16x2_max(bf16x2_min(gw.w, a.lim2), a.glo2));
+        gw = make_uint4(bf16x2_min(gw.x, a.lim2), bf16x2_min(gw.y, a.lim2), bf16x2_min(gw.z, a.lim2),
+                        bf16x2_min(gw.w, a.lim2));
         uw = make_uint4(bf16x2_max(bf16x2_min(uw.x, a.lim2), a.nlim2), bf16x2_max(bf16x2_min(uw.y, a.lim2), a.nlim2),
                         bf16x2_max(bf16x2_min(uw.z, a.lim2), a.nlim2), bf16x2_max(bf16x2_min(uw.w, a.lim2), a.nlim2));
     }

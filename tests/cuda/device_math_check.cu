@@ -37,7 +37,8 @@ __global__ void oai_kernel(const float* g, const float* u, float* out, int n, fl
 }
 
 // The same through the pre-clamped form the packed-bf16 kernels use: g
-// clamped to [glo_clamp, limit] and u to limit first, then
+// clamped to [glo_clamp, limit] and u to limit first (glo_clamp below the
+// activation's own lower bound changes nothing), then
 // activation8<ACT_OAI, true>.
 __global__ void oai_clamped_kernel(const float* g, const float* u, float* out, int n, float alpha, float beta,
                                    float limit, float glo_clamp) {
