@@ -16,6 +16,11 @@
  *   swiglu             SwiGLU to bf16
  *   quantize_fp8       FP8 quantisation of bf16 rows
  *
+ * and a two-segment norm, one launch for two row sets over the same rows:
+ *
+ *   rmsnorm_dual_quant the q and kv latent norms of multi-head latent
+ *                      attention (each segment quantised and/or copied)
+ *
  * The operations follow these pages:
  *   [P1] "[ROCm][MiniMax-M3.1] Fuse MXFP8 quant into the add+RMSNorm and
  *        SwiGLU epilogues" (vllm PR 65478): "Purpose" (the two fusions),
@@ -26,16 +31,16 @@
  *        and SiLU-and-mul" (sglang PR 48043): "Modifications" (1x128 group
  *        FP8; SiLU-and-mul rounded like the unfused op; bf16 inputs only).
  *   [P4] "[ROCm] Fuse per-token activation quant into RMSNorm" (sglang PR
- *        34502): "Change" (per-token FP8, [m, 1] scale).
+ *        34502): "Change" (per-token FP8, [m, 1] scale; fp16 activations
+ *        stay fp16; the q/kv norm), "Motivation" (the standalone quant).
  *
  * Conventions shared by all entry points
  *   - All tensor pointers are DEVICE pointers owned by the caller (the dual
  *     norm's two segment descriptors are host structs, read during the call
- *     only). The library
- *     allocates nothing, keeps no state between calls (but the calling
- *     thread's last launch error, see sgq_launch_error), never synchronises and
- *     launches nothing but its one kernel, so calls may be captured into CUDA
- *     graphs.
+ *     only). The library allocates nothing, keeps no state between calls
+ *     (but the calling thread's last launch error, see sgq_launch_error),
+ *     never synchronises and launches nothing but its one kernel, so calls
+ *     may be captured into CUDA graphs.
  *   - All tensors are contiguous and row-major (the dual norm's inputs may
  *     have a row stride). 16-bit activations are bfloat16, or IEEE fp16 with
  *     SGQ_F_FP16 where an entry point accepts it. Quantised values are OCP
@@ -46,7 +51,8 @@
  *   - Alignment: every tensor pointer must be 16-byte aligned, except a
  *     float32 scale pointer (4 bytes) and an E8M0 scale pointer (1 byte).
  *   - Width rules: MXFP8 needs W % 32 == 0, 1x128 needs W % 128 == 0,
- *     per-token needs W % 8 == 0; W <= SGQ_MAX_WIDTH.
+ *     per-token (and the unquantised outputs of rmsnorm_add, swiglu and an
+ *     unquantised dual segment) needs W % 8 == 0; W <= SGQ_MAX_WIDTH.
  *   - Outputs may not overlap inputs or each other, except that residual_out
  *     may equal residual_in exactly (in-place update).
  *   - M == 0 returns SGQ_OK without a launch (pointers are not inspected).
