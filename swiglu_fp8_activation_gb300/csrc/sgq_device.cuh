@@ -354,38 +354,35 @@ __device__ __forceinline__ float group_max(float v) {
     return v;
 }
 
-// Sum (or max) over the `tpr` threads of one row. `part` holds one slot per
-// warp of the CTA; warps of a row are contiguous. Every thread of the CTA must
-// call it (it contains __syncthreads). The row's warp partials are combined in
-// warp order, so every thread of a row gets the same value.
+// Sum (or max, of values >= 0) over the `tpr` threads of one row. `part`
+// holds one slot per warp of the CTA; warps of a row are contiguous. Every
+// thread of the CTA must call it (it contains __syncthreads). Each warp of
+// the row then reads the row's warp partials one per lane (at most 16, the
+// rest 0) and combines them with the same xor butterfly, whose every step adds
+// the same two operands in every lane: every thread of a row gets the
+// bit-identical value, with no loop.
 template <bool IS_MAX>
 __device__ __forceinline__ float row_reduce(float v, float* part, int tpr, int lrow) {
     v = IS_MAX ? warp_max(v) : warp_sum(v);
-    const int warp = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) part[warp] = v;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) part[warp] = v;
     __syncthreads();
-    const int w0 = lrow * (tpr >> 5), nw = tpr >> 5;
-    float r = part[w0];
-    for (int i = 1; i < nw; ++i) r = IS_MAX ? fmaxf(r, part[w0 + i]) : r + part[w0 + i];
-    return r;
+    const int nw = tpr >> 5;
+    const float r = lane < nw ? part[lrow * nw + lane] : 0.0f;
+    return IS_MAX ? warp_max(r) : warp_sum(r);
 }
 
-// Sum of `a` and max of `b` over the `tpr` threads of one row, in one
-// shared-memory round (one __syncthreads); same rules as row_reduce.
+// Sum of `a` and max of `b` (b >= 0) over the `tpr` threads of one row, in
+// one shared-memory round (one __syncthreads); same rules as row_reduce.
 __device__ __forceinline__ float2 row_reduce_sum_max(float a, float b, float2* part, int tpr, int lrow) {
     a = warp_sum(a);
     b = warp_max(b);
-    const int warp = threadIdx.x >> 5;
-    if ((threadIdx.x & 31) == 0) part[warp] = make_float2(a, b);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) part[warp] = make_float2(a, b);
     __syncthreads();
-    const int w0 = lrow * (tpr >> 5), nw = tpr >> 5;
-    float2 r = part[w0];
-    for (int i = 1; i < nw; ++i) {
-        const float2 q = part[w0 + i];
-        r.x += q.x;
-        r.y = fmaxf(r.y, q.y);
-    }
-    return r;
+    const int nw = tpr >> 5;
+    const float2 r = lane < nw ? part[lrow * nw + lane] : make_float2(0.0f, 0.0f);
+    return make_float2(warp_sum(r.x), warp_max(r.y));
 }
 
 // ------------------------------------------------------------------ scales
