@@ -10,7 +10,8 @@
 * div_rn() and div2_rn() (one reciprocal per group + Markstein's FMA
   correction) against CUDA's correctly rounded __fdiv_rn, bit for bit, for
   the FP8 quotients the kernels form (|a| <= b * 448 * (1 + 2^-20), b
-  normal) and for random pairs.
+  normal), the FP8 scale amax / 448, quotients by integer widths and random
+  pairs.
 """
 import ctypes as C
 import os
@@ -112,7 +113,10 @@ def test_div_rn_and_packed_form_match_ieee_division(devlib):
     a3 = np.abs(rng.standard_normal(n) * 2.0 ** rng.integers(-100, 120, n)).astype(np.float32) + np.float32(2.0 ** -100)
     a3[: n // 2] = torch.from_numpy(a3[: n // 2]).bfloat16().float().numpy()
     b3 = np.full(n, 448.0, np.float32)
-    for aa, bb in ((a, b), (a2, b2), (a3, b3)):
+    # quotients by integer widths (multiples of 8 up to the maximum width)
+    a4 = np.abs(rng.standard_normal(n) * 2.0 ** rng.integers(-90, 100, n)).astype(np.float32) + np.float32(2.0 ** -100)
+    b4 = (8 * rng.integers(1, 2049, n)).astype(np.float32)
+    for aa, bb in ((a, b), (a2, b2), (a3, b3), (a4, b4)):
         at, bt = torch.from_numpy(aa).cuda(), torch.from_numpy(bb).cuda()
         qf, qp, qi = torch.empty_like(at), torch.empty_like(at), torch.empty_like(at)
         assert devlib.run_div(_p(at), _p(bt), _p(qf), _p(qp), _p(qi), n) == 0
