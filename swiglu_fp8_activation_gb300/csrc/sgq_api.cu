@@ -215,6 +215,21 @@ int norm_call(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, const vo
     return launched(sgq::launch_norm(fmt, dt_of(flags), plan, a, static_cast<cudaStream_t>(stream)));
 }
 
+// Column segments a row for a SwiGLU launch over `rows` rows (the grid's
+// second dimension): while twice the CTAs still fit on the device at one a
+// multiprocessor, a row is split in two, up to 8 segments, each a whole
+// number of scale groups and at least 1024 columns. At small M this spreads
+// a wide row's activation arithmetic (two special-function operations an
+// element) over 8 multiprocessors instead of one. The per-token format needs
+// the row's amax and is never split.
+int swiglu_segments(int fmt, int64_t rows, int64_t I, int sms) {
+    if (fmt == SGQ_FMT_FP8_PER_TOKEN || sms <= 0) return 1;
+    const int64_t nch = I / 8, gch = fmt == SGQ_FMT_FP8_BLOCK128 ? 16 : 4;   // chunks a row, a scale group
+    int s = 1;
+    while (s < 8 && rows * 2 * s <= sms && nch % (2 * s * gch) == 0 && nch / (2 * s) >= 128) s *= 2;
+    return s;
+}
+
 // The SwiGLU launch behind swiglu_quant (q_out set) and swiglu (out set:
 // the bf16 activation, no quantisation).
 int swiglu_call(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float alpha, float beta, float limit,
@@ -241,8 +256,13 @@ int swiglu_call(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float al
                           {out, (size_t)M * I * 2}};
     if (any_overlap(spans, 4)) return SGQ_ERR_INVALID_ARG;
 
+    // Rows too few to fill the device are split into column segments.
+    const int sms = sm_count();
+    const int seg = swiglu_segments(fmt, so.Ms, I, sms);
     sgq::Plan plan;
-    if (!plan_launch(M, (int)I, so, &plan)) return SGQ_ERR_UNSUPPORTED;
+    if (!sgq::plan_rows(so.Ms, (int)(I / seg), sms, &plan)) return SGQ_ERR_UNSUPPORTED;
+    plan.full = plan.full && so.Ms == M && seg == 1;   // the exact-fit kernels run whole rows
+    plan.seg = seg;
     sgq::SwigluArgs a;
     a.gu = static_cast<const uint16_t*>(gate_up);
     a.q = static_cast<uint8_t*>(q_out);
@@ -251,6 +271,7 @@ int swiglu_call(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float al
     a.out = static_cast<uint16_t*>(out);
     a.M = M;
     a.I = (int)I;
+    a.segc = (int)(I / 8 / seg);
     a.tpr = plan.tpr;
     a.rpc = plan.rpc;
     a.flags = flags;

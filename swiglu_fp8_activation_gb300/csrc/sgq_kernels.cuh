@@ -58,6 +58,7 @@ struct SwigluArgs {
     float alpha, beta, limit;
     uint32_t lim2, nlim2;    // bf16x2 of limit and -limit (the CLAMP16 kernels)
     float khi, klo;          // -alpha log2(e) in two fp32 parts (OAI)
+    int segc;                // chunks a column segment (I / 8 / gridDim.y)
 };
 
 struct QuantArgs {
@@ -440,6 +441,10 @@ __host__ __device__ constexpr int swiglu_stage_bytes(int nv, int threads) { retu
 // processed as soon as its own group has landed.
 // CLAMP16 (OAI only, see activation8): the limit is a bf16 value and the
 // clamps of g and u run on the packed bf16 pairs before widening.
+// Column segments: the bounds-checked kernels may run each row as gridDim.y
+// CTAs, CTA y taking chunks [y * segc, (y + 1) * segc), a whole number of
+// scale groups (the MX and 1x128 formats have nothing row-wide). Chunk
+// indices stay the row's own, so every address and scale index is unchanged.
 template <int FMT, int LAYOUT, int NV, int ACT, bool FULL, bool CLAMP16>
 __device__ __forceinline__ void swiglu_rows(const SwigluArgs& a) {
     extern __shared__ uint4 stage[];
@@ -452,12 +457,14 @@ __device__ __forceinline__ void swiglu_rows(const SwigluArgs& a) {
     const bool row_ok = FULL || row < a.M;
     const int I = a.I, nchunks = I >> 3;
     const uint16_t* grow = a.gu + row * (int64_t)(2 * I);
+    const int cb = FULL ? 0 : (int)blockIdx.y * a.segc;               // the segment's first chunk
+    const int cend = FULL ? nchunks : cb + a.segc;
 
     pdl_wait();
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
-        const int c = t + v * tpr;
-        const bool ok = FULL || (row_ok && c < nchunks);   // else zero-fill, reading nothing
+        const int c = cb + t + v * tpr;
+        const bool ok = FULL || (row_ok && c < cend);      // else zero-fill, reading nothing
         cp_async16(&stage[(2 * v) * nt + threadIdx.x], ok ? (const void*)(grow + (int64_t)c * 8) : (const void*)a.gu,
                    ok ? 16 : 0);
         cp_async16(&stage[(2 * v + 1) * nt + threadIdx.x],
@@ -479,8 +486,8 @@ __device__ __forceinline__ void swiglu_rows(const SwigluArgs& a) {
         if (FMT != FMT_PT) {           // MX and 1x128: chunk by chunk, as each lands
 #pragma unroll
             for (int v = 0; v < NV; ++v) {
-                const int c = t + v * tpr;
-                const bool ok = FULL || (row_ok && c < nchunks);
+                const int c = cb + t + v * tpr;
+                const bool ok = FULL || (row_ok && c < cend);
                 float g[8], u[8], src[8];
                 cp_async_wait_group_of<NV>(v);
                 load_gate_up<CLAMP16>(&stage[(2 * v) * nt + threadIdx.x], &stage[(2 * v + 1) * nt + threadIdx.x], a,
@@ -498,7 +505,7 @@ __device__ __forceinline__ void swiglu_rows(const SwigluArgs& a) {
                         }
                     }
                     // chunks past the row end loaded zeros, and every activation of 0 and 0 is 0
-                    quantize_chunk<FMT, LAYOUT>(src, row, c, ok, FULL || (srow_ok && c < nchunks), I, a.q, sr);
+                    quantize_chunk<FMT, LAYOUT>(src, row, c, ok, FULL || (srow_ok && c < cend), I, a.q, sr);
                 }
             }
         } else {                       // per-token: the whole row, then its amax
@@ -524,17 +531,17 @@ __device__ __forceinline__ void swiglu_rows(const SwigluArgs& a) {
             if (MODE == 0) {           // (the bf16-out launches use the MX kernels; kept complete here)
 #pragma unroll
                 for (int v = 0; v < NV; ++v) {
-                    const int c = t + v * tpr;
-                    st16_if(a.out + row * I + (int64_t)c * 8, f32x8_to_bf16x8(src[v]), FULL || (row_ok && c < nchunks));
+                    const int c = cb + t + v * tpr;
+                    st16_if(a.out + row * I + (int64_t)c * 8, f32x8_to_bf16x8(src[v]), FULL || (row_ok && c < cend));
                 }
                 return;
             }
             const float2 pt = per_token_scale(row_reduce<true>(m, part_amax, tpr, lrow));
 #pragma unroll
             for (int v = 0; v < NV; ++v) {
-                const int c = t + v * tpr;
-                quantize_chunk<FMT, LAYOUT>(src[v], row, c, FULL || (row_ok && c < nchunks),
-                                            FULL || (srow_ok && c < nchunks), I, a.q, sr, pt.x, pt.y);
+                const int c = cb + t + v * tpr;
+                quantize_chunk<FMT, LAYOUT>(src[v], row, c, FULL || (row_ok && c < cend),
+                                            FULL || (srow_ok && c < cend), I, a.q, sr, pt.x, pt.y);
             }
         }
     };

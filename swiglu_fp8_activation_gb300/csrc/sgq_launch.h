@@ -9,7 +9,8 @@
 namespace sgq {
 
 // Launch geometry of one call: `nv` chunks per thread, `tpr` threads per row,
-// `rpc` rows per CTA, `grid` CTAs.
+// `rpc` rows per CTA, `grid` CTAs (times `seg` column segments a row, the
+// grid's second dimension, for the SwiGLU launches that split rows).
 struct Plan {
     int nv;
     int tpr;
@@ -17,6 +18,7 @@ struct Plan {
     int64_t grid;
     bool full;   // W/8 == tpr * nv and M % rpc == 0: no bounds checks needed
     int sms;     // multiprocessors of the device (0 if unknown)
+    int seg = 1;
 };
 
 // Pick a plan for M rows of width W (W % 8 == 0). Returns false when W needs
@@ -36,7 +38,7 @@ cudaError_t launch_pdl(void (*k)(const Args), const Plan& p, const Args& a, cuda
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.gridDim = dim3((unsigned)p.grid, (unsigned)p.seg);
     cfg.blockDim = dim3((unsigned)(p.rpc * p.tpr));
     cfg.dynamicSmemBytes = (size_t)dynamic_smem;
     cfg.stream = stream;

@@ -1,0 +1,126 @@
+"""GPU parity of the SwiGLU launches that split rows into column segments.
+
+At small M the library runs each row of a wide SwiGLU as up to 8 CTAs, each
+taking a whole number of scale groups (MXFP8 and 1x128 only; the per-token
+format needs the row's amax). The cases below are chosen so that the launch
+is segmented on the device under test (checked against the host's rule),
+including segments that do not fill their CTA's threads, layouts that pad
+rows, SiLU's bf16 roundings and the bf16 output of the unfused chain. Each
+result must match the oracle under the usual tolerances, equal bit for bit
+the same rows computed inside a batch large enough to run unsegmented, and
+leave the bytes around its outputs untouched.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle.parity import check_bf16, check_swiglu
+from swiglu_fp8_activation_gb300 import inputs, scale_shape, swiglu, swiglu_quant
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+GUARD = 4096
+BIG_M = 256                      # enough rows that no launch splits them
+
+
+def _sms():
+    return torch.cuda.get_device_properties(DEV).multi_processor_count
+
+
+def _segments(fmt, rows, I, sms):
+    """The host's choice of column segments a row (the C library's rule)."""
+    if fmt == "per_token":
+        return 1
+    nch, gch = I // 8, (16 if fmt == "block128" else 4)
+    s = 1
+    while s < 8 and rows * 2 * s <= sms and nch % (2 * s * gch) == 0 and nch // (2 * s) >= 128:
+        s *= 2
+    return s
+
+
+def _rows_of(fmt, M, layout):
+    if layout == "swizzled":
+        return -(-M // 128) * 128
+    if layout == "col_major":
+        return -(-M // 4) * 4
+    return M
+
+
+def _guarded(shape, dtype):
+    """A tensor of `shape` inside a 0xFF-filled byte buffer, and its byte count."""
+    esz = torch.empty((), dtype=dtype).element_size()
+    n = int(np.prod(shape)) * esz
+    raw = torch.full((n + GUARD,), 0xFF, dtype=torch.uint8, device=DEV)
+    return raw, raw[:n].view(dtype).view(shape), n
+
+
+def _gate_up(M, I, seed):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(M, 2 * I, generator=g) * 3.0).to(torch.bfloat16)
+
+
+def _bits(t):
+    return inputs.bf16_bits(t.detach().cpu())
+
+
+# (fmt, act, M, I, scale layout, from_fp32, round_act_bf16)
+CASES = [
+    ("block128", "silu_mul", 1, 12288, "row", False, True),        # 8 segments of 192 chunks
+    ("block128", "silu_mul", 32, 12288, "row", False, True),       # 4 segments
+    ("block128", "silu_mul", 1, 12288, "col_major", True, False),  # padding rows of the layout
+    ("block128", "swiglu_oai", 19, 5120, "col_major", True, False),
+    ("mxfp8", "swiglu_oai", 1, 2304, "row", True, False),          # 144-chunk segments in 160 threads
+    ("mxfp8", "swiglu_oai", 7, 12288, "row", True, False),
+    ("mxfp8", "silu_mul", 3, 4224, "row", False, False),           # 132-chunk segments in 160 threads
+    ("mxfp8", "swiglu_oai", 5, 6144, "row", False, False),
+]
+
+
+def _name(c):
+    return "-".join(str(v) for v in c)
+
+
+@pytest.mark.parametrize("c", CASES, ids=_name)
+def test_segmented_swiglu_quant(c):
+    fmt, act, M, I, layout, from32, rnd = c
+    rows = _rows_of(fmt, M, layout)
+    assert _segments(fmt, rows, I, _sms()) > 1, "case does not exercise a segmented launch on this device"
+    gu = _gate_up(M, I, seed=M * 7919 + I)
+    kw = dict(fmt=fmt, act=act, quant_from_fp32=from32, round_act_bf16=rnd)
+    qraw, q, qn = _guarded((M, I), torch.uint8)
+    sdt = torch.uint8 if fmt == "mxfp8" else torch.float32
+    sraw, s, sn = _guarded(scale_shape(fmt, M, I, layout), sdt)
+    swiglu_quant(gu.to(DEV), q_out=q, scale_out=s, scale_layout=layout, **kw)
+    # the same rows at the top of a batch that runs unsegmented, row-major scales
+    big = torch.cat([gu, _gate_up(BIG_M - M, I, seed=I)], dim=0)
+    assert _segments(fmt, BIG_M, I, _sms()) == 1
+    qb, sb = swiglu_quant(big.to(DEV), **kw)
+    torch.cuda.synchronize()
+    assert (qraw[qn:] == 0xFF).all(), "bytes written past q_out"
+    assert (sraw[sn:] == 0xFF).all(), "bytes written past scale_out"
+    assert torch.equal(q, qb[:M])
+    s_row = sb[:M].cpu().numpy()
+    if layout == "row":
+        np.testing.assert_array_equal(s.cpu().numpy(), s_row)
+    else:
+        np.testing.assert_array_equal(s.cpu().numpy(), oracle.scale_layout(fmt, s_row, layout))
+    ref = oracle.swiglu_quant(fmt, act, _bits(gu), from_fp32=from32, round_act_bf16=rnd)
+    check_swiglu(fmt, ref, qb[:M].cpu().numpy(), s_row, from_fp32=from32)
+
+
+@pytest.mark.parametrize("act,M,I,rnd", [("silu_mul", 1, 12288, True), ("swiglu_oai", 5, 2304, False),
+                                         ("silu_mul", 3, 4224, False)])
+def test_segmented_swiglu_bf16(act, M, I, rnd):
+    # the unfused chain's activation step (bf16 out, no quantisation) splits by MXFP8's groups
+    assert _segments("mxfp8", M, I, _sms()) > 1
+    gu = _gate_up(M, I, seed=M + I)
+    raw, out, n = _guarded((M, I), torch.bfloat16)
+    swiglu(gu.to(DEV), act=act, round_act_bf16=rnd, out=out)
+    big = torch.cat([gu, _gate_up(BIG_M - M, I, seed=I + 1)], dim=0)
+    ob = swiglu(big.to(DEV), act=act, round_act_bf16=rnd)
+    torch.cuda.synchronize()
+    assert (raw[n:] == 0xFF).all(), "bytes written past out"
+    assert torch.equal(out, ob[:M])
+    ref = oracle.swiglu_quant("mxfp8", act, _bits(gu), from_fp32=True, round_act_bf16=rnd)
+    check_bf16("activation", inputs.bf16_bits(inputs.to_bf16(ref["a"])), _bits(out))
