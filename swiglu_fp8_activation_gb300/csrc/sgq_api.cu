@@ -163,6 +163,22 @@ int launched(cudaError_t e) {
     return SGQ_ERR_LAUNCH;
 }
 
+// Column segments a row for a norm launch over `rows` rows (the grid's second
+// dimension): while twice the CTAs still fit on the device at one a
+// multiprocessor, a row is split in two, up to 8 segments, each a multiple of
+// 32 chunks (256 columns; whole warps and whole scale groups) and at least 64
+// chunks. Each CTA still reads the whole row of x and r for the sum of
+// squares, from L2 at these sizes, but reads the weight and writes the outputs
+// of its own segment only: at small M the row's output work and stores then
+// spread over several multiprocessors.
+int norm_segments(int64_t rows, int64_t H, int sms) {
+    if (sms <= 0) return 1;
+    const int64_t nch = H / 8;
+    int s = 1;
+    while (s < 8 && rows * 2 * s <= sms && nch % (64 * s) == 0 && nch / (2 * s) >= 64) s *= 2;
+    return s;
+}
+
 // The norm launch behind rmsnorm_add_quant (q_out set) and rmsnorm_add
 // (q_out null: only the bf16 copy). Width divisibility by the quant group
 // and the output pointers required by each entry are checked by the caller.
@@ -194,8 +210,14 @@ int norm_call(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, const vo
                           {r_out_span, act}};
     if (any_overlap(spans, 7)) return SGQ_ERR_INVALID_ARG;
 
+    // Rows too few to fill the device are split into column segments, except
+    // for an in-place residual update (another CTA of the row reads r back).
+    const int sms = sm_count();
+    const int seg = residual_out && residual_out == residual_in ? 1 : norm_segments(so.Ms, H, sms);
     sgq::Plan plan;
-    if (!plan_launch(M, (int)H, so, &plan)) return SGQ_ERR_UNSUPPORTED;
+    if (!sgq::plan_rows(so.Ms, (int)H, sms, &plan)) return SGQ_ERR_UNSUPPORTED;
+    plan.full = plan.full && so.Ms == M && seg == 1;   // the exact-fit kernels write whole rows
+    plan.seg = seg;
     sgq::NormArgs a;
     a.x = static_cast<const uint16_t*>(x);
     a.r_in = static_cast<const uint16_t*>(residual_in);
@@ -212,6 +234,7 @@ int norm_call(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, const vo
     a.rpc = plan.rpc;
     a.eps = eps;
     a.flags = flags;
+    a.segc = (int)(H / 8 / seg);
     return launched(sgq::launch_norm(fmt, dt_of(flags), plan, a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -481,6 +504,7 @@ int rmsnorm_dual_quant(int fmt, uint32_t flags, int64_t M, float eps, const sgq_
         a.rpc = rpc[i];
         a.eps = eps;
         a.flags = flags;
+        a.segc = (int)(s.H / 8);   // whole rows
     }
     d.grid0 = grid0;
     return launched(sgq::launch_norm_dual(fmt, dt_of(flags), plan, d, static_cast<cudaStream_t>(stream)));

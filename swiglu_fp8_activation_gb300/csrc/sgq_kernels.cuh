@@ -42,6 +42,7 @@ struct NormArgs {
     int rpc;                 // rows per CTA
     float eps;
     uint32_t flags;
+    int segc;                // output chunks a column segment (H / 8 / gridDim.y)
 };
 
 struct SwigluArgs {
@@ -202,7 +203,14 @@ __host__ __device__ constexpr int norm_stage_bytes(bool has_res, int nv, int thr
 // FULL: every thread's chunks lie inside the row and every row inside M (the
 // plan divides both exactly), so no bounds are checked. DT is the 16-bit
 // type of x, r, w and the written rows.
-template <int FMT, int LAYOUT, int NV, bool HAS_RES, bool FULL, int DT>
+// SEG: column segments (the bounds-checked single norm): each row may run as
+// gridDim.y CTAs. Every one of them reads the whole row of x and r and forms
+// the same sum of squares (and max |z|) in the same order, so all get the
+// bit-identical inv; CTA y then writes only chunks [y * segc, (y + 1) * segc),
+// segc a multiple of 32, so that a warp's chunks are all in or all out. The
+// host never splits an in-place residual update, which another CTA of the row
+// would read back.
+template <int FMT, int LAYOUT, int NV, bool HAS_RES, bool FULL, int DT, bool SEG = false>
 __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
     extern __shared__ uint4 stage[];
     __shared__ float2 part[32];
@@ -216,6 +224,8 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
     const int H = a.H, nchunks = H >> 3;
     const int64_t base = row * (int64_t)H;
     auto slot = [&](int v, int i) { return &stage[(NIN * v + i) * nt + threadIdx.x]; };
+    const int cb = SEG ? (int)blockIdx.y * a.segc : 0;                // the chunks this CTA writes
+    const int cend = SEG ? cb + a.segc : nchunks;
 
     // 1. every load of the row (x, r and the weight) goes out at once, copied
     //    asynchronously into this thread's shared-memory slots, one commit
@@ -231,7 +241,13 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
         cp_async16(slot(v, 0), ok ? (const void*)(a.x + row * a.ldx + (int64_t)c * 8) : (const void*)a.x, nb);
         if (HAS_RES)
             cp_async16(slot(v, 1), ok ? (const void*)(a.r_in + base + (int64_t)c * 8) : (const void*)a.x, nb);
-        cp_async16_cached(slot(v, NIN - 1), ok ? (const void*)(a.w + (int64_t)c * 8) : (const void*)a.x, nb);
+        if constexpr (SEG) {   // the weight only where this CTA writes (the per-token max |z| needs all of it)
+            const bool okw = ok && (FMT == FMT_PT || (c >= cb && c < cend));
+            cp_async16_cached(slot(v, NIN - 1), okw ? (const void*)(a.w + (int64_t)c * 8) : (const void*)a.x,
+                              okw ? 16 : 0);
+        } else {
+            cp_async16_cached(slot(v, NIN - 1), ok ? (const void*)(a.w + (int64_t)c * 8) : (const void*)a.x, nb);
+        }
         cp_async_commit();
     }
     pdl_trigger();
@@ -259,7 +275,9 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
                 h[k] = hs.x;
                 h[k + 1] = hs.y;
             }
-            if (a.r_out) st16_if(a.r_out + base + (int64_t)c * 8, pack8<DT>(h), FULL || (row_ok && c < nchunks));
+            if (a.r_out)
+                st16_if(a.r_out + base + (int64_t)c * 8, pack8<DT>(h),
+                        FULL || (row_ok && (SEG ? c >= cb && c < cend : c < nchunks)));
         }
         load8<DT>(ld_smem16(slot(v, NIN - 1)), wf);
 #pragma unroll
@@ -306,6 +324,9 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
             const int c = t + v * tpr;
+            // warps whose chunks lie outside this CTA's segment (or wholly past
+            // the row end) skip the chunk; c & ~31 is the same in every lane
+            if (SEG && ((c & ~31) < cb || (c & ~31) >= cend)) continue;
             const bool ok = FULL || (row_ok && c < nchunks);
             float y[8], src[8];
 #pragma unroll
@@ -335,7 +356,7 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
 
 template <int FMT, int LAYOUT, int NV, bool HAS_RES, bool FULL, int DT>
 __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
-    norm_rows<FMT, LAYOUT, NV, HAS_RES, FULL, DT>(a, blockIdx.x);
+    norm_rows<FMT, LAYOUT, NV, HAS_RES, FULL, DT, !FULL>(a, blockIdx.x);
 }
 
 // Two independent row sets normed in one launch (the q and kv latent norms

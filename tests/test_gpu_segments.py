@@ -1,22 +1,28 @@
-"""GPU parity of the SwiGLU launches that split rows into column segments.
+"""GPU parity of the launches that split rows into column segments.
 
-At small M the library runs each row of a wide SwiGLU as up to 8 CTAs, each
-taking a whole number of scale groups (MXFP8 and 1x128 only; the per-token
-format needs the row's amax). The cases below are chosen so that the launch
-is segmented on the device under test (checked against the host's rule),
-including segments that do not fill their CTA's threads, layouts that pad
-rows, SiLU's bf16 roundings and the bf16 output of the unfused chain. Each
-result must match the oracle under the usual tolerances, equal bit for bit
-the same rows computed inside a batch large enough to run unsegmented, and
-leave the bytes around its outputs untouched.
+SwiGLU: at small M the library runs each row of a wide SwiGLU as up to 8
+CTAs, each taking a whole number of scale groups (MXFP8 and 1x128 only; the
+per-token format needs the row's amax). The cases below are chosen so that
+the launch is segmented on the device under test (checked against the host's
+rule), including segments that do not fill their CTA's threads, layouts that
+pad rows, SiLU's bf16 roundings and the bf16 output of the unfused chain.
+Each result must match the oracle under the usual tolerances, equal bit for
+bit the same rows computed inside a batch large enough to run unsegmented,
+and leave the bytes around its outputs untouched.
+
+Norms: a row may also run as up to 8 CTAs that each form the whole row's sum
+of squares and write one column segment, in every format, but never for an
+in-place residual update. The split results must match the oracle, leave the
+bytes around every output untouched, and equal bit for bit the in-place
+launch of the same inputs (same plan, unsplit).
 """
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from oracle.parity import check_bf16, check_swiglu
-from swiglu_fp8_activation_gb300 import inputs, scale_shape, swiglu, swiglu_quant
+from oracle.parity import check_bf16, check_norm, check_swiglu
+from swiglu_fp8_activation_gb300 import inputs, rmsnorm_add_quant, scale_shape, swiglu, swiglu_quant
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -124,3 +130,72 @@ def test_segmented_swiglu_bf16(act, M, I, rnd):
     assert torch.equal(out, ob[:M])
     ref = oracle.swiglu_quant("mxfp8", act, _bits(gu), from_fp32=True, round_act_bf16=rnd)
     check_bf16("activation", inputs.bf16_bits(inputs.to_bf16(ref["a"])), _bits(out))
+
+
+def _norm_segments(rows, H, sms):
+    """The host's choice of column segments a row for a norm launch."""
+    nch = H // 8
+    s = 1
+    while s < 8 and rows * 2 * s <= sms and nch % (64 * s) == 0 and nch // (2 * s) >= 64:
+        s *= 2
+    return s
+
+
+# (fmt, M, H, gemma, residual, normed, from_fp32, scale layout)
+NORM_CASES = [
+    ("mxfp8", 8, 6144, True, True, True, False, "row"),          # 8 segments of 96 chunks
+    ("mxfp8", 16, 6144, True, True, True, False, "row"),
+    ("mxfp8", 64, 6144, True, True, False, False, "row"),        # 2 segments
+    ("mxfp8", 2, 8704, False, True, True, True, "row"),          # 3 chunks a thread, past the row end
+    ("mxfp8", 3, 2560, True, False, True, False, "row"),
+    ("block128", 1, 4096, False, False, False, True, "row"),     # 8 segments of 64 chunks
+    ("block128", 5, 4096, False, True, True, False, "col_major"),
+    ("per_token", 1, 7168, False, False, False, False, "row"),   # 4 segments; the row scale from segment 0
+    ("per_token", 3, 1536, False, True, True, True, "row"),
+]
+
+
+def _norm_name(c):
+    return "-".join(str(v) for v in c)
+
+
+@pytest.mark.parametrize("c", NORM_CASES, ids=_norm_name)
+def test_segmented_norm(c):
+    fmt, M, H, gemma, res, normed, from32, layout = c
+    assert _norm_segments(_rows_of(fmt, M, layout), H, _sms()) > 1, "case does not split on this device"
+    t = inputs.norm_inputs(M, H, seed=M * 131 + H, x_std=3.0, r_std=1.0 if res else None,
+                           w_mean=0.0 if gemma else 1.0, w_std=0.1)
+    x, w = t["x"].to(DEV), t["w"].to(DEV)
+    r = t["r"].to(DEV) if res else None
+    qraw, q, qn = _guarded((M, H), torch.uint8)
+    sdt = torch.float32 if fmt != "mxfp8" else torch.uint8
+    sraw, s, sn = _guarded(scale_shape(fmt, M, H, layout), sdt)
+    nraw, n, nn = _guarded((M, H), torch.bfloat16)
+    rraw, ro, rn = _guarded((M, H), torch.bfloat16)
+    kw = dict(fmt=fmt, gemma=gemma, quant_from_fp32=from32, scale_layout=layout)
+    rmsnorm_add_quant(x, w, residual_in=r, residual_out=ro if res else None, q_out=q, scale_out=s,
+                      normed_out=n if normed else None, **kw)
+    torch.cuda.synchronize()
+    for raw, nbytes, what in ((qraw, qn, "q_out"), (sraw, sn, "scale_out"), (nraw, nn, "normed_out"),
+                              (rraw, rn, "residual_out")):
+        assert (raw[nbytes:] == 0xFF).all(), f"bytes written past {what}"
+    if res:
+        # the in-place update of the same residual runs unsplit with the same plan: bit for bit equal
+        r2 = r.clone()
+        q2, s2, n2, _ = rmsnorm_add_quant(x, w, residual_in=r2, normed=normed, **kw)
+        torch.cuda.synchronize()
+        assert torch.equal(q, q2) and torch.equal(s, s2) and torch.equal(ro, r2)
+        if normed:
+            assert torch.equal(n, n2)
+    s_row = s.cpu().numpy()
+    if layout != "row":
+        q3, s3, _, _ = rmsnorm_add_quant(x, w, residual_in=r.clone() if res else None,
+                                         **{**kw, "scale_layout": "row"})
+        torch.cuda.synchronize()
+        assert torch.equal(q, q3)
+        np.testing.assert_array_equal(s_row, oracle.scale_layout(fmt, s3.cpu().numpy(), layout))
+        s_row = s3.cpu().numpy()
+    ref = oracle.rmsnorm_add_quant(fmt, _bits(t["x"]), _bits(t["r"]) if res else None, _bits(t["w"]), eps=1e-6,
+                                   gemma=gemma, from_fp32=from32, normed=normed)
+    check_norm(fmt, ref, q.cpu().numpy(), s_row, _bits(n) if normed else None, _bits(ro) if res else None,
+               from_fp32=from32)
