@@ -643,7 +643,10 @@ def run_profile(args):
     launches. norm / swiglu: the M=8192 prefill workload (inputs > L2,
     rotated). pertoken: RMSNorm + per-token FP8 at W=7168, M=4096 (three
     rotating input sets, 176 MB together). silu128: SiLU-and-mul + 1x128
-    (bf16 roundings) at I=12288, M=2048 (three sets, 302 MB together)."""
+    (bf16 roundings) at I=12288, M=2048 (three sets, 302 MB together).
+    norm8: the decode norm (add + Gemma RMSNorm + MXFP8 + bf16 copy, separate
+    residual output) at M=8, H=6144, inputs resident in L2; norm8_inplace:
+    the same with the residual updated in place (whole rows, one CTA each)."""
     import torch
     dev = torch.device("cuda", 0)
     if args.profile == "silu128":
@@ -661,6 +664,23 @@ def run_profile(args):
         fn = lib.swiglu_quant
         nbytes = swiglu_bytes(M, I, "block128")
         get = lambda k: arglist[k % ROTATE]
+    elif args.profile in ("norm8", "norm8_inplace"):
+        from swiglu_fp8_activation_gb300 import inputs, library
+        import ctypes as C
+        case = inputs.norm_case_gemma_mx(8)
+        t = inputs.make_norm(case)
+        x, r, w = (t[k].to(dev) for k in ("x", "r", "w"))
+        q = torch.empty(case.M, case.H, dtype=torch.uint8, device=dev)
+        sc = torch.empty(case.M, case.H // 32, dtype=torch.uint8, device=dev)
+        nrm = torch.empty(case.M, case.H, dtype=torch.bfloat16, device=dev)
+        ro = r if args.profile == "norm8_inplace" else torch.empty_like(nrm)
+        lib = library()
+        stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+        ptr = lambda a: C.c_void_p(a.data_ptr())
+        args1 = (0, 1, case.M, case.H, case.eps, ptr(x), ptr(r), ptr(ro), ptr(w), ptr(q), ptr(sc), ptr(nrm), stream)
+        fn = lib.rmsnorm_add_quant
+        nbytes = norm_bytes(case.M, case.H)
+        get = lambda k: args1
     elif args.profile == "pertoken":
         from swiglu_fp8_activation_gb300 import inputs, library
         case = inputs.norm_case_per_token(4096, 7168)
@@ -705,7 +725,7 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle time")
     ap.add_argument("--quick", action="store_true", help="skip the decode and other-config tables")
-    ap.add_argument("--profile", choices=("norm", "swiglu", "pertoken", "silu128"),
+    ap.add_argument("--profile", choices=("norm", "swiglu", "pertoken", "silu128", "norm8", "norm8_inplace"),
                     help="time one kernel only (for ncu)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -199,3 +199,24 @@ def test_segmented_norm(c):
                                    gemma=gemma, from_fp32=from32, normed=normed)
     check_norm(fmt, ref, q.cpu().numpy(), s_row, _bits(n) if normed else None, _bits(ro) if res else None,
                from_fp32=from32)
+
+
+def test_segmented_norm_fp16():
+    # fp16 rows with a separate residual, split in 8 (M = 4, H = 4096)
+    M, H = 4, 4096
+    assert _norm_segments(M, H, _sms()) > 1
+    g = torch.Generator().manual_seed(4096)
+    x = (torch.randn(M, H, generator=g) * 3.0).to(torch.float16)
+    r = torch.randn(M, H, generator=g).to(torch.float16)
+    w = (0.1 * torch.randn(H, generator=g)).to(torch.float16)
+    xd, rd, wd = x.to(DEV), r.to(DEV), w.to(DEV)
+    ro = torch.empty_like(rd)
+    q, s, n, _ = rmsnorm_add_quant(xd, wd, residual_in=rd, residual_out=ro, normed=True)
+    r2 = rd.clone()
+    q2, s2, n2, _ = rmsnorm_add_quant(xd, wd, residual_in=r2, normed=True)   # in place: unsplit
+    torch.cuda.synchronize()
+    assert torch.equal(q, q2) and torch.equal(s, s2) and torch.equal(n, n2) and torch.equal(ro, r2)
+    f16 = lambda t: t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    ref = oracle.rmsnorm_add_quant("mxfp8", f16(x), f16(r), f16(w), eps=1e-6, gemma=True, from_fp32=False,
+                                   normed=True, fp16=True)
+    check_norm("mxfp8", ref, q.cpu().numpy(), s.cpu().numpy(), f16(n), f16(ro), from_fp32=False)
