@@ -220,3 +220,58 @@ def test_segmented_norm_fp16():
     ref = oracle.rmsnorm_add_quant("mxfp8", f16(x), f16(r), f16(w), eps=1e-6, gemma=True, from_fp32=False,
                                    normed=True, fp16=True)
     check_norm("mxfp8", ref, q.cpu().numpy(), s.cpu().numpy(), f16(n), f16(ro), from_fp32=False)
+
+
+def test_split_launches_chained():
+    # Four layers: norm (8 segments) -> SwiGLU on its bf16 copy (2 segments), the residual carried
+    # from layer to layer. Launched back to back (each launch may begin before the previous one
+    # ends), and replayed from a CUDA graph, the chain must equal the same chain with a device
+    # synchronisation after every launch, and the in-place residual chain (whole rows).
+    M, H, L = 8, 6144, 4
+    assert _norm_segments(M, H, _sms()) == 8 and _segments("mxfp8", M, H // 2, _sms()) == 2
+    g = torch.Generator().manual_seed(77)
+    xs = [(torch.randn(M, H, generator=g) * 3.0).to(torch.bfloat16).to(DEV) for _ in range(L)]
+    ws = [(0.1 * torch.randn(H, generator=g)).to(torch.bfloat16).to(DEV) for _ in range(L)]
+    r0 = torch.randn(M, H, generator=g).to(torch.bfloat16).to(DEV)
+
+    def buffers():
+        return dict(r=[torch.empty(M, H, dtype=torch.bfloat16, device=DEV) for _ in range(L)],
+                    q=[torch.empty(M, H, dtype=torch.uint8, device=DEV) for _ in range(L)],
+                    s=[torch.empty(M, H // 32, dtype=torch.uint8, device=DEV) for _ in range(L)],
+                    n=[torch.empty(M, H, dtype=torch.bfloat16, device=DEV) for _ in range(L)],
+                    aq=[torch.empty(M, H // 2, dtype=torch.uint8, device=DEV) for _ in range(L)],
+                    asc=[torch.empty(M, H // 64, dtype=torch.uint8, device=DEV) for _ in range(L)])
+
+    def chain(b, sync):
+        r_in = r0
+        for k in range(L):
+            rmsnorm_add_quant(xs[k], ws[k], residual_in=r_in, residual_out=b["r"][k], q_out=b["q"][k],
+                              scale_out=b["s"][k], normed_out=b["n"][k])
+            if sync:
+                torch.cuda.synchronize()
+            swiglu_quant(b["n"][k], q_out=b["aq"][k], scale_out=b["asc"][k])
+            if sync:
+                torch.cuda.synchronize()
+            r_in = b["r"][k]
+
+    ref, eager, graphed = buffers(), buffers(), buffers()
+    chain(ref, sync=True)
+    chain(eager, sync=False)
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        chain(graphed, sync=False)
+    gr.replay()
+    torch.cuda.synchronize()
+    for key in ref:
+        for k in range(L):
+            assert torch.equal(ref[key][k], eager[key][k]), (key, k, "back to back")
+            assert torch.equal(ref[key][k], graphed[key][k]), (key, k, "graph replay")
+    # the in-place residual chain runs whole rows: the same values
+    r = r0.clone()
+    for k in range(L):
+        q, s, n, _ = rmsnorm_add_quant(xs[k], ws[k], residual_in=r, normed=True)
+        torch.cuda.synchronize()
+        assert torch.equal(r, ref["r"][k]) and torch.equal(q, ref["q"][k]) and torch.equal(s, ref["s"][k])
+        assert torch.equal(n, ref["n"][k])
