@@ -240,16 +240,17 @@ int norm_call(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, const vo
 
 // Column segments a row for a SwiGLU launch over `rows` rows (the grid's
 // second dimension): while twice the CTAs still fit on the device at one a
-// multiprocessor, a row is split in two, up to 8 segments, each a whole
-// number of scale groups and at least 1024 columns. At small M this spreads
-// a wide row's activation arithmetic (two special-function operations an
-// element) over 8 multiprocessors instead of one. The per-token format needs
-// the row's amax and is never split.
+// multiprocessor, a row is split in two, up to 16 segments, each a whole
+// number of scale groups and at least 512 columns. At small M this spreads a
+// wide row's activation arithmetic (two special-function operations an
+// element) over up to 16 multiprocessors instead of one. (Allowing two CTAs
+// an SM measured slower.) The per-token format needs the row's amax and is
+// never split.
 int swiglu_segments(int fmt, int64_t rows, int64_t I, int sms) {
     if (fmt == SGQ_FMT_FP8_PER_TOKEN || sms <= 0) return 1;
     const int64_t nch = I / 8, gch = fmt == SGQ_FMT_FP8_BLOCK128 ? 16 : 4;   // chunks a row, a scale group
     int s = 1;
-    while (s < 8 && rows * 2 * s <= sms && nch % (2 * s * gch) == 0 && nch / (2 * s) >= 128) s *= 2;
+    while (s < 16 && rows * 2 * s <= sms && nch % (2 * s * gch) == 0 && nch / (2 * s) >= 64) s *= 2;
     return s;
 }
 
