@@ -261,6 +261,64 @@ def time_prefill(pf, steps, warmup, world):
     return total_ms, statistics.mean(norm_ms), statistics.mean(swiglu_ms)
 
 
+def time_alone(pf, which, steps):
+    """One kernel of the prefill step launched `steps` times back to back
+    (inputs rotated over the buffer sets, each larger than L2), timed with
+    CUDA events around the loop: µs per launch."""
+    import torch
+    idx = 0 if which == "norm" else 1
+    fn = pf.lib.rmsnorm_add_quant if which == "norm" else pf.lib.swiglu_quant
+    for k in range(3):
+        _call(fn, pf.args[k % ROTATE][idx])
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for k in range(steps):
+        _call(fn, pf.args[k % ROTATE][idx])
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) * 1e3 / steps
+
+
+def host_us_per_call(dev, calls=2000):
+    """Host time of one eager call of the raw C ABI at M=8 (norm + MXFP8 +
+    bf16 copy, H=6144), through ctypes, while the GPU runs the launches;
+    beside it the ctypes floor (a call of sgq_abi_version, which does
+    nothing)."""
+    import ctypes as C
+
+    import torch
+
+    from swiglu_fp8_activation_gb300 import inputs, library
+    lib = library()
+    case = inputs.norm_case_gemma_mx(8)
+    t = inputs.make_norm(case)
+    x, r, w = (t[k].to(dev) for k in ("x", "r", "w"))
+    q = torch.empty(8, H, dtype=torch.uint8, device=dev)
+    sc = torch.empty(8, H // 32, dtype=torch.uint8, device=dev)
+    n = torch.empty(8, H, dtype=torch.bfloat16, device=dev)
+    ro = torch.empty_like(n)
+    ptr = lambda a: C.c_void_p(a.data_ptr())
+    stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    args = (0, 1, 8, H, 1e-6, ptr(x), ptr(r), ptr(ro), ptr(w), ptr(q), ptr(sc), ptr(n), stream)
+    fn = lib.rmsnorm_add_quant
+    for _ in range(50):
+        _call(fn, args)
+    torch.cuda.synchronize()
+    best, floor = float("inf"), float("inf")
+    for _ in range(5):
+        t0 = time.perf_counter()
+        for _ in range(calls):
+            fn(*args)
+        best = min(best, (time.perf_counter() - t0) / calls * 1e6)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(calls):
+            lib.sgq_abi_version()
+        floor = min(floor, (time.perf_counter() - t0) / calls * 1e6)
+    return round(best, 3), round(floor, 3)
+
+
 def graph_us_per_launch(fn, iters=200, reps=20):
     """µs per launch: a CUDA graph of `iters` back-to-back launches, 3 warm
     replays, median of `reps` timed replays."""
@@ -288,7 +346,8 @@ def graph_us_per_launch(fn, iters=200, reps=20):
 
 def decode_table(dev):
     """µs per launch at M = 8..192 for the two decode workloads (fused norm
-    +MXFP8+bf16 copy at H=6144; OAI SwiGLU+MXFP8 at I=768), each beside its
+    +MXFP8+bf16 copy at H=6144, with a separate residual output and with the
+    residual updated in place; OAI SwiGLU+MXFP8 at I=768), each beside its
     unfused chain (norm to bf16, then a separate MXFP8 quant; SwiGLU to bf16,
     then a separate quant), both chains' launches in one graph, as the pages'
     decode table compares them."""
@@ -296,7 +355,7 @@ def decode_table(dev):
 
     from swiglu_fp8_activation_gb300 import (inputs, quantize_fp8, rmsnorm_add, rmsnorm_add_quant, swiglu,
                                               swiglu_quant)
-    out = {"norm_mxfp8_bf16copy_H6144": {}, "norm_then_quant_H6144": {},
+    out = {"norm_mxfp8_bf16copy_H6144": {}, "norm_mxfp8_bf16copy_H6144_inplace": {}, "norm_then_quant_H6144": {},
            "swiglu_oai_mxfp8_I768": {}, "swiglu_then_quant_I768": {}}
     for M in DECODE_MS:
         nc = inputs.norm_case_gemma_mx(M)
@@ -308,6 +367,9 @@ def decode_table(dev):
         ro = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
         fn = lambda: rmsnorm_add_quant(x, w, residual_in=r, residual_out=ro, q_out=q, scale_out=s, normed_out=n)
         out["norm_mxfp8_bf16copy_H6144"][str(M)] = round(graph_us_per_launch(fn), 3)
+        ri = r.clone()   # the residual updated in place, launch after launch
+        fni = lambda: rmsnorm_add_quant(x, w, residual_in=ri, residual_out=ri, q_out=q, scale_out=s, normed_out=n)
+        out["norm_mxfp8_bf16copy_H6144_inplace"][str(M)] = round(graph_us_per_launch(fni), 3)
 
         def norm_chain():
             rmsnorm_add(x, w, residual_in=r, residual_out=ro, normed_out=n)
@@ -591,6 +653,10 @@ def run_ours(args, world, rank, local):
         others = other_configs(dev) if rank == 0 and not args.quick else None
         qkv = qkv_norm_configs(dev) if rank == 0 and not args.quick else None
     total_ms = max_over_ranks(total_ms, world)
+    alone_steps = max(args.steps, 200)
+    norm_alone_us = time_alone(pf, "norm", alone_steps)
+    swiglu_alone_us = time_alone(pf, "swiglu", alone_steps)
+    host_us, ctypes_us = host_us_per_call(dev) if rank == 0 and not args.quick else (None, None)
     e2e_ms, h2d, d2h = time_e2e(pf, dev, args.e2e_steps)
     e2e_ms = max_over_ranks(e2e_ms, world)
     if rank != 0:
@@ -619,7 +685,14 @@ def run_ours(args, world, rank, local):
                      "traffic": _measured_traffic("norm_mxfp8_H6144_M8192"), "algorithmic_bytes": nb},
         "kernels": {"norm_us": round(norm_ms * 1e3, 2), "norm_GBps": round(norm_gbs, 1),
                     "swiglu_us": round(swiglu_ms * 1e3, 2), "swiglu_GBps": round(swiglu_gbs, 1),
-                    "swiglu_frac": round(swiglu_gbs / peak, 4)},
+                    "swiglu_frac": round(swiglu_gbs / peak, 4),
+                    "alone": {"launches": alone_steps,
+                              "norm_us": round(norm_alone_us, 2),
+                              "norm_frac": round(nb / (norm_alone_us * 1e-6) / 1e9 / peak, 4),
+                              "swiglu_us": round(swiglu_alone_us, 2),
+                              "swiglu_frac": round(swiglu_bytes(M_PREFILL, I_PREFILL) / (swiglu_alone_us * 1e-6)
+                                                   / 1e9 / peak, 4)}},
+        "host_us_per_eager_call_M8": {"rmsnorm_add_quant": host_us, "ctypes_floor": ctypes_us},
         "decode_us_per_launch": decode,
         "other_configs": others,
         "qkv_latent_norm_us": qkv,

@@ -37,10 +37,12 @@
  * Conventions shared by all entry points
  *   - All tensor pointers are DEVICE pointers owned by the caller (the dual
  *     norm's two segment descriptors are host structs, read during the call
- *     only). The library allocates nothing, keeps no state between calls
- *     (but the calling thread's last launch error, see sgq_launch_error),
- *     never synchronises and launches nothing but its one kernel, so calls
- *     may be captured into CUDA graphs.
+ *     only). The library allocates nothing, never synchronises and launches
+ *     nothing but its one kernel, so calls may be captured into CUDA graphs.
+ *     State kept between calls: the calling thread's last launch error (see
+ *     sgq_launch_error), each device's multiprocessor count (queried on the
+ *     first call on that device), the shared-memory opt-in each kernel was
+ *     given on each device, and the planning count of sgq_set_sm_budget.
  *   - All tensors are contiguous and row-major (the dual norm's inputs may
  *     have a row stride). 16-bit activations are bfloat16, or IEEE fp16 with
  *     SGQ_F_FP16 where an entry point accepts it. Quantised values are OCP
@@ -55,10 +57,17 @@
  *     unquantised dual segment) needs W % 8 == 0; W <= SGQ_MAX_WIDTH.
  *   - Outputs may not overlap inputs or each other, except that residual_out
  *     may equal residual_in exactly (in-place update).
+ *   - Launch order: every kernel may begin while the kernel before it on the
+ *     stream is finishing (programmatic dependent launch), and waits for
+ *     that kernel to complete before it reads an activation or writes any
+ *     output. The norms read their weight before that wait, so the kernel
+ *     launched just before a norm on its stream must not write that norm's
+ *     weight (weights written by a copy, or by any earlier kernel, are fine).
  *   - M == 0 returns SGQ_OK without a launch (pointers are not inspected).
  *   - Errors: arguments are checked on the host before anything is launched;
  *     a rejected call leaves every buffer untouched. SGQ_ERR_LAUNCH reports a
- *     failed launch (cudaGetLastError after the launch).
+ *     failed launch (the error cudaLaunchKernelEx returns for this launch; an
+ *     error pending on the thread from other work is left alone).
  *   - Non-finite inputs (inf, NaN) are outside the contract: the kernels do
  *     not fault on them, but their outputs are unspecified. So are norm rows
  *     whose sum of squares overflows fp32 (|h| of order 1e19 / sqrt(H)).
@@ -160,7 +169,9 @@ typedef void* sgq_stream_t;
  *   residual_in   [M, H] bf16, read, or NULL
  *   residual_out  [M, H] bf16, written, or NULL; must be NULL when residual_in
  *                 is NULL; may equal residual_in
- *   weight        [H] bf16, read
+ *   weight        [H] bf16, read before the launch waits for the kernel that
+ *                 precedes it on the stream, which must not write it (see
+ *                 "Launch order" above)
  *   q_out         [M, H] E4M3, written
  *   scale_out     scales in the layout of fmt and flags, written
  *   normed_out    [M, H] bf16, written, or NULL
@@ -298,6 +309,20 @@ typedef struct sgq_norm_seg {
  */
 int rmsnorm_dual_quant(int fmt, uint32_t flags, int64_t M, float eps, const sgq_norm_seg_t* seg_a,
                        const sgq_norm_seg_t* seg_b, sgq_stream_t stream);
+
+/*
+ * Plan launches as if the device had `sms` multiprocessors; 0 (the default)
+ * uses the current device's own count, queried once per device. The count
+ * decides how many rows share a CTA, how many threads own a row and when a
+ * row runs as several CTAs (column segments), e.g. for callers that give
+ * these kernels only part of the GPU (an MPS or green-context partition).
+ * Every plan meets the same contract, but a norm's sum of squares is added
+ * in the order its plan gives, so the bits of a norm's outputs may differ
+ * between two counts (within the stated tolerances of the definition).
+ * Process-wide, for calls made after it returns. sms < 0 returns
+ * SGQ_ERR_INVALID_ARG. Not part of any page: a host planning control.
+ */
+int sgq_set_sm_budget(int sms);
 
 /* A static, human-readable name of a status code. */
 const char* sgq_status_string(int status);

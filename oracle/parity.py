@@ -14,7 +14,8 @@ Tolerances:
     In excused groups the dequantised values agree within one E4M3 step.
     Elements the oracle marks as ties (fp32-source FP8 formats: y/s within
     2^-22 of an E4M3 midpoint, where either neighbour is a correct rounding)
-    must be within one step but do not count toward the 1e-4.
+    count toward the 1e-4 like any other element; their mismatches are also
+    reported on their own (`tie_mismatch`).
 The check also counts mismatches at elements the oracle did not flag as near
 a rounding boundary (`unflagged`), a stricter signal reported in the stats.
 """
@@ -71,8 +72,12 @@ def _dequant(fmt: str, q: np.ndarray, scale: np.ndarray, gs: int) -> np.ndarray:
     return vals * np.repeat(s, gs, axis=1)
 
 
-def check_quant(fmt: str, ref: dict, q: np.ndarray, scale: np.ndarray, from_fp32: bool) -> dict:
-    """Compare codes and scales with the oracle result `ref` (same rows)."""
+def check_quant(fmt: str, ref: dict, q: np.ndarray, scale: np.ndarray, from_fp32: bool, budget: bool = True) -> dict:
+    """Compare codes and scales with the oracle result `ref` (same rows).
+
+    budget=False leaves out the 1e-4 fraction test (every other test still
+    applies), for callers that check the fraction over several row blocks
+    at once from the returned counts `code_mismatch` and `n_plain`."""
     q = np.asarray(q)
     scale = np.asarray(scale)
     M, W = ref["q"].shape
@@ -113,10 +118,12 @@ def check_quant(fmt: str, ref: dict, q: np.ndarray, scale: np.ndarray, from_fp32
     n_plain = int(plain.sum())
     tie = (ref["amb"] & AMB_TIE) != 0
     assert step[plain].max(initial=0) <= 1, f"E4M3 code off by {step[plain].max()} steps"
-    mism = (step != 0) & plain & ~tie
+    mism = (step != 0) & plain
     frac = float(mism.sum()) / max(n_plain, 1)
-    stats["tie_mismatch"] = int(((step != 0) & plain & tie).sum())
-    assert frac <= MAX_CODE_MISMATCH_FRACTION, f"E4M3 mismatch fraction {frac:.2e} > 1e-4"
+    stats["tie_mismatch"] = int((mism & tie).sum())
+    if budget:
+        assert frac <= MAX_CODE_MISMATCH_FRACTION, \
+            f"E4M3 mismatch fraction {frac:.2e} > 1e-4 ({int(mism.sum())} of {n_plain}, {stats['tie_mismatch']} at ties)"
     if excused.any():
         dq_ref = _dequant(fmt, ref["q"], rs, gs)
         dq = _dequant(fmt, q, scale, gs)
@@ -125,7 +132,7 @@ def check_quant(fmt: str, ref: dict, q: np.ndarray, scale: np.ndarray, from_fp32
         e = np.abs(dq_ref - dq)
         assert (e[excused] <= tol[excused] * (1 + 1e-9)).all(), "excused group dequantised values differ by more than one step"
     flagged = (ref["amb"] & AMB_CODE) != 0
-    stats.update(code_mismatch=int(mism.sum()), code_mismatch_frac=frac,
+    stats.update(code_mismatch=int(mism.sum()), code_mismatch_frac=frac, n_plain=n_plain,
                  unflagged=int((mism & ~flagged).sum()), excused_elems=int(excused.sum()))
     return stats
 
@@ -136,8 +143,9 @@ def _scale_values(fmt: str, s: np.ndarray) -> np.ndarray:
     return s.astype(np.float64)
 
 
-def check_norm(fmt: str, ref: dict, q, scale, normed_bits=None, residual_bits=None, *, from_fp32: bool) -> dict:
-    stats = check_quant(fmt, ref, q, scale, from_fp32)
+def check_norm(fmt: str, ref: dict, q, scale, normed_bits=None, residual_bits=None, *, from_fp32: bool,
+               budget: bool = True) -> dict:
+    stats = check_quant(fmt, ref, q, scale, from_fp32, budget)
     if residual_bits is not None:
         stats.update(check_bf16("residual", ref["residual"], np.asarray(residual_bits)))
     if normed_bits is not None:
@@ -145,5 +153,5 @@ def check_norm(fmt: str, ref: dict, q, scale, normed_bits=None, residual_bits=No
     return stats
 
 
-def check_swiglu(fmt: str, ref: dict, q, scale, *, from_fp32: bool) -> dict:
-    return check_quant(fmt, ref, q, scale, from_fp32)
+def check_swiglu(fmt: str, ref: dict, q, scale, *, from_fp32: bool, budget: bool = True) -> dict:
+    return check_quant(fmt, ref, q, scale, from_fp32, budget)

@@ -23,5 +23,5 @@ from .binding import (  # noqa: F401
     FORMATS, ACTS, F_GEMMA_WEIGHT, F_QUANT_FROM_FP32, F_ACT_ROUND_BF16, F_SCALE_SWIZZLED, F_SCALE_COL_MAJOR,
     SCALE_LAYOUTS, scale_shape,
     SgqError, library, library_path, rmsnorm_add_quant, swiglu_quant, status_string,
-    rmsnorm_add, swiglu, quantize_fp8, rmsnorm_dual_quant, NormSeg, F_FP16,
+    rmsnorm_add, swiglu, quantize_fp8, rmsnorm_dual_quant, NormSeg, F_FP16, set_sm_budget,
 )

@@ -76,12 +76,20 @@ def library() -> C.CDLL:
         L.sgq_abi_version.argtypes = []
         L.sgq_launch_error.restype = C.c_char_p
         L.sgq_launch_error.argtypes = []
+        L.sgq_set_sm_budget.restype = C.c_int
+        L.sgq_set_sm_budget.argtypes = [C.c_int]
         _lib = L
     return _lib
 
 
 def status_string(status: int) -> str:
     return library().sgq_status_string(int(status)).decode()
+
+
+def set_sm_budget(sms: int) -> None:
+    """Plan launches as if the device had `sms` multiprocessors (0: the
+    device's own count). Process-wide; see sgq_set_sm_budget in sgq.h."""
+    _check(library().sgq_set_sm_budget(int(sms)), "sgq_set_sm_budget")
 
 
 def _check(status: int, what: str):

@@ -6,6 +6,10 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+#include <mutex>
+#include <unordered_map>
+
 #include <cuda_runtime.h>
 
 #include "sgq.h"
@@ -56,9 +60,23 @@ bool plan_rows(int64_t M, int W, int sm_count, Plan* p) {
 
 namespace {
 thread_local cudaError_t last_launch_error = cudaSuccess;
+
+// Largest dynamic shared memory granted to each (kernel, device) so far.
+std::mutex smem_mu;
+std::unordered_map<const void*, int> smem_granted[64];
 }  // namespace
 
 void note_launch_error(cudaError_t e) { last_launch_error = e; }
+
+cudaError_t ensure_dynamic_smem(const void* kernel, int device, int bytes) {
+    if (device < 0 || device >= 64) return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    std::lock_guard<std::mutex> lock(smem_mu);
+    int& granted = smem_granted[device][kernel];
+    if (granted >= bytes) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) granted = bytes;
+    return e;
+}
 
 }  // namespace sgq
 
@@ -78,8 +96,6 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 int group_of(int fmt) { return fmt == SGQ_FMT_MXFP8 ? 32 : fmt == SGQ_FMT_FP8_BLOCK128 ? 128 : 8; }
-
-int sm_count();
 
 int dt_of(uint32_t flags) { return (flags & SGQ_F_FP16) ? sgq::DT_F16 : sgq::DT_BF16; }
 
@@ -127,20 +143,49 @@ bool scale_geometry(int fmt, uint32_t flags, int64_t M, int64_t W, sgq::ScaleOut
     return true;
 }
 
+// The current device and its multiprocessor count. The count is queried
+// once per device and cached; on the call path the one runtime call left is
+// cudaGetDevice, which reads the calling thread's current device.
+// sgq_set_sm_budget() replaces the count used for planning.
+constexpr int kMaxDevices = 64;
+std::atomic<int> sm_cache[kMaxDevices];
+std::atomic<int> sm_budget{0};
+
+struct Device {
+    int id;
+    int sms;
+};
+
+Device current_device() {
+    Device d = {-1, 0};
+    if (cudaGetDevice(&d.id) != cudaSuccess) return {-1, 0};
+    const int budget = sm_budget.load(std::memory_order_relaxed);
+    if (budget > 0) {
+        d.sms = budget;
+        return d;
+    }
+    if (d.id < 0 || d.id >= kMaxDevices) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d.id) == cudaSuccess) d.sms = n;
+        return d;
+    }
+    int n = sm_cache[d.id].load(std::memory_order_relaxed);
+    if (n <= 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d.id) != cudaSuccess) n = 0;
+        if (n > 0) sm_cache[d.id].store(n, std::memory_order_relaxed);
+    }
+    d.sms = n;
+    return d;
+}
+
 // Plan the rows of a launch whose scale layout covers so.Ms >= M rows: the
 // grid covers the layout's padding rows too, and the exact-fit kernels only
 // run when there are none.
-bool plan_launch(int64_t M, int W, const sgq::ScaleOut& so, sgq::Plan* p) {
-    if (!sgq::plan_rows(so.Ms, W, sm_count(), p)) return false;
+bool plan_launch(int64_t M, int W, const sgq::ScaleOut& so, const Device& dev, sgq::Plan* p) {
+    if (!sgq::plan_rows(so.Ms, W, dev.sms, p)) return false;
     p->full = p->full && so.Ms == M;
+    p->device = dev.id;
     return true;
-}
-
-int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return n;
 }
 
 struct Span {
@@ -212,10 +257,12 @@ int norm_call(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, const vo
 
     // Rows too few to fill the device are split into column segments, except
     // for an in-place residual update (another CTA of the row reads r back).
-    const int sms = sm_count();
+    const Device dev = current_device();
+    const int sms = dev.sms;
     const int seg = residual_out && residual_out == residual_in ? 1 : norm_segments(so.Ms, H, sms);
     sgq::Plan plan;
     if (!sgq::plan_rows(so.Ms, (int)H, sms, &plan)) return SGQ_ERR_UNSUPPORTED;
+    plan.device = dev.id;
     plan.full = plan.full && so.Ms == M && seg == 1;   // the exact-fit kernels write whole rows
     plan.seg = seg;
     sgq::NormArgs a;
@@ -281,10 +328,12 @@ int swiglu_call(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float al
     if (any_overlap(spans, 4)) return SGQ_ERR_INVALID_ARG;
 
     // Rows too few to fill the device are split into column segments.
-    const int sms = sm_count();
+    const Device dev = current_device();
+    const int sms = dev.sms;
     const int seg = swiglu_segments(fmt, so.Ms, I, sms);
     sgq::Plan plan;
     if (!sgq::plan_rows(so.Ms, (int)(I / seg), sms, &plan)) return SGQ_ERR_UNSUPPORTED;
+    plan.device = dev.id;
     plan.full = plan.full && so.Ms == M && seg == 1;   // the exact-fit kernels run whole rows
     plan.seg = seg;
     sgq::SwigluArgs a;
@@ -361,6 +410,12 @@ extern "C" {
 
 int sgq_abi_version(void) { return SGQ_ABI_VERSION; }
 
+int sgq_set_sm_budget(int sms) {
+    if (sms < 0) return SGQ_ERR_INVALID_ARG;
+    sm_budget.store(sms, std::memory_order_relaxed);
+    return SGQ_OK;
+}
+
 const char* sgq_launch_error(void) {
     return sgq::last_launch_error == cudaSuccess ? "no launch error" : cudaGetErrorString(sgq::last_launch_error);
 }
@@ -431,7 +486,7 @@ int quantize_fp8(int fmt, uint32_t flags, int64_t M, int64_t W, const void* src,
     if (any_overlap(spans, 3)) return SGQ_ERR_INVALID_ARG;
 
     sgq::Plan plan;
-    if (!plan_launch(M, (int)W, so, &plan)) return SGQ_ERR_UNSUPPORTED;
+    if (!plan_launch(M, (int)W, so, current_device(), &plan)) return SGQ_ERR_UNSUPPORTED;
     sgq::QuantArgs a;
     a.src = static_cast<const uint16_t*>(src);
     a.q = static_cast<uint8_t*>(q_out);
@@ -484,7 +539,9 @@ int rmsnorm_dual_quant(int fmt, uint32_t flags, int64_t M, float eps, const sgq_
     sgq::Plan plan;
     int tpr[2], rpc[2];
     int64_t grid0 = 0;
-    if (!plan_dual(M, (int)seg_a->H, (int)seg_b->H, sm_count(), &plan, tpr, rpc, &grid0)) return SGQ_ERR_UNSUPPORTED;
+    const Device dev = current_device();
+    if (!plan_dual(M, (int)seg_a->H, (int)seg_b->H, dev.sms, &plan, tpr, rpc, &grid0)) return SGQ_ERR_UNSUPPORTED;
+    plan.device = dev.id;
     sgq::DualArgs d;
     for (int i = 0; i < 2; ++i) {
         const sgq_norm_seg_t& s = *sg[i];

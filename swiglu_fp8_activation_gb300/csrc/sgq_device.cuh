@@ -217,7 +217,9 @@ __device__ __forceinline__ uint32_t f32x4_to_e4m3x4(float a0, float a1, float a2
 // Programmatic dependent launch. pdl_wait() blocks until the grid this launch
 // depends on has completed and its writes are visible; it returns at once
 // when the launch has no programmatic dependency. Every kernel here calls it
-// before its first global memory access, so an early start is always safe.
+// before it reads an activation or writes anything; only the norms' weight,
+// which the entry points require the preceding kernel not to write, is read
+// before it.
 // pdl_trigger() lets the next grid on the stream begin launching; that grid
 // in turn waits in its own pdl_wait() before touching memory.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

@@ -228,10 +228,22 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
     const int cend = SEG ? cb + a.segc : nchunks;
 
     // 1. every load of the row (x, r and the weight) goes out at once, copied
-    //    asynchronously into this thread's shared-memory slots, one commit
-    //    group per chunk. A thread reads back only its own slots, and writes
-    //    the updated residual of a chunk only after that chunk's group has
-    //    landed, so an in-place residual update is safe.
+    //    asynchronously into this thread's shared-memory slots. The weight is
+    //    not written by the grid this launch may overlap (a contract of the
+    //    entry points), so its copies go out before pdl_wait() as one commit
+    //    group of their own; then x and r, one commit group per chunk. A
+    //    thread reads back only its own slots, and writes the updated residual
+    //    of a chunk only after that chunk's group has landed, so an in-place
+    //    residual update is safe.
+    // SEG: the weight only where this CTA writes (the per-token max |z| needs all of it)
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        const int c = t + v * tpr;
+        const bool okw = (FULL || (row_ok && c < nchunks)) && (!SEG || FMT == FMT_PT || (c >= cb && c < cend));
+        cp_async16_cached(slot(v, NIN - 1), okw ? (const void*)(a.w + (int64_t)c * 8) : (const void*)a.w,
+                          okw ? 16 : 0);
+    }
+    cp_async_commit();
     pdl_wait();
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
@@ -241,19 +253,15 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
         cp_async16(slot(v, 0), ok ? (const void*)(a.x + row * a.ldx + (int64_t)c * 8) : (const void*)a.x, nb);
         if (HAS_RES)
             cp_async16(slot(v, 1), ok ? (const void*)(a.r_in + base + (int64_t)c * 8) : (const void*)a.x, nb);
-        if constexpr (SEG) {   // the weight only where this CTA writes (the per-token max |z| needs all of it)
-            const bool okw = ok && (FMT == FMT_PT || (c >= cb && c < cend));
-            cp_async16_cached(slot(v, NIN - 1), okw ? (const void*)(a.w + (int64_t)c * 8) : (const void*)a.x,
-                              okw ? 16 : 0);
-        } else {
-            cp_async16_cached(slot(v, NIN - 1), ok ? (const void*)(a.w + (int64_t)c * 8) : (const void*)a.x, nb);
-        }
         cp_async_commit();
     }
     pdl_trigger();
 
     // 2. h = x + r in fp32; write the updated residual; z = h * w'; partial
-    //    sum of squares (and max |z| for the per-token format)
+    //    sum of squares (and max |z| for the per-token format). SEG: warps
+    //    whose chunks lie outside this CTA's segment only add their h^2 to the
+    //    sum (c & ~31 is the same in every lane of a warp, and segc is a
+    //    multiple of 32); their z is never used, except by the per-token max.
     const bool from32 = (a.flags & F_FROM_FP32) != 0;
     // w' = w + 1 (Gemma) or w + (-0), which is w exactly, signed zeros included
     const float w_add = (a.flags & F_GEMMA) ? 1.0f : -0.0f;
@@ -263,6 +271,7 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
         const int c = t + v * tpr;
+        const bool mine = !SEG || FMT == FMT_PT || ((c & ~31) >= cb && (c & ~31) < cend);
         float h[8], wf[8];
         cp_async_wait_group_of<NV>(v);
         load8<DT>(ld_smem16(slot(v, 0)), h);
@@ -275,9 +284,17 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
                 h[k] = hs.x;
                 h[k + 1] = hs.y;
             }
-            if (a.r_out)
+            if (a.r_out && mine)
                 st16_if(a.r_out + base + (int64_t)c * 8, pack8<DT>(h),
                         FULL || (row_ok && (SEG ? c >= cb && c < cend : c < nchunks)));
+        }
+        if (!mine) {
+#pragma unroll
+            for (int k = 0; k < 8; k += 2) {
+                const float2 hp = make_float2(h[k], h[k + 1]);
+                ss2 = __ffma2_rn(hp, hp, ss2);
+            }
+            continue;
         }
         load8<DT>(ld_smem16(slot(v, NIN - 1)), wf);
 #pragma unroll

@@ -10,7 +10,7 @@ namespace sgq {
 
 // Launch geometry of one call: `nv` chunks per thread, `tpr` threads per row,
 // `rpc` rows per CTA, `grid` CTAs (times `seg` column segments a row, the
-// grid's second dimension, for the SwiGLU launches that split rows).
+// grid's second dimension, for the launches that split rows).
 struct Plan {
     int nv;
     int tpr;
@@ -19,22 +19,31 @@ struct Plan {
     bool full;   // W/8 == tpr * nv and M % rpc == 0: no bounds checks needed
     int sms;     // multiprocessors of the device (0 if unknown)
     int seg = 1;
+    int device = -1;   // the current device, for the per-device kernel attributes
 };
 
 // Pick a plan for M rows of width W (W % 8 == 0). Returns false when W needs
 // more than kMaxTPR threads per row.
 bool plan_rows(int64_t M, int W, int sm_count, Plan* p);
 
+// Kernels above 48 KB of static plus dynamic shared memory must opt in once
+// per device; the library records the largest opt-in given to each kernel on
+// each device, so that a launch calls cudaFuncSetAttribute only the first time
+// it needs more than was granted before (a mutex-guarded table lookup else).
+cudaError_t ensure_dynamic_smem(const void* kernel, int device, int bytes);
+
 // Launch kernel k on `stream` with programmatic stream serialisation: the
 // grid may begin launching while the preceding kernel on the stream finishes
-// (the kernels wait in pdl_wait() before touching memory).
+// (the kernels wait in pdl_wait() before touching memory the preceding grid
+// may write). The result is cudaLaunchKernelEx's own, which reports the
+// configuration and launch errors of this launch; a sticky or pending error
+// left on the thread by unrelated work is neither read nor cleared.
 template <typename Args>
 cudaError_t launch_pdl(void (*k)(const Args), const Plan& p, const Args& a, cudaStream_t stream,
                        int dynamic_smem = 0) {
-    // Above 48 KB of static plus dynamic shared memory a kernel must opt in
-    // (static use here is a few hundred bytes).
+    // (static shared memory here is a few hundred bytes)
     if (dynamic_smem > 40 * 1024) {
-        const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, dynamic_smem);
+        const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(k), p.device, dynamic_smem);
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};
@@ -47,8 +56,7 @@ cudaError_t launch_pdl(void (*k)(const Args), const Plan& p, const Args& a, cuda
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k, a);
-    return e != cudaSuccess ? e : cudaGetLastError();
+    return cudaLaunchKernelEx(&cfg, k, a);
 }
 
 // dt: DT_BF16 or DT_F16, the 16-bit activation type.

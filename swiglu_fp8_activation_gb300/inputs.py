@@ -47,25 +47,58 @@ def _stream_base(seed: int, tag: int) -> np.uint64:
     return _mix(key * _GAMMA + _GAMMA)[0]
 
 
-def words(n: int, seed: int, tag: int) -> np.ndarray:
-    """n consecutive SplitMix64 outputs of stream (seed, tag)."""
-    base = _stream_base(seed, tag)
-    idx = np.arange(1, n + 1, dtype=np.uint64)
+_CHUNK = 1 << 18          # draws per piece: keeps every temporary in cache
+
+
+def _pieces(n: int, fill) -> np.ndarray:
+    """An array of n draws filled piece by piece by fill(out_slice, start, stop)
+    on a few host threads (numpy releases the interpreter lock inside its
+    loops). Every draw depends on its index alone, so the result does not
+    depend on the piece size or the thread count."""
+    out = np.empty(n, dtype=np.float64)
+    starts = range(0, n, _CHUNK)
+    if n <= 4 * _CHUNK:
+        for a in starts:
+            fill(out, a, min(a + _CHUNK, n))
+        return out
+    import concurrent.futures as cf
+    import os
+    with cf.ThreadPoolExecutor(min(16, os.cpu_count() or 1)) as ex:
+        list(ex.map(lambda a: fill(out, a, min(a + _CHUNK, n)), starts))
+    return out
+
+
+def _words_at(base: np.uint64, first: int, count: int) -> np.ndarray:
+    """SplitMix64 outputs number first .. first + count - 1 of a stream."""
+    idx = np.arange(first, first + count, dtype=np.uint64)
     with np.errstate(over="ignore"):
         return _mix(base + idx * _GAMMA)
 
 
+def words(n: int, seed: int, tag: int) -> np.ndarray:
+    """n consecutive SplitMix64 outputs of stream (seed, tag)."""
+    return _words_at(_stream_base(seed, tag), 1, n)
+
+
 def uniform(n: int, seed: int, tag: int) -> np.ndarray:
     """n uniforms in [0, 1) from the top 53 bits of each word."""
-    return (words(n, seed, tag) >> np.uint64(11)).astype(np.float64) * _TWO_NEG53
+    base = _stream_base(seed, tag)
+
+    def fill(out, a, b):
+        out[a:b] = (_words_at(base, a + 1, b - a) >> np.uint64(11)).astype(np.float64) * _TWO_NEG53
+    return _pieces(n, fill)
 
 
 def normal(n: int, seed: int, tag: int) -> np.ndarray:
     """n standard normals by Box-Muller (cosine branch), two words per draw."""
-    w = words(2 * n, seed, tag)
-    u1 = ((w[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * _TWO_NEG53  # (0, 1]
-    u2 = (w[1::2] >> np.uint64(11)).astype(np.float64) * _TWO_NEG53  # [0, 1)
-    return np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2)
+    base = _stream_base(seed, tag)
+
+    def fill(out, a, b):
+        w = _words_at(base, 2 * a + 1, 2 * (b - a))
+        u1 = ((w[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * _TWO_NEG53  # (0, 1]
+        u2 = (w[1::2] >> np.uint64(11)).astype(np.float64) * _TWO_NEG53  # [0, 1)
+        out[a:b] = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2)
+    return _pieces(n, fill)
 
 
 def to_bf16(a: np.ndarray) -> torch.Tensor:

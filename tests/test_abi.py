@@ -37,7 +37,8 @@ def _header_value(name):
 def test_library_exports_every_declared_function(sgq_lib):
     names = _declared_functions()
     assert set(names) == {"rmsnorm_add_quant", "swiglu_quant", "rmsnorm_add", "swiglu", "quantize_fp8",
-                          "rmsnorm_dual_quant", "sgq_status_string", "sgq_abi_version", "sgq_launch_error"}
+                          "rmsnorm_dual_quant", "sgq_status_string", "sgq_abi_version", "sgq_launch_error",
+                          "sgq_set_sm_budget"}
     for n in names:
         assert hasattr(sgq_lib, n), n
     m = re.search(r"#define SGQ_ABI_VERSION (\d+)", _header())
@@ -61,6 +62,11 @@ def test_enum_and_flag_values_agree():
 def test_launch_error_text_without_a_failure(sgq_lib):
     sgq_lib.sgq_launch_error.restype = C.c_char_p
     assert sgq_lib.sgq_launch_error() == b"no launch error"
+
+
+def test_sm_budget_rejects_a_negative_count(sgq_lib):
+    assert sgq_lib.sgq_set_sm_budget(-1) == 1
+    assert sgq_lib.sgq_set_sm_budget(0) == 0
 
 
 def test_status_strings(sgq_lib):

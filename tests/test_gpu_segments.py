@@ -275,3 +275,59 @@ def test_split_launches_chained():
         torch.cuda.synchronize()
         assert torch.equal(r, ref["r"][k]) and torch.equal(q, ref["q"][k]) and torch.equal(s, ref["s"][k])
         assert torch.equal(n, ref["n"][k])
+
+
+def test_forced_segments_with_swizzled_scales():
+    # The swizzled E8M0 layout pads the rows to 128, which never splits on a
+    # 152-SM device. Planning for 4096 multiprocessors (sgq_set_sm_budget)
+    # splits them: the norm in 8 segments (its segments need W/32 % 16 == 0),
+    # and SwiGLU at I = 2240 (70 groups, 70 % 4 == 2) in 2, whose second
+    # segment holds the last group, which completes its tile row with zero
+    # codes. Each must equal bit for bit what the unsplit launches give.
+    from swiglu_fp8_activation_gb300 import set_sm_budget
+    budget, M, H, I = 4096, 50, 4096, 2240
+    assert _norm_segments(128, H, budget) == 8 and _norm_segments(128, H, _sms()) == 1
+    assert _segments("mxfp8", 128, I, budget) == 2 and (I // 32) % 4 == 2
+    t = inputs.norm_inputs(M, H, seed=50, x_std=3.0, r_std=1.0, w_mean=0.0, w_std=0.1)
+    x, r, w = (t[k].to(DEV) for k in ("x", "r", "w"))
+    gu = _gate_up(M, I, seed=2240)
+    sraw, s, sn = _guarded(scale_shape("mxfp8", M, H, "swizzled"), torch.uint8)
+    ro = torch.empty_like(r)
+    araw, a_s, an = _guarded(scale_shape("mxfp8", M, I, "swizzled"), torch.uint8)
+    try:
+        set_sm_budget(budget)
+        q, _, n, _ = rmsnorm_add_quant(x, w, residual_in=r, residual_out=ro, scale_out=s, normed=True,
+                                       scale_layout="swizzled")
+        r2 = r.clone()   # in place: never split, same plan otherwise
+        q2, s2, n2, _ = rmsnorm_add_quant(x, w, residual_in=r2, normed=True, scale_layout="swizzled")
+        aq, _ = swiglu_quant(gu.to(DEV), scale_out=a_s, scale_layout="swizzled")
+        torch.cuda.synchronize()
+    finally:
+        set_sm_budget(0)
+    aq_row, as_row = swiglu_quant(gu.to(DEV))            # the device's own plan: unsplit, row-major
+    torch.cuda.synchronize()
+    assert (sraw[sn:] == 0xFF).all() and (araw[an:] == 0xFF).all(), "bytes written past a scale buffer"
+    assert torch.equal(q, q2) and torch.equal(s, s2) and torch.equal(n, n2) and torch.equal(ro, r2)
+    assert torch.equal(aq, aq_row)
+    np.testing.assert_array_equal(a_s.cpu().numpy(), oracle.scale_layout("mxfp8", as_row.cpu().numpy(), "swizzled"))
+    ref = oracle.rmsnorm_add_quant("mxfp8", _bits(t["x"]), _bits(t["r"]), _bits(t["w"]), eps=1e-6, gemma=True,
+                                   from_fp32=False, normed=True)
+    s_sw = s.cpu().numpy()
+    s_row = _unswizzle(s_sw, M, H // 32)
+    np.testing.assert_array_equal(s_sw, oracle.scale_layout("mxfp8", s_row, "swizzled"))   # padding is code 0
+    check_norm("mxfp8", ref, q.cpu().numpy(), s_row, _bits(n), _bits(ro), from_fp32=False)
+    ref2 = oracle.swiglu_quant("mxfp8", "swiglu_oai", _bits(gu), from_fp32=True)
+    check_swiglu("mxfp8", ref2, aq.cpu().numpy(), as_row.cpu().numpy(), from_fp32=True)
+
+
+def _unswizzle(flat, M, G):
+    """Row-major [M, G] codes read back out of the swizzled [Mp, Gp] buffer."""
+    flat = np.asarray(flat).reshape(-1)
+    Gp = -(-G // 4) * 4
+    out = np.zeros((M, G), dtype=flat.dtype)
+    for r in range(M):
+        for g in range(G):
+            tile = (r // 128) * (Gp // 4) + g // 4
+            rr = r % 128
+            out[r, g] = flat[tile * 512 + (rr % 32) * 16 + (rr // 32) * 4 + g % 4]
+    return out

@@ -73,7 +73,7 @@ def test_checker_accepts_one_ulp_and_one_rare_step():
     assert st["code_mismatch"] == 1
 
 
-def test_ties_do_not_count_but_must_be_within_one_step():
+def test_ties_count_toward_the_budget_and_must_be_within_one_step():
     # fp32-source 1x128 norm with plain weights: exact ties are common
     case = inputs.norm_case_block128(64, 4096)
     t = inputs.make_norm(case)
@@ -81,11 +81,42 @@ def test_ties_do_not_count_but_must_be_within_one_step():
                                    eps=case.eps, gemma=False, from_fp32=True)
     tie = (ref["amb"] & oracle.AMB_TIE) != 0
     assert tie.sum() > 30          # about 4e-4 of the elements
-    q = ref["q"].copy()
-    idx = np.flatnonzero(tie & ((q & 0x7F) > 8) & ((q & 0x7F) < 0x7E))
-    q.flat[idx] += 1               # flip every tie by one step: still accepted
+    q0 = ref["q"].copy()
+    idx = np.flatnonzero(tie & ((q0 & 0x7F) > 8) & ((q0 & 0x7F) < 0x7E))
+    budget = int(1e-4 * q0.size)   # 26 of 262144
+    q = q0.copy()
+    q.flat[idx[:budget]] += 1      # ties flipped by one step, within the budget: accepted and counted
     st = check_norm("block128", ref, q, ref["scale"], from_fp32=True)
-    assert st["tie_mismatch"] == idx.size and st["code_mismatch"] == 0
-    q.flat[idx[0]] += 1            # two steps at a tie: rejected
+    assert st["tie_mismatch"] == budget and st["code_mismatch"] == budget
+    q = q0.copy()
+    q.flat[idx] += 1               # every tie flipped: above 1e-4, rejected
     with pytest.raises(AssertionError):
         check_norm("block128", ref, q, ref["scale"], from_fp32=True)
+    st = check_norm("block128", ref, q, ref["scale"], from_fp32=True, budget=False)
+    assert st["code_mismatch"] == idx.size and st["n_plain"] == q0.size
+    q = q0.copy()
+    q.flat[idx[0]] += 2            # two steps at a tie: rejected
+    with pytest.raises(AssertionError):
+        check_norm("block128", ref, q, ref["scale"], from_fp32=True, budget=False)
+
+
+def test_full_row_blocks_apply_the_budget_to_the_totals():
+    import fullrows
+    gu = inputs.bf16_bits(inputs.swiglu_inputs(600, 256, seed=4, std=2.0))
+    ref = oracle.swiglu_quant("mxfp8", "swiglu_oai", gu, from_fp32=True, diagnostics=False)
+    q0 = ref["q"]
+    st = fullrows.swiglu_all_rows("mxfp8", "swiglu_oai", gu, q0, ref["scale"], from_fp32=True)
+    assert st["code_mismatch"] == 0 and st["n_plain"] <= q0.size
+    ok = np.flatnonzero(((q0 & 0x7F) > 8) & ((q0 & 0x7F) < 0x7E))
+    allowed = int(1e-4 * st["n_plain"])                 # 15 of 153600
+    # one step off in two row blocks: within the budget over all rows, though
+    # one block alone holds more than 1e-4 of its own elements
+    first = ok[ok < 256 * 256][:allowed - 2]
+    last = ok[ok >= 512 * 256][:2]
+    q = q0.copy()
+    q.flat[np.r_[first, last]] += 1
+    st = fullrows.swiglu_all_rows("mxfp8", "swiglu_oai", gu, q, ref["scale"], from_fp32=True)
+    assert st["code_mismatch"] == allowed
+    q.flat[ok[ok >= 256 * 256][:20]] += 1               # over the budget in total: rejected
+    with pytest.raises(AssertionError):
+        fullrows.swiglu_all_rows("mxfp8", "swiglu_oai", gu, q, ref["scale"], from_fp32=True)
