@@ -15,7 +15,9 @@ Tolerances:
     Elements the oracle marks as ties (fp32-source FP8 formats: y/s within
     2^-22 of an E4M3 midpoint, where either neighbour is a correct rounding)
     count toward the 1e-4 like any other element; their mismatches are also
-    reported on their own (`tie_mismatch`).
+    reported on their own (`tie_mismatch`). A test may name an explicit
+    allowance of tie mismatches beyond the budget (`tie_allowance`, an
+    element count) where the budget is under one element.
 The check also counts mismatches at elements the oracle did not flag as near
 a rounding boundary (`unflagged`), a stricter signal reported in the stats.
 """
@@ -72,12 +74,16 @@ def _dequant(fmt: str, q: np.ndarray, scale: np.ndarray, gs: int) -> np.ndarray:
     return vals * np.repeat(s, gs, axis=1)
 
 
-def check_quant(fmt: str, ref: dict, q: np.ndarray, scale: np.ndarray, from_fp32: bool, budget: bool = True) -> dict:
+def check_quant(fmt: str, ref: dict, q: np.ndarray, scale: np.ndarray, from_fp32: bool, budget: bool = True,
+                tie_allowance: int = 0) -> dict:
     """Compare codes and scales with the oracle result `ref` (same rows).
 
     budget=False leaves out the 1e-4 fraction test (every other test still
     applies), for callers that check the fraction over several row blocks
-    at once from the returned counts `code_mismatch` and `n_plain`."""
+    at once from the returned counts `code_mismatch` and `n_plain`.
+    tie_allowance: an explicit number of mismatches allowed beyond the 1e-4
+    budget, all of which must lie at elements the oracle marks as ties (for
+    cases so small that the budget is under one element); 0 by default."""
     q = np.asarray(q)
     scale = np.asarray(scale)
     M, W = ref["q"].shape
@@ -122,8 +128,11 @@ def check_quant(fmt: str, ref: dict, q: np.ndarray, scale: np.ndarray, from_fp32
     frac = float(mism.sum()) / max(n_plain, 1)
     stats["tie_mismatch"] = int((mism & tie).sum())
     if budget:
-        assert frac <= MAX_CODE_MISMATCH_FRACTION, \
-            f"E4M3 mismatch fraction {frac:.2e} > 1e-4 ({int(mism.sum())} of {n_plain}, {stats['tie_mismatch']} at ties)"
+        n_mism, n_tie = int(mism.sum()), stats["tie_mismatch"]
+        over = n_mism - MAX_CODE_MISMATCH_FRACTION * n_plain
+        ok = over <= 0 or (over <= tie_allowance and n_mism - n_tie <= MAX_CODE_MISMATCH_FRACTION * n_plain
+                           and n_tie >= over)
+        assert ok, f"E4M3 mismatch fraction {frac:.2e} > 1e-4 ({n_mism} of {n_plain}, {n_tie} at ties)"
     if excused.any():
         dq_ref = _dequant(fmt, ref["q"], rs, gs)
         dq = _dequant(fmt, q, scale, gs)
@@ -144,8 +153,8 @@ def _scale_values(fmt: str, s: np.ndarray) -> np.ndarray:
 
 
 def check_norm(fmt: str, ref: dict, q, scale, normed_bits=None, residual_bits=None, *, from_fp32: bool,
-               budget: bool = True) -> dict:
-    stats = check_quant(fmt, ref, q, scale, from_fp32, budget)
+               budget: bool = True, tie_allowance: int = 0) -> dict:
+    stats = check_quant(fmt, ref, q, scale, from_fp32, budget, tie_allowance)
     if residual_bits is not None:
         stats.update(check_bf16("residual", ref["residual"], np.asarray(residual_bits)))
     if normed_bits is not None:
@@ -153,5 +162,6 @@ def check_norm(fmt: str, ref: dict, q, scale, normed_bits=None, residual_bits=No
     return stats
 
 
-def check_swiglu(fmt: str, ref: dict, q, scale, *, from_fp32: bool, budget: bool = True) -> dict:
-    return check_quant(fmt, ref, q, scale, from_fp32, budget)
+def check_swiglu(fmt: str, ref: dict, q, scale, *, from_fp32: bool, budget: bool = True,
+                 tie_allowance: int = 0) -> dict:
+    return check_quant(fmt, ref, q, scale, from_fp32, budget, tie_allowance)

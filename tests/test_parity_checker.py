@@ -120,3 +120,28 @@ def test_full_row_blocks_apply_the_budget_to_the_totals():
     q.flat[ok[ok >= 256 * 256][:20]] += 1               # over the budget in total: rejected
     with pytest.raises(AssertionError):
         fullrows.swiglu_all_rows("mxfp8", "swiglu_oai", gu, q, ref["scale"], from_fp32=True)
+
+
+def test_tie_allowance_admits_only_ties_beyond_the_budget():
+    # one fp32-source 1x128 row of 8192 elements (budget under one element) with four exact ties
+    t = inputs.norm_inputs(1, 8192, seed=0, x_std=1.0, r_std=None, w_mean=1.0, w_std=0.1)
+    ref = oracle.rmsnorm_add_quant("block128", inputs.bf16_bits(t["x"]), None, inputs.bf16_bits(t["w"]),
+                                   eps=1e-6, gemma=False, from_fp32=True)
+    q0 = ref["q"]
+    tie = (ref["amb"] & oracle.AMB_TIE) != 0
+    inner = ((q0 & 0x7F) > 8) & ((q0 & 0x7F) < 0x7E)
+    it, nt = np.flatnonzero(tie & inner), np.flatnonzero(~tie & inner)
+    assert it.size >= 2
+    q = q0.copy()
+    q.flat[it[0]] += 1             # one tie: over the budget without an allowance
+    with pytest.raises(AssertionError):
+        check_norm("block128", ref, q, ref["scale"], from_fp32=True)
+    st = check_norm("block128", ref, q, ref["scale"], from_fp32=True, tie_allowance=1)
+    assert st["tie_mismatch"] == 1
+    q.flat[it[1]] += 1             # two ties: beyond an allowance of one
+    with pytest.raises(AssertionError):
+        check_norm("block128", ref, q, ref["scale"], from_fp32=True, tie_allowance=1)
+    q = q0.copy()
+    q.flat[nt[0]] += 1             # one mismatch away from any tie: the allowance does not cover it
+    with pytest.raises(AssertionError):
+        check_norm("block128", ref, q, ref["scale"], from_fp32=True, tie_allowance=1)
