@@ -363,6 +363,16 @@ int swiglu_call(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float al
     a.klo = (float)(k - (double)a.khi);
     a.lim2 = lb | (lb << 16);
     a.nlim2 = a.lim2 ^ 0x80008000u;
+    a.tail2 = 0;
+    if (clamp16) {
+        // the least bf16 gate t with RN(khi t) <= 125, from the largest bf16
+        // not above 125 / khi (khi < 0) upwards: every gate >= t keeps the
+        // sigmoid's main formula in range, and only chunks holding a gate
+        // below t take the kernel's far-negative branch
+        uint32_t tb = bf16_bits_rn((float)(125.0 / (double)a.khi));
+        while (bf16_value(tb) * a.khi > 125.0f) tb = (tb & 0x8000u) ? tb - 1 : tb + 1;   // towards +inf
+        a.tail2 = tb | (tb << 16);
+    }
     return launched(sgq::launch_swiglu(fmt, plan, a, clamp16, static_cast<cudaStream_t>(stream)));
 }
 

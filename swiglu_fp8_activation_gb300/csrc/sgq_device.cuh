@@ -93,6 +93,15 @@ __device__ __forceinline__ void st16_if(void* p, uint4 v, bool pred) {
         "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"((int)pred));
 }
 
+// The same with the streaming (evict-first) cache policy, for an output that
+// no kernel soon after reads back, so that its lines leave L2 for memory
+// first and do not linger dirty into the next kernel's time.
+__device__ __forceinline__ void st16_cs_if(void* p, uint4 v, bool pred) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %5, 0;\n\t@p st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};\n}" ::"l"(p),
+        "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"((int)pred));
+}
+
 __device__ __forceinline__ void st8_if(void* p, uint2 v, bool pred) {
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %3, 0;\n\t@p st.global.v2.u32 [%0], {%1,%2};\n}" ::"l"(p),
                  "r"(v.x), "r"(v.y), "r"((int)pred));
@@ -312,6 +321,60 @@ __device__ __forceinline__ void sigmoid8(const float (&x)[8], float khi, float k
             }
         }
     }
+}
+
+// The same for gate values whose far-negative tail the caller detected on
+// the packed bf16 inputs: `rare` is true when some x may have
+// RN(khi x) > 125. Here x is not clamped from below, so where RN(khi x) > 125
+// the main formula may overflow (to inf or NaN); only those elements are
+// recomputed, as in sigmoid8, from max(x, xlo), xlo the x whose sigmoid
+// argument is kSigLo (below it the sigmoid is 0 in fp32). Every result equals
+// sigmoid8's for the argument max(x, xlo).
+__device__ __forceinline__ void sigmoid8_prechecked(const float (&x)[8], float khi, float klo, float xlo, bool rare,
+                                                    float (&out)[8]) {
+    float2 e[4], m[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 xv = make_float2(x[2 * i], x[2 * i + 1]);
+        const float2 qh = __fmul2_rn(xv, f2(khi));
+        const float2 nr = __ffma2_rn(xv, f2(-khi), qh);
+        const float2 nt = __ffma2_rn(xv, f2(-klo), nr);
+        m[i] = __fmul2_rn(nt, f2(-kLn2));
+        e[i] = make_float2(ex2_approx(qh.x), ex2_approx(qh.y));
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 E = __ffma2_rn(e[i], m[i], e[i]);
+        const float2 d = __fadd2_rn(E, f2(1.0f));
+        const float2 nd = __ffma2_rn(E, f2(-1.0f), f2(-1.0f));
+        const float2 r0 = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+        const float2 res = __ffma2_rn(nd, r0, f2(1.0f));
+        const float2 r = __ffma2_rn(r0, res, r0);
+        out[2 * i] = r.x;
+        out[2 * i + 1] = r.y;
+    }
+    if (rare) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float xc = fmaxf(x[j], xlo);
+            const float qh = xc * khi;
+            if (qh > 125.0f) {
+                const float nt = fmaf(xc, -klo, fmaf(xc, -khi, qh));
+                const float mj = nt * -kLn2;
+                const float v = ex2_approx(126.0f - qh);
+                out[j] = fmaf(v, -mj, v) * 0x1p-126f;
+            }
+        }
+    }
+}
+
+// True when either bf16 half of a is below the same half of b.
+__device__ __forceinline__ bool bf16x2_any_lt(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("{\n\t.reg .pred p, q;\n\tsetp.lt.bf16x2 p|q, %1, %2;\n\tor.pred p, p, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(a), "r"(b));
+    return r != 0;
 }
 
 // a / b rounded to nearest even, given r = RN(1/b) (b and r normal). q0 = a*r

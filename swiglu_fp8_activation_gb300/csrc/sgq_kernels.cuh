@@ -58,6 +58,7 @@ struct SwigluArgs {
     int act;
     float alpha, beta, limit;
     uint32_t lim2, nlim2;    // bf16x2 of limit and -limit (the CLAMP16 kernels)
+    uint32_t tail2;          // bf16x2 of the least gate t with RN(khi t) <= 125 (the CLAMP16 kernels)
     float khi, klo;          // -alpha log2(e) in two fp32 parts (OAI)
     int segc;                // chunks a column segment (I / 8 / gridDim.y)
 };
@@ -199,6 +200,14 @@ __host__ __device__ constexpr int norm_stage_bytes(bool has_res, int nv, int thr
     return nv * norm_stage_inputs(has_res) * threads * 16;
 }
 
+// Where the norm keeps z = h * w' between the row reduction and the output
+// pass: in registers (NV x 8 floats a thread across the reduction's barrier),
+// or written back over the thread's own x and weight slots in shared memory,
+// which frees those registers for more resident CTAs. The per-token format,
+// whose register count limited it to four 224-thread CTAs an SM, takes the
+// shared-memory form.
+__host__ __device__ constexpr bool norm_z_in_smem(int fmt) { return fmt == FMT_PT; }
+
 // The rows of CTA `blk` of one norm launch (blockDim.x = a.rpc * a.tpr).
 // FULL: every thread's chunks lie inside the row and every row inside M (the
 // plan divides both exactly), so no bounds are checked. DT is the 16-bit
@@ -265,6 +274,7 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
     const bool from32 = (a.flags & F_FROM_FP32) != 0;
     // w' = w + 1 (Gemma) or w + (-0), which is w exactly, signed zeros included
     const float w_add = (a.flags & F_GEMMA) ? 1.0f : -0.0f;
+    constexpr bool ZS = norm_z_in_smem(FMT);
     float z[NV][8];
     float2 ss2 = make_float2(0.0f, 0.0f);
     float zmax = 0.0f;
@@ -284,9 +294,11 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
                 h[k] = hs.x;
                 h[k + 1] = hs.y;
             }
+            // the updated residual is next read by the following layer's norm,
+            // after the sublayer in between: streamed out (evict-first)
             if (a.r_out && mine)
-                st16_if(a.r_out + base + (int64_t)c * 8, pack8<DT>(h),
-                        FULL || (row_ok && (SEG ? c >= cb && c < cend : c < nchunks)));
+                st16_cs_if(a.r_out + base + (int64_t)c * 8, pack8<DT>(h),
+                           FULL || (row_ok && (SEG ? c >= cb && c < cend : c < nchunks)));
         }
         if (!mine) {
 #pragma unroll
@@ -306,6 +318,10 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
             z[v][k] = zp.x;
             z[v][k + 1] = zp.y;
             if (FMT == FMT_PT) zmax = fmaxf(zmax, fmaxf(fabsf(zp.x), fabsf(zp.y)));
+        }
+        if (ZS) {   // over this thread's own x and weight slots of chunk v, both read above
+            *reinterpret_cast<float4*>(slot(v, 0)) = make_float4(z[v][0], z[v][1], z[v][2], z[v][3]);
+            *reinterpret_cast<float4*>(slot(v, NIN - 1)) = make_float4(z[v][4], z[v][5], z[v][6], z[v][7]);
         }
     }
     float ss = ss2.x + ss2.y;
@@ -345,10 +361,19 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
             // the row end) skip the chunk; c & ~31 is the same in every lane
             if (SEG && ((c & ~31) < cb || (c & ~31) >= cend)) continue;
             const bool ok = FULL || (row_ok && c < nchunks);
-            float y[8], src[8];
+            float y[8], src[8], zc[8];
+            if (ZS) {
+                const float4 lo = *reinterpret_cast<const float4*>(slot(v, 0));
+                const float4 hi = *reinterpret_cast<const float4*>(slot(v, NIN - 1));
+                zc[0] = lo.x, zc[1] = lo.y, zc[2] = lo.z, zc[3] = lo.w;
+                zc[4] = hi.x, zc[5] = hi.y, zc[6] = hi.z, zc[7] = hi.w;
+            } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) zc[k] = z[v][k];
+            }
 #pragma unroll
             for (int k = 0; k < 8; k += 2) {                   // z = 0 past the row end (zero-filled copies)
-                const float2 yp = __fmul2_rn(f2(inv), make_float2(z[v][k], z[v][k + 1]));
+                const float2 yp = __fmul2_rn(f2(inv), make_float2(zc[k], zc[k + 1]));
                 y[k] = yp.x;
                 y[k + 1] = yp.y;
             }
@@ -405,21 +430,25 @@ __global__ void __launch_bounds__(kMaxTPR) norm_dual_kernel(const DualArgs d) {
 // CLAMPED (OAI only): g and u arrive already clamped to limit (g' and u'),
 // and alpha > 0 with alpha * limit <= 2^100, so g' bounds the sigmoid's
 // argument from above (sigmoid8 is exact there for any argument below
-// 2^120) and only the lower clamp remains. (Clamping g from below on the
+// 2^120) and only the lower clamp remains; the caller has tested the packed
+// bf16 gates against the sigmoid's far-negative tail (`rare`), and the
+// lower clamp is applied only where that tail is reached. (Clamping g from below on the
 // packed bf16 words as well measured 8-17% slower at decode sizes: the
 // second dependent bf16x2 min/max lengthens the critical path.)
 template <int ACT, bool CLAMPED = false, bool ROUND = false>
 __device__ __forceinline__ void activation8(const float (&g)[8], const float (&u)[8], float khi, float klo,
-                                            float beta, float limit, float glo, float ghi, float (&a)[8]) {
+                                            float beta, float limit, float glo, float ghi, float (&a)[8],
+                                            bool rare = true) {
     float sg[8];
     if (ACT == ACT_OAI) {
         float gc[8], gs[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             gc[k] = CLAMPED ? g[k] : fminf(g[k], limit);
-            gs[k] = CLAMPED ? fmaxf(gc[k], glo) : fmaxf(fminf(gc[k], ghi), glo);
+            gs[k] = CLAMPED ? gc[k] : fmaxf(fminf(gc[k], ghi), glo);
         }
-        sigmoid8(gs, khi, klo, sg);                                     // sigmoid(alpha * gs)
+        if (CLAMPED) sigmoid8_prechecked(gs, khi, klo, glo, rare, sg);  // sigmoid(alpha * max(g', glo))
+        else sigmoid8(gs, khi, klo, sg);                                 // sigmoid(alpha * gs)
 #pragma unroll
         for (int k = 0; k < 8; k += 2) {
             const float2 uc = CLAMPED ? make_float2(u[k], u[k + 1])
@@ -455,15 +484,20 @@ __device__ __forceinline__ float2 oai_gate_range(float alpha) {
 // One chunk of gate and up from their shared-memory slots, widened to fp32;
 // with CLAMP16, g = min(g, limit) and u = clamp(u, -limit, limit) first, on
 // the packed bf16 pairs (exact: limit is a bf16 value).
+// `rare` (CLAMP16 only): some gate of the chunk lies below a.tail2, where
+// the sigmoid's argument reaches its far-negative tail (3 packed min and one
+// packed compare for the chunk instead of a test per element).
 template <bool CLAMP16>
 __device__ __forceinline__ void load_gate_up(const uint4* gs, const uint4* us, const SwigluArgs& a, float (&g)[8],
-                                             float (&u)[8]) {
+                                             float (&u)[8], bool& rare) {
     uint4 gw = ld_smem16(gs), uw = ld_smem16(us);
+    rare = true;
     if (CLAMP16) {
         gw = make_uint4(bf16x2_min(gw.x, a.lim2), bf16x2_min(gw.y, a.lim2), bf16x2_min(gw.z, a.lim2),
                         bf16x2_min(gw.w, a.lim2));
         uw = make_uint4(bf16x2_max(bf16x2_min(uw.x, a.lim2), a.nlim2), bf16x2_max(bf16x2_min(uw.y, a.lim2), a.nlim2),
                         bf16x2_max(bf16x2_min(uw.z, a.lim2), a.nlim2), bf16x2_max(bf16x2_min(uw.w, a.lim2), a.nlim2));
+        rare = bf16x2_any_lt(bf16x2_min(bf16x2_min(gw.x, gw.y), bf16x2_min(gw.z, gw.w)), a.tail2);
     }
     bf16x8_to_f32(gw, g);
     bf16x8_to_f32(uw, u);
@@ -527,10 +561,11 @@ __device__ __forceinline__ void swiglu_rows(const SwigluArgs& a) {
                 const int c = cb + t + v * tpr;
                 const bool ok = FULL || (row_ok && c < cend);
                 float g[8], u[8], src[8];
+                bool rare;
                 cp_async_wait_group_of<NV>(v);
                 load_gate_up<CLAMP16>(&stage[(2 * v) * nt + threadIdx.x], &stage[(2 * v + 1) * nt + threadIdx.x], a,
-                                      g, u);
-                activation8<ACT, CLAMP16, ROUND>(g, u, a.khi, a.klo, a.beta, a.limit, gr.x, gr.y, src);
+                                      g, u, rare);
+                activation8<ACT, CLAMP16, ROUND>(g, u, a.khi, a.klo, a.beta, a.limit, gr.x, gr.y, src, rare);
                 if (MODE == 0) {
                     st16_if(a.out + row * I + (int64_t)c * 8, f32x8_to_bf16x8(src), ok);
                 } else {
@@ -552,10 +587,11 @@ __device__ __forceinline__ void swiglu_rows(const SwigluArgs& a) {
 #pragma unroll
             for (int v = 0; v < NV; ++v) {
                 float g[8], u[8];
+                bool rare;
                 cp_async_wait_group_of<NV>(v);
                 load_gate_up<CLAMP16>(&stage[(2 * v) * nt + threadIdx.x], &stage[(2 * v + 1) * nt + threadIdx.x], a,
-                                      g, u);
-                activation8<ACT, CLAMP16, ROUND>(g, u, a.khi, a.klo, a.beta, a.limit, gr.x, gr.y, src[v]);
+                                      g, u, rare);
+                activation8<ACT, CLAMP16, ROUND>(g, u, a.khi, a.klo, a.beta, a.limit, gr.x, gr.y, src[v], rare);
 #pragma unroll
                 for (int k = 0; k < 8; k += 2) {
                     if (MODE == 2) {
