@@ -389,34 +389,111 @@ def decode_table(dev):
     return out
 
 
+L2_BYTES = 129 * 2 ** 20
+
+
+def _input_sets(nbytes: int, M: int) -> int:
+    """Input sets a measurement rotates over: one at decode sizes (inputs
+    resident in L2, as the pages' microbenchmark), else enough that the sets
+    together exceed 2.5 times the L2, so every launch reads its inputs from
+    HBM."""
+    return 1 if M < 1024 else max(3, -(-int(2.5 * L2_BYTES) // nbytes))
+
+
 def other_configs(dev):
     """µs per launch (CUDA-graph replay, as above) of the Qwen3-like 1x128 and
-    MLA-like per-token workloads."""
+    MLA-like per-token workloads. At M >= 1024 the graph's launches rotate
+    over input sets larger than L2 together."""
     import torch
 
     from swiglu_fp8_activation_gb300 import inputs, rmsnorm_add_quant, swiglu_quant
     res = {}
     w = inputs.workloads()
     for case in w["cfg3_block128"] + w["cfg4_per_token"]:
+        k = [0]
         if isinstance(case, inputs.NormCase):
             t = inputs.make_norm(case)
-            x, wt = t["x"].to(dev), t["w"].to(dev)
+            n_sets = _input_sets(t["x"].numel() * 2, case.M)
+            xs, wt = [t["x"].to(dev) for _ in range(n_sets)], t["w"].to(dev)
             q = torch.empty(case.M, case.H, dtype=torch.uint8, device=dev)
             shape = (case.M, 1) if case.fmt == "per_token" else (case.M, case.H // 128)
             s = torch.empty(shape, dtype=torch.float32, device=dev)
-            fn = (lambda x=x, wt=wt, q=q, s=s, c=case: rmsnorm_add_quant(
-                x, wt, fmt=c.fmt, eps=c.eps, gemma=c.gemma, quant_from_fp32=c.from_fp32, q_out=q, scale_out=s))
+
+            def fn(c=case, xs=xs, wt=wt, q=q, s=s):
+                x = xs[k[0] % len(xs)]
+                k[0] += 1
+                rmsnorm_add_quant(x, wt, fmt=c.fmt, eps=c.eps, gemma=c.gemma, quant_from_fp32=c.from_fp32,
+                                  q_out=q, scale_out=s)
             key, nbytes = f"{case.name}_W{case.H}_M{case.M}", norm_bytes(case.M, case.H, False, False, case.fmt)
         else:
-            gu = inputs.make_swiglu(case).to(dev)
+            g = inputs.make_swiglu(case)
+            n_sets = _input_sets(g.numel() * 2, case.M)
+            gus = [g.to(dev) for _ in range(n_sets)]
             q = torch.empty(case.M, case.I, dtype=torch.uint8, device=dev)
             s = torch.empty(case.M, case.I // 128, dtype=torch.float32, device=dev)
-            fn = (lambda gu=gu, q=q, s=s, c=case: swiglu_quant(
-                gu, fmt=c.fmt, act=c.act, quant_from_fp32=c.from_fp32, round_act_bf16=c.round_act_bf16,
-                q_out=q, scale_out=s))
+
+            def fn(c=case, gus=gus, q=q, s=s):
+                gu = gus[k[0] % len(gus)]
+                k[0] += 1
+                swiglu_quant(gu, fmt=c.fmt, act=c.act, quant_from_fp32=c.from_fp32,
+                             round_act_bf16=c.round_act_bf16, q_out=q, scale_out=s)
             key, nbytes = f"{case.name}_I{case.I}_M{case.M}", swiglu_bytes(case.M, case.I, case.fmt)
-        us = graph_us_per_launch(fn, iters=100, reps=10)
-        res[key] = {"us": round(us, 3), "GBps": round(nbytes / us / 1e3, 1)}
+        us = graph_us_per_launch(fn, iters=max(100, 3 * n_sets), reps=10)
+        res[key] = {"us": round(us, 3), "GBps": round(nbytes / us / 1e3, 1),
+                    "inputs": "resident in L2" if n_sets == 1 else f"rotated over {n_sets} sets (> L2)"}
+    return res
+
+
+def wide_rows(dev):
+    """µs per launch (graph replay, inputs rotated over sets larger than L2
+    together) of rows wider than one CTA covers, at M = 4096: RMSNorm +
+    per-token FP8 at W = 24576 (a cluster of two CTAs a row), add + Gemma
+    RMSNorm + MXFP8 + bf16 copy at H = 24576 (a cluster of two), and
+    SiLU-and-mul + 1x128 at I = 24576 (two column segments a row)."""
+    import torch
+
+    from swiglu_fp8_activation_gb300 import inputs, rmsnorm_add_quant, swiglu_quant
+    res = {}
+    M, W = 4096, 24576
+    k = [0]
+    t = inputs.norm_inputs(M, W, seed=24576, x_std=1.0, r_std=None, w_mean=1.0, w_std=0.1)
+    n_sets = _input_sets(M * W * 2, M)
+    xs, w = [t["x"].to(dev) for _ in range(n_sets)], t["w"].to(dev)
+    q = torch.empty(M, W, dtype=torch.uint8, device=dev)
+    s = torch.empty(M, 1, dtype=torch.float32, device=dev)
+
+    def pt():
+        rmsnorm_add_quant(xs[k[0] % n_sets], w, fmt="per_token", gemma=False, q_out=q, scale_out=s)
+        k[0] += 1
+    us = graph_us_per_launch(pt, iters=max(100, 3 * n_sets), reps=10)
+    nb = norm_bytes(M, W, False, False, "per_token")
+    res[f"rmsnorm_per_token_W{W}_M{M}"] = {"us": round(us, 3), "GBps": round(nb / us / 1e3, 1)}
+    del xs
+    t = inputs.norm_inputs(M, W, seed=24577, x_std=1.0, r_std=1.0, w_mean=0.0, w_std=0.1)
+    n_sets = _input_sets(M * W * 4, M)
+    xr = [(t["x"].to(dev), t["r"].to(dev)) for _ in range(n_sets)]
+    w = t["w"].to(dev)
+    ro, n = torch.empty(M, W, dtype=torch.bfloat16, device=dev), torch.empty(M, W, dtype=torch.bfloat16, device=dev)
+    s = torch.empty(M, W // 32, dtype=torch.uint8, device=dev)
+
+    def mx():
+        x, r = xr[k[0] % n_sets]
+        rmsnorm_add_quant(x, w, residual_in=r, residual_out=ro, q_out=q, scale_out=s, normed_out=n)
+        k[0] += 1
+    us = graph_us_per_launch(mx, iters=max(100, 3 * n_sets), reps=10)
+    res[f"gemma_add_rmsnorm_mxfp8_H{W}_M{M}"] = {"us": round(us, 3), "GBps": round(norm_bytes(M, W) / us / 1e3, 1)}
+    del xr, ro, n
+    g = inputs.swiglu_inputs(M, W, seed=24578, std=1.0)
+    n_sets = _input_sets(g.numel() * 2, M)
+    gus = [g.to(dev) for _ in range(n_sets)]
+    s = torch.empty(M, W // 128, dtype=torch.float32, device=dev)
+
+    def silu():
+        swiglu_quant(gus[k[0] % n_sets], fmt="block128", act="silu_mul", quant_from_fp32=False, round_act_bf16=True,
+                     q_out=q, scale_out=s)
+        k[0] += 1
+    us = graph_us_per_launch(silu, iters=max(100, 3 * n_sets), reps=10)
+    res[f"silu_mul_block128_I{W}_M{M}"] = {"us": round(us, 3), "GBps": round(swiglu_bytes(M, W, "block128") / us / 1e3, 1)}
     return res
 
 
@@ -652,6 +729,7 @@ def run_ours(args, world, rank, local):
         decode = decode_table(dev) if rank == 0 and not args.quick else None
         others = other_configs(dev) if rank == 0 and not args.quick else None
         qkv = qkv_norm_configs(dev) if rank == 0 and not args.quick else None
+        wide = wide_rows(dev) if rank == 0 and not args.quick else None
     total_ms = max_over_ranks(total_ms, world)
     alone_steps = max(args.steps, 200)
     norm_alone_us = time_alone(pf, "norm", alone_steps)
@@ -696,6 +774,7 @@ def run_ours(args, world, rank, local):
         "decode_us_per_launch": decode,
         "other_configs": others,
         "qkv_latent_norm_us": qkv,
+        "wide_rows_us": wide,
         "e2e": {"value": round(sb / (e2e_ms * 1e-3) / 1e9 * world, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 3),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * args.steps,
@@ -716,16 +795,18 @@ def run_profile(args):
     launches. norm / swiglu: the M=8192 prefill workload (inputs > L2,
     rotated). pertoken: RMSNorm + per-token FP8 at W=7168, M=4096 (three
     rotating input sets, 176 MB together). silu128: SiLU-and-mul + 1x128
-    (bf16 roundings) at I=12288, M=2048 (three sets, 302 MB together).
+    (bf16 roundings) at I=12288, M=2048 (three sets, 302 MB together);
+    silu128_m256 the same at M=256 and norm128_m256 RMSNorm + 1x128 (fp32
+    source) at W=4096, M=256 (the Qwen3-like workload's largest M).
     norm8: the decode norm (add + Gemma RMSNorm + MXFP8 + bf16 copy, separate
     residual output) at M=8, H=6144, inputs resident in L2; norm8_inplace:
     the same with the residual updated in place (whole rows, one CTA each)."""
     import torch
     dev = torch.device("cuda", 0)
-    if args.profile == "silu128":
+    if args.profile in ("silu128", "silu128_m256"):
         from swiglu_fp8_activation_gb300 import inputs, library
         import ctypes as C
-        M, I = 2048, 12288
+        M, I = (2048 if args.profile == "silu128" else 256), 12288
         gu = inputs.swiglu_inputs(M, I, seed=2, std=1.0)
         sets = [gu.to(dev) for _ in range(ROTATE)]
         q = torch.empty(M, I, dtype=torch.uint8, device=dev)
@@ -754,20 +835,23 @@ def run_profile(args):
         fn = lib.rmsnorm_add_quant
         nbytes = norm_bytes(case.M, case.H)
         get = lambda k: args1
-    elif args.profile == "pertoken":
+    elif args.profile in ("pertoken", "norm128_m256"):
         from swiglu_fp8_activation_gb300 import inputs, library
-        case = inputs.norm_case_per_token(4096, 7168)
+        pt = args.profile == "pertoken"
+        case = inputs.norm_case_per_token(4096, 7168) if pt else inputs.norm_case_block128(256)
         t = inputs.make_norm(case)
         sets = [(t["x"].to(dev), t["w"].to(dev)) for _ in range(ROTATE)]
         q = torch.empty(case.M, case.H, dtype=torch.uint8, device=dev)
-        sc = torch.empty(case.M, 1, dtype=torch.float32, device=dev)
+        sc = torch.empty(case.M, 1 if pt else case.H // 128, dtype=torch.float32, device=dev)
         import ctypes as C
         lib = library()
         stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
-        arglist = [(2, 0, case.M, case.H, case.eps, C.c_void_p(x.data_ptr()), None, None, C.c_void_p(w.data_ptr()),
-                    C.c_void_p(q.data_ptr()), C.c_void_p(sc.data_ptr()), None, stream) for x, w in sets]
+        flags = 0 if pt else 2                      # 1x128 quantised from the fp32 normed value
+        arglist = [(2 if pt else 1, flags, case.M, case.H, case.eps, C.c_void_p(x.data_ptr()), None, None,
+                    C.c_void_p(w.data_ptr()), C.c_void_p(q.data_ptr()), C.c_void_p(sc.data_ptr()), None, stream)
+                   for x, w in sets]
         fn, pick = lib.rmsnorm_add_quant, None
-        nbytes = norm_bytes(case.M, case.H, False, False, "per_token")
+        nbytes = norm_bytes(case.M, case.H, False, False, case.fmt)
         get = lambda k: arglist[k % ROTATE]
     else:
         pf = Prefill(dev)
@@ -798,7 +882,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle time")
     ap.add_argument("--quick", action="store_true", help="skip the decode and other-config tables")
-    ap.add_argument("--profile", choices=("norm", "swiglu", "pertoken", "silu128", "norm8", "norm8_inplace"),
+    ap.add_argument("--profile", choices=("norm", "swiglu", "pertoken", "silu128", "silu128_m256", "norm128_m256",
+                                          "norm8", "norm8_inplace"),
                     help="time one kernel only (for ncu)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -81,8 +81,13 @@
 extern "C" {
 #endif
 
-#define SGQ_ABI_VERSION 2
-#define SGQ_MAX_WIDTH 16384
+#define SGQ_ABI_VERSION 3
+/* Widest row: rows up to 16384 columns run one CTA a row (or several, each a
+ * column segment, at small M); wider rows run as a cluster of up to 8 CTAs,
+ * or as column segments where no row-wide value is needed. */
+#define SGQ_MAX_WIDTH 131072
+/* Widest segment of rmsnorm_dual_quant (one CTA a row). */
+#define SGQ_MAX_DUAL_WIDTH 16384
 
 /* Quantisation format of the output activation. */
 typedef enum sgq_format {
@@ -132,7 +137,7 @@ typedef enum sgq_act {
 typedef enum sgq_status {
     SGQ_OK = 0,
     SGQ_ERR_INVALID_ARG = 1,    /* NULL required pointer, bad enum/flag, negative size, overlap */
-    SGQ_ERR_UNSUPPORTED = 2,    /* width not a multiple of the group, or above SGQ_MAX_WIDTH */
+    SGQ_ERR_UNSUPPORTED = 2,    /* width not a multiple of the group, or above the widest row */
     SGQ_ERR_MISALIGNED = 3,     /* a pointer breaks the alignment rule above */
     SGQ_ERR_LAUNCH = 4          /* the CUDA launch failed */
 } sgq_status_t;
@@ -304,7 +309,7 @@ typedef struct sgq_norm_seg {
  *   eps           >= 0, finite
  *   seg_a, seg_b  host pointers to the two segments (read during the call
  *                 only); H a multiple of the format's group when the segment
- *                 is quantised, else of 8; H <= SGQ_MAX_WIDTH
+ *                 is quantised, else of 8; H <= SGQ_MAX_DUAL_WIDTH
  *   stream        the stream to launch on
  */
 int rmsnorm_dual_quant(int fmt, uint32_t flags, int64_t M, float eps, const sgq_norm_seg_t* seg_a,

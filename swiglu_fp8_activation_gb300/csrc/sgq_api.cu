@@ -188,6 +188,45 @@ bool plan_launch(int64_t M, int W, const sgq::ScaleOut& so, const Device& dev, s
     return true;
 }
 
+// Chunks (8 columns) one CTA of the row engine covers: kMaxTPR threads with
+// kMaxNV chunks each, 16384 columns.
+constexpr int kCtaChunks = sgq::kMaxTPR * sgq::kMaxNV;
+
+// A row of nch > kCtaChunks chunks split over a thread block cluster: the
+// fewest CTAs that cover it (at most kMaxCluster), each taking segc chunks,
+// a multiple of 32 (whole warps, whole scale groups), the last possibly
+// fewer; kMaxNV chunks a thread. False when the row needs more CTAs than a
+// cluster holds.
+bool plan_cluster(int64_t rows, int nch, const Device& dev, sgq::Plan* p, int* segc) {
+    int cs = (nch + kCtaChunks - 1) / kCtaChunks;
+    if (cs > sgq::kMaxCluster) return false;
+    const int sc = (int)round_up((nch + cs - 1) / cs, 32);
+    cs = (nch + sc - 1) / sc;
+    p->nv = sgq::kMaxNV;
+    p->tpr = (int)round_up((sc + sgq::kMaxNV - 1) / sgq::kMaxNV, 32);
+    p->rpc = 1;
+    p->grid = rows * cs;
+    p->full = false;
+    p->sms = dev.sms;
+    p->seg = 1;
+    p->device = dev.id;
+    p->cluster = cs;
+    *segc = sc;
+    return p->grid <= 0x7FFFFFFF;
+}
+
+// Column segments (the grid's second dimension) for rows of nch chunks,
+// wider than one CTA covers, in a format whose groups are gch chunks and have
+// nothing row-wide: the fewest segments that fit a CTA each, at least
+// `min_seg`, each a whole number of groups, the last possibly fewer.
+int wide_segments(int nch, int gch, int min_seg, int* segc) {
+    int s = (nch + kCtaChunks - 1) / kCtaChunks;
+    if (s < min_seg) s = min_seg;
+    const int sc = (int)round_up((nch + s - 1) / s, gch);
+    *segc = sc;
+    return (nch + sc - 1) / sc;
+}
+
 struct Span {
     const void* p;
     size_t n;
@@ -255,16 +294,24 @@ int norm_call(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, const vo
                           {r_out_span, act}};
     if (any_overlap(spans, 7)) return SGQ_ERR_INVALID_ARG;
 
-    // Rows too few to fill the device are split into column segments, except
-    // for an in-place residual update (another CTA of the row reads r back).
+    // Rows wider than one CTA covers run as a cluster of CTAs a row. Rows too
+    // few to fill the device are split into column segments, except for an
+    // in-place residual update (another CTA of the row reads r back).
     const Device dev = current_device();
     const int sms = dev.sms;
-    const int seg = residual_out && residual_out == residual_in ? 1 : norm_segments(so.Ms, H, sms);
     sgq::Plan plan;
-    if (!sgq::plan_rows(so.Ms, (int)H, sms, &plan)) return SGQ_ERR_UNSUPPORTED;
-    plan.device = dev.id;
-    plan.full = plan.full && so.Ms == M && seg == 1;   // the exact-fit kernels write whole rows
-    plan.seg = seg;
+    int segc = (int)(H / 8);
+    const bool wide = H / 8 > kCtaChunks;
+    if (wide) {
+        if (!plan_cluster(so.Ms, (int)(H / 8), dev, &plan, &segc)) return SGQ_ERR_UNSUPPORTED;
+    } else {
+        const int seg = residual_out && residual_out == residual_in ? 1 : norm_segments(so.Ms, H, sms);
+        if (!sgq::plan_rows(so.Ms, (int)H, sms, &plan)) return SGQ_ERR_UNSUPPORTED;
+        plan.device = dev.id;
+        plan.full = plan.full && so.Ms == M && seg == 1;   // the exact-fit kernels write whole rows
+        plan.seg = seg;
+        segc = (int)(H / 8 / seg);
+    }
     sgq::NormArgs a;
     a.x = static_cast<const uint16_t*>(x);
     a.r_in = static_cast<const uint16_t*>(residual_in);
@@ -281,23 +328,44 @@ int norm_call(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, const vo
     a.rpc = plan.rpc;
     a.eps = eps;
     a.flags = flags;
-    a.segc = (int)(H / 8 / seg);
-    return launched(sgq::launch_norm(fmt, dt_of(flags), plan, a, static_cast<cudaStream_t>(stream)));
+    a.segc = segc;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return launched(wide ? sgq::launch_norm_cluster(fmt, dt_of(flags), plan, a, st)
+                         : sgq::launch_norm(fmt, dt_of(flags), plan, a, st));
 }
 
 // Column segments a row for a SwiGLU launch over `rows` rows (the grid's
-// second dimension): while twice the CTAs still fit on the device at one a
-// multiprocessor, a row is split in two, up to 16 segments, each a whole
-// number of scale groups and at least 512 columns. At small M this spreads a
-// wide row's activation arithmetic (two special-function operations an
-// element) over up to 16 multiprocessors instead of one. (Allowing two CTAs
-// an SM measured slower.) The per-token format needs the row's amax and is
-// never split.
+// second dimension), each a whole number of scale groups and at least 512
+// columns, at most 16:
+//  * few rows: while twice the CTAs still fit on the device at one a
+//    multiprocessor, a row is split in two. This spreads a wide row's
+//    activation arithmetic (two special-function operations an element)
+//    over up to 16 multiprocessors instead of one. (Allowing two CTAs an SM
+//    measured slower.)
+//  * between half a wave and two waves of rows: the split whose busiest
+//    multiprocessor holds the least work (CTAs on it / segments a row), if it
+//    beats the whole rows by more than 1/16: SiLU-and-mul at I = 12288 went
+//    from 5.04 to 4.03 us at M = 192 (4 segments) and from 5.08 to 4.85 us at
+//    M = 256; beyond two waves it measured no better or worse.
+// The per-token format needs the row's amax and is never split.
 int swiglu_segments(int fmt, int64_t rows, int64_t I, int sms) {
     if (fmt == SGQ_FMT_FP8_PER_TOKEN || sms <= 0) return 1;
     const int64_t nch = I / 8, gch = fmt == SGQ_FMT_FP8_BLOCK128 ? 16 : 4;   // chunks a row, a scale group
     int s = 1;
     while (s < 16 && rows * 2 * s <= sms && nch % (2 * s * gch) == 0 && nch / (2 * s) >= 64) s *= 2;
+    if (s == 1 && rows > sms / 2 && rows <= 2 * (int64_t)sms) {
+        int64_t best_ctas = (rows + sms - 1) / sms;   // CTAs on the busiest SM, each 1/best_s of a row
+        int best_s = 1;
+        for (int c = 2; c <= 16; c *= 2) {
+            if (nch % (c * gch) != 0 || nch / c < 64) break;
+            const int64_t per = (rows * c + sms - 1) / sms;
+            if (per * best_s * 16 < best_ctas * c * 15) {
+                best_ctas = per;
+                best_s = c;
+            }
+        }
+        s = best_s;
+    }
     return s;
 }
 
@@ -327,15 +395,26 @@ int swiglu_call(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float al
                           {out, (size_t)M * I * 2}};
     if (any_overlap(spans, 4)) return SGQ_ERR_INVALID_ARG;
 
-    // Rows too few to fill the device are split into column segments.
+    // Rows too few to fill the device are split into column segments, and so
+    // are rows wider than one CTA covers; per-token rows that wide run as a
+    // cluster of CTAs a row (the row's amax is combined across it).
     const Device dev = current_device();
     const int sms = dev.sms;
-    const int seg = swiglu_segments(fmt, so.Ms, I, sms);
+    const int nch = (int)(I / 8);
     sgq::Plan plan;
-    if (!sgq::plan_rows(so.Ms, (int)(I / seg), sms, &plan)) return SGQ_ERR_UNSUPPORTED;
-    plan.device = dev.id;
-    plan.full = plan.full && so.Ms == M && seg == 1;   // the exact-fit kernels run whole rows
-    plan.seg = seg;
+    int segc = nch;
+    const bool wide = nch > kCtaChunks, cluster = wide && fmt == SGQ_FMT_FP8_PER_TOKEN;
+    if (cluster) {
+        if (!plan_cluster(so.Ms, nch, dev, &plan, &segc)) return SGQ_ERR_UNSUPPORTED;
+    } else {
+        int seg = swiglu_segments(fmt, so.Ms, I, sms);
+        if (wide) seg = wide_segments(nch, fmt == SGQ_FMT_FP8_BLOCK128 ? 16 : 4, seg, &segc);
+        else segc = nch / seg;
+        if (!sgq::plan_rows(so.Ms, segc * 8, sms, &plan)) return SGQ_ERR_UNSUPPORTED;
+        plan.device = dev.id;
+        plan.full = plan.full && so.Ms == M && seg == 1;   // the exact-fit kernels run whole rows
+        plan.seg = seg;
+    }
     sgq::SwigluArgs a;
     a.gu = static_cast<const uint16_t*>(gate_up);
     a.q = static_cast<uint8_t*>(q_out);
@@ -344,7 +423,7 @@ int swiglu_call(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float al
     a.out = static_cast<uint16_t*>(out);
     a.M = M;
     a.I = (int)I;
-    a.segc = (int)(I / 8 / seg);
+    a.segc = segc;
     a.tpr = plan.tpr;
     a.rpc = plan.rpc;
     a.flags = flags;
@@ -373,7 +452,9 @@ int swiglu_call(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float al
         while (bf16_value(tb) * a.khi > 125.0f) tb = (tb & 0x8000u) ? tb - 1 : tb + 1;   // towards +inf
         a.tail2 = tb | (tb << 16);
     }
-    return launched(sgq::launch_swiglu(fmt, plan, a, clamp16, static_cast<cudaStream_t>(stream)));
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return launched(cluster ? sgq::launch_swiglu_pt_cluster(plan, a, clamp16, st)
+                            : sgq::launch_swiglu(fmt, plan, a, clamp16, st));
 }
 
 int gcd(int a, int b) { return b == 0 ? a : gcd(b, a % b); }
@@ -495,8 +576,24 @@ int quantize_fp8(int fmt, uint32_t flags, int64_t M, int64_t W, const void* src,
     const Span spans[] = {{src, (size_t)M * W * 2}, {q_out, (size_t)M * W}, {scale_out, sbytes}};
     if (any_overlap(spans, 3)) return SGQ_ERR_INVALID_ARG;
 
+    // Rows wider than one CTA covers: column segments (MX, 1x128), or a
+    // cluster of CTAs a row (per-token, whose scale needs the row's amax).
+    const Device dev = current_device();
+    const int nch = (int)(W / 8);
     sgq::Plan plan;
-    if (!plan_launch(M, (int)W, so, current_device(), &plan)) return SGQ_ERR_UNSUPPORTED;
+    int segc = nch;
+    const bool wide = nch > kCtaChunks, cluster = wide && fmt == SGQ_FMT_FP8_PER_TOKEN;
+    if (cluster) {
+        if (!plan_cluster(so.Ms, nch, dev, &plan, &segc)) return SGQ_ERR_UNSUPPORTED;
+    } else if (wide) {
+        const int seg = wide_segments(nch, fmt == SGQ_FMT_FP8_BLOCK128 ? 16 : 4, 1, &segc);
+        if (!sgq::plan_rows(so.Ms, segc * 8, dev.sms, &plan)) return SGQ_ERR_UNSUPPORTED;
+        plan.device = dev.id;
+        plan.full = false;
+        plan.seg = seg;
+    } else {
+        if (!plan_launch(M, (int)W, so, dev, &plan)) return SGQ_ERR_UNSUPPORTED;
+    }
     sgq::QuantArgs a;
     a.src = static_cast<const uint16_t*>(src);
     a.q = static_cast<uint8_t*>(q_out);
@@ -506,7 +603,10 @@ int quantize_fp8(int fmt, uint32_t flags, int64_t M, int64_t W, const void* src,
     a.W = (int)W;
     a.tpr = plan.tpr;
     a.rpc = plan.rpc;
-    return launched(sgq::launch_quant(fmt, dt_of(flags), plan, a, static_cast<cudaStream_t>(stream)));
+    a.segc = segc;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return launched(cluster ? sgq::launch_quant_pt_cluster(dt_of(flags), plan, a, st)
+                            : sgq::launch_quant(fmt, dt_of(flags), plan, a, st));
 }
 
 int rmsnorm_dual_quant(int fmt, uint32_t flags, int64_t M, float eps, const sgq_norm_seg_t* seg_a,
@@ -518,7 +618,7 @@ int rmsnorm_dual_quant(int fmt, uint32_t flags, int64_t M, float eps, const sgq_
     for (int i = 0; i < 2; ++i) {
         const sgq_norm_seg_t& s = *sg[i];
         if (s.H <= 0 || s.ld < s.H) return SGQ_ERR_INVALID_ARG;
-        if (s.H % (s.q_out ? group_of(fmt) : 8) != 0 || s.H > SGQ_MAX_WIDTH) return SGQ_ERR_UNSUPPORTED;
+        if (s.H % (s.q_out ? group_of(fmt) : 8) != 0 || s.H > SGQ_MAX_DUAL_WIDTH) return SGQ_ERR_UNSUPPORTED;
         if (M > kMaxElements / s.ld) return SGQ_ERR_INVALID_ARG;
     }
     if (M == 0) return SGQ_OK;

@@ -42,8 +42,9 @@ constexpr uint32_t F_FROM_FP32 = 1u << 1;
 constexpr uint32_t F_ACT_BF16 = 1u << 2;
 
 constexpr int kMaxNV = 4;          // chunks per thread
-constexpr int kMaxTPR = 512;       // threads per row (SGQ_MAX_WIDTH = kMaxTPR * kMaxNV * 8)
+constexpr int kMaxTPR = 512;       // threads per row (one CTA covers kMaxTPR * kMaxNV * 8 columns)
 constexpr int kTargetCTA = 256;    // threads per CTA when several rows share one
+constexpr int kMaxCluster = 8;     // CTAs a row at most when a row is wider than one CTA covers
 
 // ----------------------------------------------------------------- memory
 
@@ -234,6 +235,64 @@ __device__ __forceinline__ uint32_t f32x4_to_e4m3x4(float a0, float a1, float a2
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// ---------------------------------------------------------------- clusters
+
+// Thread block clusters: the CTAs of a cluster run at the same time, and each
+// may write the others' shared memory. A row wider than one CTA covers is
+// split over the CTAs of one cluster, which exchange their partial reductions
+// through shared memory (no global memory, no flags).
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_ctas() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+// The cluster barrier in two halves: every thread of every CTA of the
+// cluster arrives, then waits for all the others (hardware barrier phases,
+// as __syncthreads is for one CTA). The relaxed arrive orders no memory; the
+// release / acquire pair makes the shared-memory stores before the arrive
+// visible to the threads after the wait.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// Store v into the copy of the shared variable at p held by the cluster's
+// CTA `rank`.
+__device__ __forceinline__ void st_cluster_f32x2(const void* p, uint32_t rank, float2 v) {
+    const uint32_t local = (uint32_t)__cvta_generic_to_shared(p);
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(remote), "f"(v.x), "f"(v.y) : "memory");
+}
+
+// One float2 from every CTA of the cluster, combined in rank order (sum of
+// .x, max of .y, which is >= 0), so that every CTA gets the bit-identical
+// result. v is this CTA's value (the same in all its threads). Every thread
+// of every CTA calls it once, after cluster_arrive_relaxed(): the wait that
+// completes that arrive guarantees every CTA of the cluster is running
+// before any thread writes another's shared memory; CTA i's thread j writes
+// v into slot i of CTA j, and the second arrive / wait makes those stores
+// visible. No shared memory of another CTA is touched afterwards, so each
+// CTA may exit when it likes.
+__device__ __forceinline__ float2 cluster_combine(float2 v, float2 (&slots)[kMaxCluster]) {
+    const uint32_t n = cluster_ctas(), me = cluster_rank();
+    cluster_wait();
+    if (threadIdx.x < n) st_cluster_f32x2(&slots[me], threadIdx.x, v);
+    cluster_arrive();
+    cluster_wait();
+    float2 r = slots[0];
+    for (uint32_t i = 1; i < n; ++i) r = make_float2(r.x + slots[i].x, fmaxf(r.y, slots[i].y));
+    return r;
+}
+
 // ------------------------------------------------------------ arithmetic
 
 // Hardware reciprocal approximation (about 1 ulp); subnormal inputs and
@@ -300,9 +359,9 @@ __device__ __forceinline__ void sigmoid8(const float (&x)[8], float khi, float k
     for (int i = 0; i < 4; ++i) {
         const float2 E = __ffma2_rn(e[i], m[i], e[i]);
         const float2 d = __fadd2_rn(E, f2(1.0f));
-        const float2 nd = __ffma2_rn(E, f2(-1.0f), f2(-1.0f));             // -(1 + E)
         const float2 r0 = make_float2(rcp_approx(d.x), rcp_approx(d.y));
-        const float2 res = __ffma2_rn(nd, r0, f2(1.0f));                   // 1 - d*r0
+        // 1 - d*r0, with -d = RN(-(1 + E)) the exact negation of d (rounding to nearest is symmetric)
+        const float2 res = __ffma2_rn(make_float2(-d.x, -d.y), r0, f2(1.0f));
         const float2 r = __ffma2_rn(r0, res, r0);                          // one Newton-Raphson step
         out[2 * i] = r.x;
         out[2 * i + 1] = r.y;
@@ -346,9 +405,8 @@ __device__ __forceinline__ void sigmoid8_prechecked(const float (&x)[8], float k
     for (int i = 0; i < 4; ++i) {
         const float2 E = __ffma2_rn(e[i], m[i], e[i]);
         const float2 d = __fadd2_rn(E, f2(1.0f));
-        const float2 nd = __ffma2_rn(E, f2(-1.0f), f2(-1.0f));
         const float2 r0 = make_float2(rcp_approx(d.x), rcp_approx(d.y));
-        const float2 res = __ffma2_rn(nd, r0, f2(1.0f));
+        const float2 res = __ffma2_rn(make_float2(-d.x, -d.y), r0, f2(1.0f));
         const float2 r = __ffma2_rn(r0, res, r0);
         out[2 * i] = r.x;
         out[2 * i + 1] = r.y;

@@ -42,7 +42,7 @@ struct NormArgs {
     int rpc;                 // rows per CTA
     float eps;
     uint32_t flags;
-    int segc;                // output chunks a column segment (H / 8 / gridDim.y)
+    int segc;                // output chunks a column segment (SEG) or cluster CTA (CL); H / 8 for whole rows
 };
 
 struct SwigluArgs {
@@ -60,7 +60,7 @@ struct SwigluArgs {
     uint32_t lim2, nlim2;    // bf16x2 of limit and -limit (the CLAMP16 kernels)
     uint32_t tail2;          // bf16x2 of the least gate t with RN(khi t) <= 125 (the CLAMP16 kernels)
     float khi, klo;          // -alpha log2(e) in two fp32 parts (OAI)
-    int segc;                // chunks a column segment (I / 8 / gridDim.y)
+    int segc;                // chunks a column segment or cluster CTA (I / 8 when rows are whole)
 };
 
 struct QuantArgs {
@@ -71,6 +71,7 @@ struct QuantArgs {
     int W;
     int tpr;
     int rpc;
+    int segc;                // chunks a column segment or cluster CTA (W / 8 when rows are whole)
 };
 
 // One row's view of ScaleOut in layout LAYOUT (a compile-time choice, so
@@ -219,7 +220,14 @@ __host__ __device__ constexpr bool norm_z_in_smem(int fmt) { return fmt == FMT_P
 // segc a multiple of 32, so that a warp's chunks are all in or all out. The
 // host never splits an in-place residual update, which another CTA of the row
 // would read back.
-template <int FMT, int LAYOUT, int NV, bool HAS_RES, bool FULL, int DT, bool SEG = false>
+// CL: a row wider than one CTA covers, split over the CTAs of a cluster (one
+// row per cluster, blk = the row): CTA k of the cluster reads, computes and
+// writes only chunks [k * segc, min((k + 1) * segc, H / 8)), segc a multiple
+// of 32, and the CTAs' partial sums of squares (and max |z|) are combined in
+// rank order through shared memory (cluster_combine), so every CTA of the row
+// gets the bit-identical inv. Each CTA reads only its own columns, so an
+// in-place residual update is safe here too.
+template <int FMT, int LAYOUT, int NV, bool HAS_RES, bool FULL, int DT, bool SEG = false, bool CL = false>
 __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
     extern __shared__ uint4 stage[];
     __shared__ float2 part[32];
@@ -233,8 +241,10 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
     const int H = a.H, nchunks = H >> 3;
     const int64_t base = row * (int64_t)H;
     auto slot = [&](int v, int i) { return &stage[(NIN * v + i) * nt + threadIdx.x]; };
-    const int cb = SEG ? (int)blockIdx.y * a.segc : 0;                // the chunks this CTA writes
-    const int cend = SEG ? cb + a.segc : nchunks;
+    const int cb = SEG ? (int)blockIdx.y * a.segc : CL ? (int)cluster_rank() * a.segc : 0;   // the chunks this CTA writes
+    const int cend = SEG ? cb + a.segc : CL ? min(cb + a.segc, nchunks) : nchunks;
+    const int c0 = CL ? cb : 0;              // chunk of thread 0's first copy (CL: the segment's first)
+    const int clim = CL ? cend : nchunks;    // chunks this CTA reads end here
 
     // 1. every load of the row (x, r and the weight) goes out at once, copied
     //    asynchronously into this thread's shared-memory slots. The weight is
@@ -247,8 +257,8 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
     // SEG: the weight only where this CTA writes (the per-token max |z| needs all of it)
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
-        const int c = t + v * tpr;
-        const bool okw = (FULL || (row_ok && c < nchunks)) && (!SEG || FMT == FMT_PT || (c >= cb && c < cend));
+        const int c = c0 + t + v * tpr;
+        const bool okw = (FULL || (row_ok && c < clim)) && (!SEG || FMT == FMT_PT || (c >= cb && c < cend));
         cp_async16_cached(slot(v, NIN - 1), okw ? (const void*)(a.w + (int64_t)c * 8) : (const void*)a.w,
                           okw ? 16 : 0);
     }
@@ -256,8 +266,8 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
     pdl_wait();
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
-        const int c = t + v * tpr;
-        const bool ok = FULL || (row_ok && c < nchunks);   // else zero-fill, reading nothing
+        const int c = c0 + t + v * tpr;
+        const bool ok = FULL || (row_ok && c < clim);      // else zero-fill, reading nothing
         const int nb = ok ? 16 : 0;
         cp_async16(slot(v, 0), ok ? (const void*)(a.x + row * a.ldx + (int64_t)c * 8) : (const void*)a.x, nb);
         if (HAS_RES)
@@ -265,6 +275,7 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
         cp_async_commit();
     }
     pdl_trigger();
+    if (CL) cluster_arrive_relaxed();       // completed in cluster_combine, once the whole cluster runs
 
     // 2. h = x + r in fp32; write the updated residual; z = h * w'; partial
     //    sum of squares (and max |z| for the per-token format). SEG: warps
@@ -272,58 +283,64 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
     //    sum (c & ~31 is the same in every lane of a warp, and segc is a
     //    multiple of 32); their z is never used, except by the per-token max.
     const bool from32 = (a.flags & F_FROM_FP32) != 0;
-    // w' = w + 1 (Gemma) or w + (-0), which is w exactly, signed zeros included
-    const float w_add = (a.flags & F_GEMMA) ? 1.0f : -0.0f;
     constexpr bool ZS = norm_z_in_smem(FMT);
     float z[NV][8];
     float2 ss2 = make_float2(0.0f, 0.0f);
     float zmax = 0.0f;
+    // w' = w + 1 (Gemma) or w itself: the chunk loop is specialised on the
+    // weight form, so that a plain weight costs no addition
+    auto pass1 = [&](auto gemma_tag) {
+        constexpr bool GEMMA = decltype(gemma_tag)::value;
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
-        const int c = t + v * tpr;
-        const bool mine = !SEG || FMT == FMT_PT || ((c & ~31) >= cb && (c & ~31) < cend);
-        float h[8], wf[8];
-        cp_async_wait_group_of<NV>(v);
-        load8<DT>(ld_smem16(slot(v, 0)), h);
-        if (HAS_RES) {
-            float rf[8];
-            load8<DT>(ld_smem16(slot(v, 1)), rf);
+        for (int v = 0; v < NV; ++v) {
+            const int c = c0 + t + v * tpr;
+            const bool mine = !SEG || FMT == FMT_PT || ((c & ~31) >= cb && (c & ~31) < cend);
+            float h[8], wf[8];
+            cp_async_wait_group_of<NV>(v);
+            load8<DT>(ld_smem16(slot(v, 0)), h);
+            if (HAS_RES) {
+                float rf[8];
+                load8<DT>(ld_smem16(slot(v, 1)), rf);
 #pragma unroll
-            for (int k = 0; k < 8; k += 2) {
-                const float2 hs = __fadd2_rn(make_float2(h[k], h[k + 1]), make_float2(rf[k], rf[k + 1]));
-                h[k] = hs.x;
-                h[k + 1] = hs.y;
+                for (int k = 0; k < 8; k += 2) {
+                    const float2 hs = __fadd2_rn(make_float2(h[k], h[k + 1]), make_float2(rf[k], rf[k + 1]));
+                    h[k] = hs.x;
+                    h[k + 1] = hs.y;
+                }
+                // the updated residual is next read by the following layer's norm,
+                // after the sublayer in between: streamed out (evict-first)
+                if (a.r_out && mine)
+                    st16_cs_if(a.r_out + base + (int64_t)c * 8, pack8<DT>(h),
+                               FULL || (row_ok && (SEG ? c >= cb && c < cend : c < clim)));
             }
-            // the updated residual is next read by the following layer's norm,
-            // after the sublayer in between: streamed out (evict-first)
-            if (a.r_out && mine)
-                st16_cs_if(a.r_out + base + (int64_t)c * 8, pack8<DT>(h),
-                           FULL || (row_ok && (SEG ? c >= cb && c < cend : c < nchunks)));
-        }
-        if (!mine) {
+            if (!mine) {
+#pragma unroll
+                for (int k = 0; k < 8; k += 2) {
+                    const float2 hp = make_float2(h[k], h[k + 1]);
+                    ss2 = __ffma2_rn(hp, hp, ss2);
+                }
+                continue;
+            }
+            load8<DT>(ld_smem16(slot(v, NIN - 1)), wf);
 #pragma unroll
             for (int k = 0; k < 8; k += 2) {
                 const float2 hp = make_float2(h[k], h[k + 1]);
+                const float2 wp = GEMMA ? __fadd2_rn(make_float2(wf[k], wf[k + 1]), f2(1.0f))
+                                        : make_float2(wf[k], wf[k + 1]);
                 ss2 = __ffma2_rn(hp, hp, ss2);
+                const float2 zp = __fmul2_rn(hp, wp);
+                z[v][k] = zp.x;
+                z[v][k + 1] = zp.y;
+                if (FMT == FMT_PT) zmax = fmaxf(zmax, fmaxf(fabsf(zp.x), fabsf(zp.y)));
             }
-            continue;
+            if (ZS) {   // over this thread's own x and weight slots of chunk v, both read above
+                *reinterpret_cast<float4*>(slot(v, 0)) = make_float4(z[v][0], z[v][1], z[v][2], z[v][3]);
+                *reinterpret_cast<float4*>(slot(v, NIN - 1)) = make_float4(z[v][4], z[v][5], z[v][6], z[v][7]);
+            }
         }
-        load8<DT>(ld_smem16(slot(v, NIN - 1)), wf);
-#pragma unroll
-        for (int k = 0; k < 8; k += 2) {
-            const float2 hp = make_float2(h[k], h[k + 1]);
-            const float2 wp = __fadd2_rn(make_float2(wf[k], wf[k + 1]), f2(w_add));
-            ss2 = __ffma2_rn(hp, hp, ss2);
-            const float2 zp = __fmul2_rn(hp, wp);
-            z[v][k] = zp.x;
-            z[v][k + 1] = zp.y;
-            if (FMT == FMT_PT) zmax = fmaxf(zmax, fmaxf(fabsf(zp.x), fabsf(zp.y)));
-        }
-        if (ZS) {   // over this thread's own x and weight slots of chunk v, both read above
-            *reinterpret_cast<float4*>(slot(v, 0)) = make_float4(z[v][0], z[v][1], z[v][2], z[v][3]);
-            *reinterpret_cast<float4*>(slot(v, NIN - 1)) = make_float4(z[v][4], z[v][5], z[v][6], z[v][7]);
-        }
-    }
+    };
+    if (a.flags & F_GEMMA) pass1(std::true_type{});
+    else pass1(std::false_type{});
     float ss = ss2.x + ss2.y;
 
     // 3. inv = 1/sqrt(mean(h^2) + eps), each step correctly rounded
@@ -334,6 +351,12 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
         row_zmax = r.y;
     } else {
         ss = row_reduce<false>(ss, reinterpret_cast<float*>(part), tpr, lrow);
+    }
+    if (CL) {                                // the row's totals over the cluster, in rank order
+        __shared__ float2 cl_slots[kMaxCluster];
+        const float2 r = cluster_combine(make_float2(ss, row_zmax), cl_slots);
+        ss = r.x;
+        row_zmax = r.y;
     }
     float inv = __frsqrt_rn(__fdiv_rn(ss, (float)H) + a.eps);
     if (!FULL && !row_ok) inv = 0.0f;                          // a padding row of the scale layout: all zero
@@ -356,11 +379,11 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
         constexpr bool QUANT = decltype(quant_tag)::value, FROM32 = decltype(from32_tag)::value;
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
-            const int c = t + v * tpr;
+            const int c = c0 + t + v * tpr;
             // warps whose chunks lie outside this CTA's segment (or wholly past
             // the row end) skip the chunk; c & ~31 is the same in every lane
             if (SEG && ((c & ~31) < cb || (c & ~31) >= cend)) continue;
-            const bool ok = FULL || (row_ok && c < nchunks);
+            const bool ok = FULL || (row_ok && c < clim);
             float y[8], src[8], zc[8];
             if (ZS) {
                 const float4 lo = *reinterpret_cast<const float4*>(slot(v, 0));
@@ -386,7 +409,7 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
                 } else {
                     load8<DT>(yb, src);
                 }
-                quantize_chunk<FMT, LAYOUT>(src, row, c, ok, FULL || (srow_ok && c < nchunks), H, a.q, sr, pt.x,
+                quantize_chunk<FMT, LAYOUT>(src, row, c, ok, FULL || (srow_ok && c < clim), H, a.q, sr, pt.x,
                                             pt.y);
             }
         }
@@ -399,6 +422,14 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
 template <int FMT, int LAYOUT, int NV, bool HAS_RES, bool FULL, int DT>
 __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
     norm_rows<FMT, LAYOUT, NV, HAS_RES, FULL, DT, !FULL>(a, blockIdx.x);
+}
+
+// Rows wider than one CTA covers: a cluster of gridDim.x / M CTAs a row
+// (cluster dimension set at launch), CTA k of the cluster taking the row's
+// k-th column segment; four chunks a thread, bounds always checked.
+template <int FMT, int LAYOUT, bool HAS_RES, int DT>
+__global__ void __launch_bounds__(kMaxTPR) norm_cluster_kernel(const NormArgs a) {
+    norm_rows<FMT, LAYOUT, kMaxNV, HAS_RES, false, DT, false, true>(a, blockIdx.x / cluster_ctas());
 }
 
 // Two independent row sets normed in one launch (the q and kv latent norms
@@ -514,10 +545,15 @@ __host__ __device__ constexpr int swiglu_stage_bytes(int nv, int threads) { retu
 // CLAMP16 (OAI only, see activation8): the limit is a bf16 value and the
 // clamps of g and u run on the packed bf16 pairs before widening.
 // Column segments: the bounds-checked kernels may run each row as gridDim.y
-// CTAs, CTA y taking chunks [y * segc, (y + 1) * segc), a whole number of
-// scale groups (the MX and 1x128 formats have nothing row-wide). Chunk
-// indices stay the row's own, so every address and scale index is unchanged.
-template <int FMT, int LAYOUT, int NV, int ACT, bool FULL, bool CLAMP16>
+// CTAs, CTA y taking chunks [y * segc, min((y + 1) * segc, I / 8)), a whole
+// number of scale groups (the MX and 1x128 formats have nothing row-wide).
+// Chunk indices stay the row's own, so every address and scale index is
+// unchanged.
+// CL (per-token only): a row wider than one CTA covers, split over the CTAs
+// of a cluster, one row per cluster: CTA k takes chunks
+// [k * segc, min((k + 1) * segc, I / 8)), and the CTAs' amaxes are combined
+// through shared memory (cluster_combine) into the row's scale.
+template <int FMT, int LAYOUT, int NV, int ACT, bool FULL, bool CLAMP16, bool CL = false>
 __device__ __forceinline__ void swiglu_rows(const SwigluArgs& a) {
     extern __shared__ uint4 stage[];
     __shared__ float part_amax[32];
@@ -525,12 +561,12 @@ __device__ __forceinline__ void swiglu_rows(const SwigluArgs& a) {
     const int nt = blockDim.x;
     const int lrow = threadIdx.x / tpr;
     const int t = threadIdx.x - lrow * tpr;
-    const int64_t row = (int64_t)blockIdx.x * a.rpc + lrow;
+    const int64_t row = CL ? (int64_t)(blockIdx.x / cluster_ctas()) : (int64_t)blockIdx.x * a.rpc + lrow;
     const bool row_ok = FULL || row < a.M;
     const int I = a.I, nchunks = I >> 3;
     const uint16_t* grow = a.gu + row * (int64_t)(2 * I);
-    const int cb = FULL ? 0 : (int)blockIdx.y * a.segc;               // the segment's first chunk
-    const int cend = FULL ? nchunks : cb + a.segc;
+    const int cb = FULL ? 0 : (int)(CL ? cluster_rank() : blockIdx.y) * a.segc;   // the segment's first chunk
+    const int cend = FULL ? nchunks : min(cb + a.segc, nchunks);
 
     pdl_wait();
 #pragma unroll
@@ -544,6 +580,7 @@ __device__ __forceinline__ void swiglu_rows(const SwigluArgs& a) {
         cp_async_commit();
     }
     pdl_trigger();
+    if (CL) cluster_arrive_relaxed();       // completed in cluster_combine, once the whole cluster runs
 
     const bool round_silu = (a.flags & F_ACT_BF16) != 0, from32 = (a.flags & F_FROM_FP32) != 0;
     const float2 gr = oai_gate_range(a.alpha);
@@ -608,9 +645,15 @@ __device__ __forceinline__ void swiglu_rows(const SwigluArgs& a) {
                     const int c = cb + t + v * tpr;
                     st16_if(a.out + row * I + (int64_t)c * 8, f32x8_to_bf16x8(src[v]), FULL || (row_ok && c < cend));
                 }
+                if (CL) cluster_wait();   // completes the arrive above
                 return;
             }
-            const float2 pt = per_token_scale(row_reduce<true>(m, part_amax, tpr, lrow));
+            float amax = row_reduce<true>(m, part_amax, tpr, lrow);
+            if (CL) {                  // the row's amax over the cluster
+                __shared__ float2 cl_slots[kMaxCluster];
+                amax = cluster_combine(make_float2(0.0f, amax), cl_slots).y;
+            }
+            const float2 pt = per_token_scale(amax);
 #pragma unroll
             for (int v = 0; v < NV; ++v) {
                 const int c = cb + t + v * tpr;
@@ -646,47 +689,61 @@ __global__ void __maxnreg__(56) swiglu_quant_kernel_r56(const SwigluArgs a) {
     swiglu_rows<FMT, LAYOUT, NV, ACT, FULL, CLAMP16>(a);
 }
 
+// Per-token SwiGLU rows wider than one CTA covers: a cluster of
+// gridDim.x / M CTAs a row; four chunks a thread, bounds always checked.
+template <int ACT, bool CLAMP16>
+__global__ void __launch_bounds__(kMaxTPR) swiglu_pt_cluster_kernel(const SwigluArgs a) {
+    swiglu_rows<FMT_PT, SCALE_ROW_MAJOR, kMaxNV, ACT, false, CLAMP16, true>(a);
+}
+
 // Bytes of dynamic shared memory the standalone quant kernel stages its loads in.
 __host__ __device__ constexpr int quant_stage_bytes(int nv, int threads) { return nv * threads * 16; }
 
 // Standalone FP8 quantisation of 16-bit rows (the quant of the unfused
 // chains). Same row engine and quantiser as the fused kernels; the source is
-// the bf16 (DT_BF16) or fp16 (DT_F16) value itself.
-template <int FMT, int LAYOUT, int NV, bool FULL, int DT>
-__global__ void __launch_bounds__(kMaxTPR) quant_kernel(const QuantArgs a) {
+// the bf16 (DT_BF16) or fp16 (DT_F16) value itself. The bounds-checked
+// kernels may split rows into gridDim.y column segments (MX and 1x128: CTA y
+// takes chunks [y * segc, min((y + 1) * segc, W / 8))); CL (per-token): a row
+// wider than one CTA covers, split over the CTAs of a cluster, the amaxes
+// combined through shared memory.
+template <int FMT, int LAYOUT, int NV, bool FULL, int DT, bool CL = false>
+__device__ __forceinline__ void quant_rows(const QuantArgs& a) {
     extern __shared__ uint4 stage[];
     __shared__ float part_amax[32];
     const int tpr = a.tpr;
     const int nt = blockDim.x;
     const int lrow = threadIdx.x / tpr;
     const int t = threadIdx.x - lrow * tpr;
-    const int64_t row = (int64_t)blockIdx.x * a.rpc + lrow;
+    const int64_t row = CL ? (int64_t)(blockIdx.x / cluster_ctas()) : (int64_t)blockIdx.x * a.rpc + lrow;
     const bool row_ok = FULL || row < a.M;
     const int W = a.W, nchunks = W >> 3;
     const uint16_t* srow = a.src + row * (int64_t)W;
+    const int cb = FULL ? 0 : (int)(CL ? cluster_rank() : blockIdx.y) * a.segc;   // the segment's first chunk
+    const int cend = FULL ? nchunks : min(cb + a.segc, nchunks);
 
     pdl_wait();
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
-        const int c = t + v * tpr;
-        const bool ok = FULL || (row_ok && c < nchunks);   // else zero-fill, reading nothing
+        const int c = cb + t + v * tpr;
+        const bool ok = FULL || (row_ok && c < cend);      // else zero-fill, reading nothing
         cp_async16(&stage[v * nt + threadIdx.x], ok ? (const void*)(srow + (int64_t)c * 8) : (const void*)a.src,
                    ok ? 16 : 0);
         cp_async_commit();
     }
     pdl_trigger();
+    if (CL) cluster_arrive_relaxed();       // completed in cluster_combine, once the whole cluster runs
 
     const bool srow_ok = FULL || row < a.so.Ms;
     const ScaleRow sr = scale_row<FMT, LAYOUT>(a.so, row);
     if (FMT != FMT_PT) {
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
-            const int c = t + v * tpr;
+            const int c = cb + t + v * tpr;
             float src[8];
             cp_async_wait_group_of<NV>(v);
             load8<DT>(ld_smem16(&stage[v * nt + threadIdx.x]), src);
-            quantize_chunk<FMT, LAYOUT>(src, row, c, FULL || (row_ok && c < nchunks), FULL || (srow_ok && c < nchunks), W,
-                                a.q, sr);
+            quantize_chunk<FMT, LAYOUT>(src, row, c, FULL || (row_ok && c < cend), FULL || (srow_ok && c < cend), W,
+                                        a.q, sr);
         }
     } else {
         float src[NV][8];
@@ -698,14 +755,31 @@ __global__ void __launch_bounds__(kMaxTPR) quant_kernel(const QuantArgs a) {
 #pragma unroll
             for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(src[v][k]));
         }
-        const float2 pt = per_token_scale(row_reduce<true>(m, part_amax, tpr, lrow));
+        float amax = row_reduce<true>(m, part_amax, tpr, lrow);
+        if (CL) {                              // the row's amax over the cluster
+            __shared__ float2 cl_slots[kMaxCluster];
+            amax = cluster_combine(make_float2(0.0f, amax), cl_slots).y;
+        }
+        const float2 pt = per_token_scale(amax);
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
-            const int c = t + v * tpr;
-            quantize_chunk<FMT, LAYOUT>(src[v], row, c, FULL || (row_ok && c < nchunks), FULL || (srow_ok && c < nchunks),
-                                W, a.q, sr, pt.x, pt.y);
+            const int c = cb + t + v * tpr;
+            quantize_chunk<FMT, LAYOUT>(src[v], row, c, FULL || (row_ok && c < cend), FULL || (srow_ok && c < cend),
+                                        W, a.q, sr, pt.x, pt.y);
         }
     }
+}
+
+template <int FMT, int LAYOUT, int NV, bool FULL, int DT>
+__global__ void __launch_bounds__(kMaxTPR) quant_kernel(const QuantArgs a) {
+    quant_rows<FMT, LAYOUT, NV, FULL, DT>(a);
+}
+
+// Per-token quantisation of rows wider than one CTA covers: a cluster of
+// gridDim.x / M CTAs a row; four chunks a thread, bounds always checked.
+template <int DT>
+__global__ void __launch_bounds__(kMaxTPR) quant_pt_cluster_kernel(const QuantArgs a) {
+    quant_rows<FMT_PT, SCALE_ROW_MAJOR, kMaxNV, false, DT, true>(a);
 }
 
 }  // namespace sgq

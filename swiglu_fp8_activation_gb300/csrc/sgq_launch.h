@@ -20,6 +20,7 @@ struct Plan {
     int sms;     // multiprocessors of the device (0 if unknown)
     int seg = 1;
     int device = -1;   // the current device, for the per-device kernel attributes
+    int cluster = 0;   // > 1: CTAs a thread block cluster (the grid is rows x cluster CTAs, one row each)
 };
 
 // Pick a plan for M rows of width W (W % 8 == 0). Returns false when W needs
@@ -51,11 +52,18 @@ cudaError_t launch_pdl(void (*k)(const Args), const Plan& p, const Args& a, cuda
     cfg.blockDim = dim3((unsigned)(p.rpc * p.tpr));
     cfg.dynamicSmemBytes = (size_t)dynamic_smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (p.cluster > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)p.cluster;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelEx(&cfg, k, a);
 }
 
@@ -74,5 +82,11 @@ cudaError_t launch_swiglu_oai_part(int fmt, const Plan& p, const SwigluArgs& a, 
 cudaError_t launch_swiglu_silu_full(int fmt, const Plan& p, const SwigluArgs& a, cudaStream_t stream);
 cudaError_t launch_swiglu_silu_part(int fmt, const Plan& p, const SwigluArgs& a, cudaStream_t stream);
 cudaError_t launch_quant(int fmt, int dt, const Plan& p, const QuantArgs& a, cudaStream_t stream);
+
+// Rows wider than one CTA covers, split over a cluster of p.cluster CTAs a
+// row (p.grid = rows * p.cluster, p.rpc = 1, four chunks a thread).
+cudaError_t launch_norm_cluster(int fmt, int dt, const Plan& p, const NormArgs& a, cudaStream_t stream);
+cudaError_t launch_swiglu_pt_cluster(const Plan& p, const SwigluArgs& a, bool clamp16, cudaStream_t stream);
+cudaError_t launch_quant_pt_cluster(int dt, const Plan& p, const QuantArgs& a, cudaStream_t stream);
 
 }  // namespace sgq

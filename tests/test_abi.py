@@ -111,7 +111,7 @@ def test_norm_argument_errors(sgq_lib):
     assert norm(L, H=48) == UNSUPPORTED               # MX needs H % 32 == 0
     assert norm(L, fmt=1, H=96) == UNSUPPORTED        # 1x128 needs H % 128 == 0
     assert norm(L, fmt=2, H=20) == UNSUPPORTED        # per-token needs H % 8 == 0
-    assert norm(L, H=16384 + 32) == UNSUPPORTED       # above SGQ_MAX_WIDTH
+    assert norm(L, H=131072 + 32) == UNSUPPORTED      # above SGQ_MAX_WIDTH
     for kw in ("x", "w", "q", "s"):
         assert norm(L, **{kw: None}) == INVALID, kw
     assert norm(L, r=None) == INVALID                 # residual_out without residual_in
@@ -165,7 +165,7 @@ def test_unfused_norm_argument_errors(sgq_lib):
     assert norm_only(L, H=0) == INVALID
     assert norm_only(L, eps=float("nan")) == INVALID
     assert norm_only(L, H=20) == UNSUPPORTED          # H % 8 == 0 is the only width rule
-    assert norm_only(L, H=16384 + 8) == UNSUPPORTED
+    assert norm_only(L, H=131072 + 8) == UNSUPPORTED
     for kw in ("x", "w", "n"):
         assert norm_only(L, **{kw: None}) == INVALID, kw
     assert norm_only(L, r=None) == INVALID            # residual_out without residual_in
@@ -197,7 +197,7 @@ def test_quantize_argument_errors(sgq_lib):
     assert quant(L, W=48) == UNSUPPORTED
     assert quant(L, fmt=1, W=192) == UNSUPPORTED
     assert quant(L, fmt=2, W=12) == UNSUPPORTED
-    assert quant(L, W=16384 + 32) == UNSUPPORTED
+    assert quant(L, W=131072 + 32) == UNSUPPORTED
     for kw in ("src", "q", "s"):
         assert quant(L, **{kw: None}) == INVALID, kw
     assert quant(L, src=C.c_void_p(BASE + 8)) == MISALIGNED

@@ -27,7 +27,7 @@ from swiglu_fp8_activation_gb300 import inputs, rmsnorm_add_quant, scale_shape, 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 GUARD = 4096
-BIG_M = 256                      # enough rows that no launch splits them
+BIG_M = 512                      # enough rows that no launch splits them (above two waves)
 
 
 def _sms():
@@ -42,6 +42,15 @@ def _segments(fmt, rows, I, sms):
     s = 1
     while s < 16 and rows * 2 * s <= sms and nch % (2 * s * gch) == 0 and nch // (2 * s) >= 64:
         s *= 2
+    if s == 1 and sms // 2 < rows <= 2 * sms:          # balance between half a wave and two waves
+        best_ctas, best_s = -(-rows // sms), 1
+        c = 2
+        while c <= 16 and nch % (c * gch) == 0 and nch // c >= 64:
+            per = -(-rows * c // sms)
+            if per * best_s * 16 < best_ctas * c * 15:
+                best_ctas, best_s = per, c
+            c *= 2
+        s = best_s
     return s
 
 
