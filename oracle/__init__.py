@@ -52,6 +52,8 @@ def lib() -> C.CDLL:
         L.ora_swiglu_quant.restype = C.c_int
         L.ora_swiglu_quant.argtypes = [C.c_int, C.c_int, C.c_uint, C.c_long, C.c_long, C.c_float,
                                        C.c_float, C.c_float, p, p, p, p, p, p, p, C.c_double]
+        L.ora_allreduce_sum.restype = C.c_int
+        L.ora_allreduce_sum.argtypes = [C.c_int, C.POINTER(C.c_void_p), C.c_long, C.c_uint, p, p, C.c_double]
         L.ora_quantize.restype = C.c_int
         L.ora_quantize.argtypes = [C.c_int, C.c_uint, C.c_long, C.c_long, p, p, p, p, p, p, C.c_double]
         _lib = L
@@ -238,3 +240,32 @@ def rmsnorm_dual_quant(fmt: str, xa: np.ndarray, wa: np.ndarray, xb: np.ndarray,
     a = rmsnorm_add_quant(fmt, xa, None, wa, eps=eps, gemma=gemma, from_fp32=from_fp32, fp16=fp16, **kw)
     b = rmsnorm_add_quant(fmt, xb, None, wb, eps=eps, gemma=gemma, from_fp32=from_fp32, fp16=fp16, **kw)
     return a, b
+
+
+def allreduce_sum(parts: list, *, fp16: bool = False, rel: float = REL_WINDOW) -> tuple:
+    """The all-reduce over tensor-parallel ranks that precedes the norm: the
+    element-wise sum of the ranks' partial tensors (16-bit patterns, all of
+    one shape) in fp64, rounded once to the activation type. Returns (the
+    sum's 16-bit patterns, a uint8 mask of the elements whose fp64 sum lies
+    within `rel` of a rounding boundary of that type)."""
+    parts = [np.ascontiguousarray(a, dtype=np.uint16) for a in parts]
+    shape = parts[0].shape
+    assert all(a.shape == shape for a in parts)
+    out = np.zeros(shape, np.uint16)
+    near = np.zeros(shape, np.uint8)
+    ptrs = (C.c_void_p * len(parts))(*[a.ctypes.data for a in parts])
+    rc = lib().ora_allreduce_sum(len(parts), ptrs, out.size, F_FP16 if fp16 else 0, _ptr(out), _ptr(near), rel)
+    if rc != 0:
+        raise ValueError("oracle rejected arguments (allreduce_sum)")
+    return out, near
+
+
+def allreduce_rmsnorm_add_quant(fmt: str, parts: list, r: np.ndarray | None, w: np.ndarray, **kw) -> dict:
+    """All-reduce + residual add + RMSNorm + FP8 quantisation, in the order of
+    its steps: x = allreduce_sum(parts) (the all-reduce's output), then
+    rmsnorm_add_quant(x, r, w). The result carries x and its boundary mask
+    (`x`, `x_near`) beside rmsnorm_add_quant's outputs."""
+    x, near = allreduce_sum(parts, fp16=kw.get("fp16", False))
+    ref = rmsnorm_add_quant(fmt, x, r, w, **kw)
+    ref["x"], ref["x_near"] = x, near
+    return ref

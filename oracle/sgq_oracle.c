@@ -453,3 +453,34 @@ int ora_quantize(int fmt, unsigned flags, long M, long W, const uint16_t* src_bi
     free(sa);
     return 0;
 }
+
+/* ------------------------------------------------------------ all-reduce */
+
+/*
+ * The all-reduce that precedes the norm under tensor parallelism ("[ROCm]
+ * [MiniMax-M3.1] Fuse MXFP8 quant into the add+RMSNorm and SwiGLU"
+ * (vllm PR 65478), "Purpose" commit 1: all-reduce + that norm, and
+ * "Limitations": a quant-emitting fused all-reduce + norm; "[ROCm] Fuse
+ * per-token activation quant into RMSNorm ..." (sglang PR 34502), "Change":
+ * the fused all-reduce + RMSNorm + quant of the entry projection). Each of the
+ * n ranks holds a partial [count] tensor; the all-reduce's output is their sum
+ * in the activation type: out[j] = round(sum_r parts[r][j]), the sum taken in
+ * fp64 (exact unless the partials' exponents span more than 45 binades) and
+ * rounded once to bf16 (fp16 with ORA_F_FP16). The fused norm then normalises
+ * out exactly as ora_rmsnorm_add_quant normalises x. near (optional) flags the
+ * elements whose sum lies within rel of a rounding boundary of the activation
+ * type, where an fp32 sum may round the other way. Returns 0, or -1 on a bad
+ * argument.
+ */
+int ora_allreduce_sum(int n, const uint16_t* const* parts, long count, unsigned flags, uint16_t* out,
+                      unsigned char* near, double rel) {
+    if (n < 1 || count < 0 || !parts || !out) return -1;
+    const int f16 = (flags & ORA_F_FP16) != 0;
+    for (long j = 0; j < count; ++j) {
+        double s = 0.0;
+        for (int r = 0; r < n; ++r) s += io_decode(f16, parts[r][j]);
+        out[j] = io_round(f16, s);
+        if (near) near[j] = (unsigned char)near_io_boundary(f16, s, rel);
+    }
+    return 0;
+}
