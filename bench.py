@@ -497,6 +497,43 @@ def wide_rows(dev):
     return res
 
 
+def allreduce_norm(dev):
+    """µs per launch (graph replay, as the decode table) of the tensor-parallel
+    all-reduce folded into the fused norm, the ranks' partials in this GPU's
+    memory (on a multi-GPU node they are peers' memory, read over NVLink):
+    TP4 add + Gemma RMSNorm + MXFP8 + bf16 copy at H=6144, and TP8 RMSNorm +
+    per-token FP8 at H=7168, at M = 1, 8, 64; beside each, the plain fused
+    norm of the same rows (one input instead of the partials)."""
+    import torch
+
+    from swiglu_fp8_activation_gb300 import allreduce_rmsnorm_add_quant, inputs, rmsnorm_add_quant
+    res = {}
+    for name, n, Hd, fmt, gemma, normed, resid in (("tp4_gemma_norm_mxfp8_bf16copy_H6144", 4, 6144, "mxfp8", True,
+                                                    True, True),
+                                                   ("tp8_rmsnorm_per_token_H7168", 8, 7168, "per_token", False,
+                                                    False, False)):
+        row = {}
+        for M in (1, 8, 64):
+            parts = [inputs.norm_inputs(M, Hd, seed=k, x_std=1.0, r_std=None, w_mean=0.0, w_std=0.1)["x"].to(dev)
+                     for k in range(n)]
+            t = inputs.norm_inputs(M, Hd, seed=99, x_std=1.0, r_std=1.0, w_mean=0.0 if gemma else 1.0, w_std=0.1)
+            w = t["w"].to(dev)
+            r = t["r"].to(dev) if resid else None
+            ro = torch.empty_like(r) if resid else None
+            q = torch.empty(M, Hd, dtype=torch.uint8, device=dev)
+            s = torch.empty(M, Hd // 32 if fmt == "mxfp8" else 1, dtype=torch.uint8 if fmt == "mxfp8" else torch.float32,
+                            device=dev)
+            nrm = torch.empty(M, Hd, dtype=torch.bfloat16, device=dev) if normed else None
+            fused = lambda: allreduce_rmsnorm_add_quant(parts, w, fmt=fmt, gemma=gemma, residual_in=r, residual_out=ro,
+                                                        q_out=q, scale_out=s, normed_out=nrm)
+            plain = lambda: rmsnorm_add_quant(parts[0], w, fmt=fmt, gemma=gemma, residual_in=r, residual_out=ro,
+                                              q_out=q, scale_out=s, normed_out=nrm)
+            row[str(M)] = {"allreduce_norm": round(graph_us_per_launch(fused, iters=100, reps=10), 3),
+                           "norm_alone": round(graph_us_per_launch(plain, iters=100, reps=10), 3)}
+        res[name] = row
+    return res
+
+
 def qkv_norm_configs(dev):
     """µs per launch (graph replay) of the q/kv latent norms of multi-head
     latent attention: q [M,1536] normed + per-token FP8, kv [M,512] normed to
@@ -730,6 +767,7 @@ def run_ours(args, world, rank, local):
         others = other_configs(dev) if rank == 0 and not args.quick else None
         qkv = qkv_norm_configs(dev) if rank == 0 and not args.quick else None
         wide = wide_rows(dev) if rank == 0 and not args.quick else None
+        arn = allreduce_norm(dev) if rank == 0 and not args.quick else None
     total_ms = max_over_ranks(total_ms, world)
     alone_steps = max(args.steps, 200)
     norm_alone_us = time_alone(pf, "norm", alone_steps)
@@ -775,6 +813,7 @@ def run_ours(args, world, rank, local):
         "other_configs": others,
         "qkv_latent_norm_us": qkv,
         "wide_rows_us": wide,
+        "allreduce_norm_us": arn,
         "e2e": {"value": round(sb / (e2e_ms * 1e-3) / 1e9 * world, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 3),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * args.steps,

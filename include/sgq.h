@@ -21,6 +21,11 @@
  *   rmsnorm_dual_quant the q and kv latent norms of multi-head latent
  *                      attention (each segment quantised and/or copied)
  *
+ * and the tensor-parallel all-reduce folded into the fused norm:
+ *
+ *   allreduce_rmsnorm_add_quant  the ranks' partial rows summed, then
+ *                      residual add + RMSNorm + FP8 quantisation
+ *
  * The operations follow these pages:
  *   [P1] "[ROCm][MiniMax-M3.1] Fuse MXFP8 quant into the add+RMSNorm and
  *        SwiGLU epilogues" (vllm PR 65478): "Purpose" (the two fusions),
@@ -86,8 +91,11 @@ extern "C" {
  * column segment, at small M); wider rows run as a cluster of up to 8 CTAs,
  * or as column segments where no row-wide value is needed. */
 #define SGQ_MAX_WIDTH 131072
-/* Widest segment of rmsnorm_dual_quant (one CTA a row). */
+/* Widest segment of rmsnorm_dual_quant, and widest row of
+ * allreduce_rmsnorm_add_quant (one CTA a row). */
 #define SGQ_MAX_DUAL_WIDTH 16384
+/* Most partial inputs (tensor-parallel ranks) of allreduce_rmsnorm_add_quant. */
+#define SGQ_MAX_RANKS 8
 
 /* Quantisation format of the output activation. */
 typedef enum sgq_format {
@@ -186,6 +194,44 @@ int rmsnorm_add_quant(int fmt, uint32_t flags, int64_t M, int64_t H, float eps,
                       const void* x, const void* residual_in, void* residual_out,
                       const void* weight, void* q_out, void* scale_out, void* normed_out,
                       sgq_stream_t stream);
+
+/*
+ * Tensor-parallel all-reduce + residual add + RMSNorm + FP8 quantisation in
+ * one launch ([P1] "Purpose" commit 1, the all-reduce + norm entry point, and
+ * "Limitations", a quant-emitting fused all-reduce + norm; [P4] "Change", the
+ * fused all-reduce + RMSNorm + quant of the entry projection). Each of the
+ * nranks ranks of a tensor-parallel group holds a partial [M, H] bf16 result
+ * of the preceding row-parallel GEMM; the all-reduce's output is their sum.
+ * For each row i:
+ *
+ *   x   = bf16(partials[0][i] + partials[1][i] + ... )   (fp32, in rank order)
+ *   then exactly rmsnorm_add_quant of x, residual_in, weight.
+ *
+ * So the result equals rmsnorm_add_quant applied to that x, bit for bit.
+ * "One shot": every rank calls it over all M rows, reading every rank's
+ * partial. "Two shot": each rank calls it on its own slice of rows (pointers
+ * offset by the slice's first row, M = the slice's rows), then the ranks
+ * gather the slices' outputs (the quantised rows are half the bf16 bytes).
+ *
+ * Arguments as for rmsnorm_add_quant, except:
+ *   flags         SGQ_F_GEMMA_WEIGHT | SGQ_F_QUANT_FROM_FP32 and a scale layout
+ *                 flag of the format (bf16 activations only)
+ *   nranks        1 .. SGQ_MAX_RANKS
+ *   H             a multiple of the format's group, at most SGQ_MAX_DUAL_WIDTH
+ *   partials      HOST array of nranks DEVICE pointers, each [M, H] bf16, read;
+ *                 on a multi-GPU node these may be other GPUs' memory mapped
+ *                 into this one (peer access), read with plain loads. The
+ *                 caller makes every partial complete and visible before the
+ *                 launch begins (e.g. a barrier among the ranks): the kernel
+ *                 waits for nothing. Partials may overlap each other and the
+ *                 inputs; no output may overlap any of them.
+ * SGQ_ERR_UNSUPPORTED also when the staging of nranks partials would need
+ * more shared memory than a CTA has (wide rows with many ranks).
+ */
+int allreduce_rmsnorm_add_quant(int fmt, uint32_t flags, int nranks, int64_t M, int64_t H, float eps,
+                                const void* const* partials, const void* residual_in, void* residual_out,
+                                const void* weight, void* q_out, void* scale_out, void* normed_out,
+                                sgq_stream_t stream);
 
 /*
  * SwiGLU + FP8 quantisation, one pass per row ([P1] "Purpose", commit 2 and

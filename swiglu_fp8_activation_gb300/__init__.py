@@ -24,4 +24,5 @@ from .binding import (  # noqa: F401
     SCALE_LAYOUTS, scale_shape,
     SgqError, library, library_path, rmsnorm_add_quant, swiglu_quant, status_string,
     rmsnorm_add, swiglu, quantize_fp8, rmsnorm_dual_quant, NormSeg, F_FP16, set_sm_budget,
+    allreduce_rmsnorm_add_quant, MAX_RANKS,
 )

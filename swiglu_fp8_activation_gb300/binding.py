@@ -76,6 +76,9 @@ def library() -> C.CDLL:
         L.sgq_abi_version.argtypes = []
         L.sgq_launch_error.restype = C.c_char_p
         L.sgq_launch_error.argtypes = []
+        L.allreduce_rmsnorm_add_quant.restype = C.c_int
+        L.allreduce_rmsnorm_add_quant.argtypes = [C.c_int, C.c_uint32, C.c_int, i64, i64, C.c_float,
+                                                  C.POINTER(C.c_void_p), vp, vp, vp, vp, vp, vp, vp]
         L.sgq_set_sm_budget.restype = C.c_int
         L.sgq_set_sm_budget.argtypes = [C.c_int]
         _lib = L
@@ -351,3 +354,54 @@ def rmsnorm_dual_quant(xa: torch.Tensor, wa: torch.Tensor, xb: torch.Tensor, wb:
                                       _stream(stream))
     _check(st, "rmsnorm_dual_quant")
     return outs[0], outs[1]
+
+
+MAX_RANKS = 8
+
+
+def allreduce_rmsnorm_add_quant(partials: list, weight: torch.Tensor, *, fmt: str = "mxfp8",
+                                residual_in: torch.Tensor | None = None,
+                                residual_out: torch.Tensor | None = None, eps: float = 1e-6,
+                                gemma: bool = True, quant_from_fp32: bool = False, normed: bool = False,
+                                q_out: torch.Tensor | None = None, scale_out: torch.Tensor | None = None,
+                                normed_out: torch.Tensor | None = None, scale_layout: str = "row", stream=None):
+    """Tensor-parallel all-reduce + residual add + RMSNorm + FP8 quantisation
+    (one kernel launch): x = bf16 of the partials' fp32 sum in rank order,
+    then rmsnorm_add_quant(x, ...). partials: the ranks' [M, H] bf16 tensors
+    (this device's memory, or peers' mapped into it); every partial must be
+    complete before the launch. Returns (q, scale, normed or None,
+    residual_out or None); residual_out defaults to residual_in.
+    """
+    if not 1 <= len(partials) <= MAX_RANKS:
+        raise SgqError(f"partials: 1 to {MAX_RANKS} tensors, got {len(partials)}")
+    M, H = partials[0].shape
+    for k, p in enumerate(partials):
+        _want(p, (M, H), torch.bfloat16, f"partials[{k}]")
+    _want(weight, (H,), torch.bfloat16, "weight")
+    if residual_in is not None:
+        _want(residual_in, (M, H), torch.bfloat16, "residual_in")
+        if residual_out is None:
+            residual_out = residual_in
+    if residual_out is not None:
+        _want(residual_out, (M, H), torch.bfloat16, "residual_out")
+    if fmt not in FORMATS:
+        raise SgqError(f"unknown format {fmt!r}")
+    dev = partials[0].device
+    lflag = _layout_flag(fmt, scale_layout)
+    if q_out is None:
+        q_out = torch.empty((M, H), dtype=torch.uint8, device=dev)
+    if scale_out is None:
+        scale_out = torch.empty(scale_shape(fmt, M, H, scale_layout), dtype=scale_dtype(fmt), device=dev)
+    if normed and normed_out is None:
+        normed_out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    _want(q_out, (M, H), torch.uint8, "q_out")
+    _want(scale_out, scale_shape(fmt, M, H, scale_layout), scale_dtype(fmt), "scale_out")
+    if normed_out is not None:
+        _want(normed_out, (M, H), torch.bfloat16, "normed_out")
+    flags = (F_GEMMA_WEIGHT if gemma else 0) | (F_QUANT_FROM_FP32 if quant_from_fp32 else 0) | lflag
+    ptrs = (C.c_void_p * len(partials))(*[p.data_ptr() for p in partials])
+    st = library().allreduce_rmsnorm_add_quant(FORMATS[fmt], flags, len(partials), M, H, float(eps), ptrs,
+                                               _ptr(residual_in), _ptr(residual_out), _ptr(weight), _ptr(q_out),
+                                               _ptr(scale_out), _ptr(normed_out), _stream(stream))
+    _check(st, "allreduce_rmsnorm_add_quant")
+    return q_out, scale_out, normed_out, residual_out

@@ -188,6 +188,9 @@ bool plan_launch(int64_t M, int W, const sgq::ScaleOut& so, const Device& dev, s
     return true;
 }
 
+// Dynamic shared memory one CTA may use (227 KB on sm_100-class parts).
+constexpr int kMaxDynamicSmem = 227 * 1024;
+
 // Chunks (8 columns) one CTA of the row engine covers: kMaxTPR threads with
 // kMaxNV chunks each, 16384 columns.
 constexpr int kCtaChunks = sgq::kMaxTPR * sgq::kMaxNV;
@@ -329,6 +332,7 @@ int norm_call(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, const vo
     a.eps = eps;
     a.flags = flags;
     a.segc = segc;
+    a.nparts = 0;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     return launched(wide ? sgq::launch_norm_cluster(fmt, dt_of(flags), plan, a, st)
                          : sgq::launch_norm(fmt, dt_of(flags), plan, a, st));
@@ -542,6 +546,74 @@ int rmsnorm_add(uint32_t flags, int64_t M, int64_t H, float eps, const void* x, 
                      normed_out, stream);
 }
 
+int allreduce_rmsnorm_add_quant(int fmt, uint32_t flags, int nranks, int64_t M, int64_t H, float eps,
+                                const void* const* partials, const void* residual_in, void* residual_out,
+                                const void* weight, void* q_out, void* scale_out, void* normed_out,
+                                sgq_stream_t stream) {
+    if (fmt < SGQ_FMT_MXFP8 || fmt > SGQ_FMT_FP8_PER_TOKEN) return SGQ_ERR_INVALID_ARG;
+    if (flags & ~(SGQ_F_GEMMA_WEIGHT | SGQ_F_QUANT_FROM_FP32 | kLayoutFlags)) return SGQ_ERR_INVALID_ARG;
+    if (nranks < 1 || nranks > SGQ_MAX_RANKS || !partials) return SGQ_ERR_INVALID_ARG;
+    if (M < 0 || H <= 0 || !(eps >= 0.0f) || isinf(eps)) return SGQ_ERR_INVALID_ARG;
+    if (H % group_of(fmt) != 0 || H % 8 != 0 || H / 8 > kCtaChunks) return SGQ_ERR_UNSUPPORTED;
+    if (M > kMaxElements / H) return SGQ_ERR_INVALID_ARG;
+    if (M == 0) return SGQ_OK;
+    if (!weight || !q_out || !scale_out) return SGQ_ERR_INVALID_ARG;
+    if (residual_out && !residual_in) return SGQ_ERR_INVALID_ARG;
+    for (int r = 0; r < nranks; ++r)
+        if (!partials[r]) return SGQ_ERR_INVALID_ARG;
+    sgq::ScaleOut so;
+    size_t sbytes = 0;
+    if (!scale_geometry(fmt, flags, M, H, &so, &sbytes)) return SGQ_ERR_INVALID_ARG;
+    for (int r = 0; r < nranks; ++r)
+        if (!aligned(partials[r], 16)) return SGQ_ERR_MISALIGNED;
+    if (!aligned(residual_in, 16) || !aligned(residual_out, 16) || !aligned(weight, 16) || !aligned(q_out, 16) ||
+        !aligned(normed_out, 16) || !aligned(scale_out, fmt == SGQ_FMT_MXFP8 ? 1 : 4))
+        return SGQ_ERR_MISALIGNED;
+    const size_t act = (size_t)M * (size_t)H * 2;
+    const void* r_out_span = residual_out == residual_in ? nullptr : residual_out;
+    // outputs may overlap nothing; the inputs (partials, residual, weight) may overlap each other
+    const Span outs[] = {{q_out, (size_t)M * H}, {scale_out, sbytes}, {normed_out, act}, {r_out_span, act}};
+    if (any_overlap(outs, 4)) return SGQ_ERR_INVALID_ARG;
+    for (const Span& o : outs) {
+        for (int r = 0; r < nranks; ++r)
+            if (overlap(o.p, o.n, partials[r], act)) return SGQ_ERR_INVALID_ARG;
+        if (overlap(o.p, o.n, weight, (size_t)H * 2)) return SGQ_ERR_INVALID_ARG;
+        if (o.p != r_out_span && overlap(o.p, o.n, residual_in, act)) return SGQ_ERR_INVALID_ARG;
+    }
+    if (overlap(r_out_span, act, residual_in, act)) return SGQ_ERR_INVALID_ARG;
+
+    // whole rows with the plain norm's plan (so the sum of squares is added
+    // in the same order as rmsnorm_add_quant's), each partial staged
+    const Device dev = current_device();
+    sgq::Plan plan;
+    if (!sgq::plan_rows(so.Ms, (int)H, dev.sms, &plan)) return SGQ_ERR_UNSUPPORTED;
+    plan.device = dev.id;
+    plan.full = plan.full && so.Ms == M;
+    if (sgq::norm_ar_stage_bytes(residual_in != nullptr, nranks, plan.nv, plan.rpc * plan.tpr) > kMaxDynamicSmem)
+        return SGQ_ERR_UNSUPPORTED;
+    sgq::NormArgs a;
+    a.x = nullptr;
+    a.r_in = static_cast<const uint16_t*>(residual_in);
+    a.r_out = static_cast<uint16_t*>(residual_out);
+    a.w = static_cast<const uint16_t*>(weight);
+    a.q = static_cast<uint8_t*>(q_out);
+    so.p = scale_out;
+    a.so = so;
+    a.normed = static_cast<uint16_t*>(normed_out);
+    a.M = M;
+    a.ldx = H;
+    a.H = (int)H;
+    a.tpr = plan.tpr;
+    a.rpc = plan.rpc;
+    a.eps = eps;
+    a.flags = flags;
+    a.segc = (int)(H / 8);
+    a.nparts = nranks;
+    for (int r = 0; r < sgq::kMaxRanks; ++r)
+        a.part[r] = static_cast<const uint16_t*>(partials[r < nranks ? r : 0]);
+    return launched(sgq::launch_norm_ar(fmt, plan, a, static_cast<cudaStream_t>(stream)));
+}
+
 int swiglu_quant(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float alpha, float beta,
                  float limit, const void* gate_up, void* q_out, void* scale_out, sgq_stream_t stream) {
     if (fmt < SGQ_FMT_MXFP8 || fmt > SGQ_FMT_FP8_PER_TOKEN) return SGQ_ERR_INVALID_ARG;
@@ -673,6 +745,7 @@ int rmsnorm_dual_quant(int fmt, uint32_t flags, int64_t M, float eps, const sgq_
         a.eps = eps;
         a.flags = flags;
         a.segc = (int)(s.H / 8);   // whole rows
+        a.nparts = 0;
     }
     d.grid0 = grid0;
     return launched(sgq::launch_norm_dual(fmt, dt_of(flags), plan, d, static_cast<cudaStream_t>(stream)));

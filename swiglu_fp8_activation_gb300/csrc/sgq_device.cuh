@@ -45,6 +45,7 @@ constexpr int kMaxNV = 4;          // chunks per thread
 constexpr int kMaxTPR = 512;       // threads per row (one CTA covers kMaxTPR * kMaxNV * 8 columns)
 constexpr int kTargetCTA = 256;    // threads per CTA when several rows share one
 constexpr int kMaxCluster = 8;     // CTAs a row at most when a row is wider than one CTA covers
+constexpr int kMaxRanks = 8;       // partial inputs of the all-reduce folded into the norm
 
 // ----------------------------------------------------------------- memory
 

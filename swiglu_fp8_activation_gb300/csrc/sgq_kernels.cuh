@@ -43,6 +43,8 @@ struct NormArgs {
     float eps;
     uint32_t flags;
     int segc;                // output chunks a column segment (SEG) or cluster CTA (CL); H / 8 for whole rows
+    int nparts;              // AR: partial inputs summed into x (x itself unused)
+    const uint16_t* part[kMaxRanks];   // AR: the ranks' partial [M, H] rows
 };
 
 struct SwigluArgs {
@@ -220,6 +222,10 @@ __host__ __device__ constexpr bool norm_z_in_smem(int fmt) { return fmt == FMT_P
 // segc a multiple of 32, so that a warp's chunks are all in or all out. The
 // host never splits an in-place residual update, which another CTA of the row
 // would read back.
+// AR: x is the all-reduce of a.nparts partial inputs (the tensor-parallel
+// ranks' [M, H] rows): their sum in fp32, in rank order, rounded once to the
+// activation type, as an all-reduce's output would be; each partial is
+// staged in a shared-memory slot of its own beside r and w.
 // CL: a row wider than one CTA covers, split over the CTAs of a cluster (one
 // row per cluster, blk = the row): CTA k of the cluster reads, computes and
 // writes only chunks [k * segc, min((k + 1) * segc, H / 8)), segc a multiple
@@ -227,11 +233,15 @@ __host__ __device__ constexpr bool norm_z_in_smem(int fmt) { return fmt == FMT_P
 // rank order through shared memory (cluster_combine), so every CTA of the row
 // gets the bit-identical inv. Each CTA reads only its own columns, so an
 // in-place residual update is safe here too.
-template <int FMT, int LAYOUT, int NV, bool HAS_RES, bool FULL, int DT, bool SEG = false, bool CL = false>
+template <int FMT, int LAYOUT, int NV, bool HAS_RES, bool FULL, int DT, bool SEG = false, bool CL = false,
+          bool AR = false>
 __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
     extern __shared__ uint4 stage[];
     __shared__ float2 part[32];
     constexpr int NIN = norm_stage_inputs(HAS_RES);
+    // shared-memory slots a chunk: x (AR: one for each partial), r, w
+    const int nslot = AR ? a.nparts + NIN - 1 : NIN;
+    const int ir = AR ? a.nparts : 1, iw = nslot - 1;
     const int tpr = a.tpr;
     const int nt = blockDim.x;
     const int lrow = threadIdx.x / tpr;
@@ -240,7 +250,7 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
     const bool row_ok = FULL || row < a.M;
     const int H = a.H, nchunks = H >> 3;
     const int64_t base = row * (int64_t)H;
-    auto slot = [&](int v, int i) { return &stage[(NIN * v + i) * nt + threadIdx.x]; };
+    auto slot = [&](int v, int i) { return &stage[(nslot * v + i) * nt + threadIdx.x]; };
     const int cb = SEG ? (int)blockIdx.y * a.segc : CL ? (int)cluster_rank() * a.segc : 0;   // the chunks this CTA writes
     const int cend = SEG ? cb + a.segc : CL ? min(cb + a.segc, nchunks) : nchunks;
     const int c0 = CL ? cb : 0;              // chunk of thread 0's first copy (CL: the segment's first)
@@ -259,8 +269,7 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
     for (int v = 0; v < NV; ++v) {
         const int c = c0 + t + v * tpr;
         const bool okw = (FULL || (row_ok && c < clim)) && (!SEG || FMT == FMT_PT || (c >= cb && c < cend));
-        cp_async16_cached(slot(v, NIN - 1), okw ? (const void*)(a.w + (int64_t)c * 8) : (const void*)a.w,
-                          okw ? 16 : 0);
+        cp_async16_cached(slot(v, iw), okw ? (const void*)(a.w + (int64_t)c * 8) : (const void*)a.w, okw ? 16 : 0);
     }
     cp_async_commit();
     pdl_wait();
@@ -269,9 +278,14 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
         const int c = c0 + t + v * tpr;
         const bool ok = FULL || (row_ok && c < clim);      // else zero-fill, reading nothing
         const int nb = ok ? 16 : 0;
-        cp_async16(slot(v, 0), ok ? (const void*)(a.x + row * a.ldx + (int64_t)c * 8) : (const void*)a.x, nb);
+        if (AR) {
+            for (int p = 0; p < a.nparts; ++p)
+                cp_async16(slot(v, p), ok ? (const void*)(a.part[p] + base + (int64_t)c * 8) : (const void*)a.w, nb);
+        } else {
+            cp_async16(slot(v, 0), ok ? (const void*)(a.x + row * a.ldx + (int64_t)c * 8) : (const void*)a.x, nb);
+        }
         if (HAS_RES)
-            cp_async16(slot(v, 1), ok ? (const void*)(a.r_in + base + (int64_t)c * 8) : (const void*)a.x, nb);
+            cp_async16(slot(v, ir), ok ? (const void*)(a.r_in + base + (int64_t)c * 8) : (const void*)a.w, nb);
         cp_async_commit();
     }
     pdl_trigger();
@@ -298,9 +312,22 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
             float h[8], wf[8];
             cp_async_wait_group_of<NV>(v);
             load8<DT>(ld_smem16(slot(v, 0)), h);
+            if (AR) {                        // x = the partials' sum in rank order, rounded to DT
+                for (int p = 1; p < a.nparts; ++p) {
+                    float pf[8];
+                    load8<DT>(ld_smem16(slot(v, p)), pf);
+#pragma unroll
+                    for (int k = 0; k < 8; k += 2) {
+                        const float2 hs = __fadd2_rn(make_float2(h[k], h[k + 1]), make_float2(pf[k], pf[k + 1]));
+                        h[k] = hs.x;
+                        h[k + 1] = hs.y;
+                    }
+                }
+                load8<DT>(pack8<DT>(h), h);
+            }
             if (HAS_RES) {
                 float rf[8];
-                load8<DT>(ld_smem16(slot(v, 1)), rf);
+                load8<DT>(ld_smem16(slot(v, ir)), rf);
 #pragma unroll
                 for (int k = 0; k < 8; k += 2) {
                     const float2 hs = __fadd2_rn(make_float2(h[k], h[k + 1]), make_float2(rf[k], rf[k + 1]));
@@ -321,7 +348,7 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
                 }
                 continue;
             }
-            load8<DT>(ld_smem16(slot(v, NIN - 1)), wf);
+            load8<DT>(ld_smem16(slot(v, iw)), wf);
 #pragma unroll
             for (int k = 0; k < 8; k += 2) {
                 const float2 hp = make_float2(h[k], h[k + 1]);
@@ -335,7 +362,7 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
             }
             if (ZS) {   // over this thread's own x and weight slots of chunk v, both read above
                 *reinterpret_cast<float4*>(slot(v, 0)) = make_float4(z[v][0], z[v][1], z[v][2], z[v][3]);
-                *reinterpret_cast<float4*>(slot(v, NIN - 1)) = make_float4(z[v][4], z[v][5], z[v][6], z[v][7]);
+                *reinterpret_cast<float4*>(slot(v, iw)) = make_float4(z[v][4], z[v][5], z[v][6], z[v][7]);
             }
         }
     };
@@ -387,7 +414,7 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
             float y[8], src[8], zc[8];
             if (ZS) {
                 const float4 lo = *reinterpret_cast<const float4*>(slot(v, 0));
-                const float4 hi = *reinterpret_cast<const float4*>(slot(v, NIN - 1));
+                const float4 hi = *reinterpret_cast<const float4*>(slot(v, iw));
                 zc[0] = lo.x, zc[1] = lo.y, zc[2] = lo.z, zc[3] = lo.w;
                 zc[4] = hi.x, zc[5] = hi.y, zc[6] = hi.z, zc[7] = hi.w;
             } else {
@@ -422,6 +449,18 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
 template <int FMT, int LAYOUT, int NV, bool HAS_RES, bool FULL, int DT>
 __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
     norm_rows<FMT, LAYOUT, NV, HAS_RES, FULL, DT, !FULL>(a, blockIdx.x);
+}
+
+// All-reduce + residual add + RMSNorm + quantisation: x is the sum of
+// a.nparts partial inputs (AR above); bf16 rows, no column segments.
+template <int FMT, int LAYOUT, int NV, bool HAS_RES, bool FULL>
+__global__ void __launch_bounds__(kMaxTPR) norm_ar_kernel(const NormArgs a) {
+    norm_rows<FMT, LAYOUT, NV, HAS_RES, FULL, DT_BF16, false, false, true>(a, blockIdx.x);
+}
+
+// Bytes of dynamic shared memory the all-reduce norm stages its loads in.
+__host__ __device__ constexpr int norm_ar_stage_bytes(bool has_res, int nparts, int nv, int threads) {
+    return nv * (norm_stage_inputs(has_res) - 1 + nparts) * threads * 16;
 }
 
 // Rows wider than one CTA covers: a cluster of gridDim.x / M CTAs a row

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_function(sgq_lib):
     names = _declared_functions()
     assert set(names) == {"rmsnorm_add_quant", "swiglu_quant", "rmsnorm_add", "swiglu", "quantize_fp8",
                           "rmsnorm_dual_quant", "sgq_status_string", "sgq_abi_version", "sgq_launch_error",
-                          "sgq_set_sm_budget"}
+                          "sgq_set_sm_budget", "allreduce_rmsnorm_add_quant"}
     for n in names:
         assert hasattr(sgq_lib, n), n
     m = re.search(r"#define SGQ_ABI_VERSION (\d+)", _header())
@@ -296,3 +296,32 @@ def test_dual_norm_argument_errors(sgq_lib):
     assert dual(L, a=_seg(n=7)) == INVALID            # two outputs in one place
     assert dual(L, a=_seg(q=5)) == INVALID            # an output over an input
     assert dual(L, M=1 << 45, a=_seg(H=16384)) == INVALID
+
+
+def allreduce(lib, fmt=0, flags=1, n=2, M=8, H=256, eps=1e-6, parts=None, r=_p(2), ro=_p(3), w=_p(4), q=_p(5),
+              s=_p(6), nrm=_p(7)):
+    if parts is None:
+        parts = [_p(0), _p(1)][:n] + [_p(8 + k) for k in range(max(0, n - 2))]
+    arr = (C.c_void_p * max(1, len(parts)))(*parts)
+    return _host_checked(lib.allreduce_rmsnorm_add_quant(fmt, flags, n, M, H, eps, arr, r, ro, w, q, s, nrm, None))
+
+
+def test_allreduce_norm_argument_errors(sgq_lib):
+    L = sgq_lib
+    L.allreduce_rmsnorm_add_quant.restype = C.c_int
+    L.allreduce_rmsnorm_add_quant.argtypes = [C.c_int, C.c_uint32, C.c_int, C.c_int64, C.c_int64, C.c_float,
+                                              C.POINTER(C.c_void_p)] + [C.c_void_p] * 7
+    assert allreduce(L, M=0) == OK                           # empty: no launch
+    assert allreduce(L, n=0, parts=[]) == INVALID
+    assert allreduce(L, n=9) == INVALID                      # above SGQ_MAX_RANKS
+    assert allreduce(L, flags=1 << 5) == INVALID             # bf16 only
+    assert allreduce(L, fmt=3) == INVALID
+    assert allreduce(L, parts=[_p(0), None]) == INVALID      # a null partial
+    assert allreduce(L, parts=[_p(0), C.c_void_p(BASE + 64 * MB + 2)]) == MISALIGNED
+    assert allreduce(L, H=48) == UNSUPPORTED                 # MX group
+    assert allreduce(L, H=16384 + 32) == UNSUPPORTED         # whole rows only
+    assert allreduce(L, q=_p(1)) == INVALID                  # an output over a partial
+    assert allreduce(L, nrm=_p(0)) == INVALID
+    assert allreduce(L, r=None) == INVALID                   # residual_out without residual_in
+    assert allreduce(L, w=None) == INVALID
+    assert allreduce(L, n=8, H=16384, M=1024) == UNSUPPORTED     # eight staged partials of a 16384 row do not fit
