@@ -311,8 +311,8 @@ int norm_call(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, const vo
         const int seg = residual_out && residual_out == residual_in ? 1 : norm_segments(so.Ms, H, sms);
         if (!sgq::plan_rows(so.Ms, (int)H, sms, &plan)) return SGQ_ERR_UNSUPPORTED;
         plan.device = dev.id;
-        plan.full = plan.full && so.Ms == M && seg == 1;   // the exact-fit kernels write whole rows
         plan.seg = seg;
+        plan.full = plan.full && so.Ms == M && seg == 1;   // the exact-fit kernels write whole rows
         segc = (int)(H / 8 / seg);
     }
     sgq::NormArgs a;

@@ -73,7 +73,11 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 template <int NV>
 __device__ __forceinline__ void cp_async_wait_group_of(int v) {
     const int pending = NV - 1 - v;
-    if (pending >= 3) cp_async_wait<3>();
+    if (pending >= 7) cp_async_wait<7>();
+    else if (pending == 6) cp_async_wait<6>();
+    else if (pending == 5) cp_async_wait<5>();
+    else if (pending == 4) cp_async_wait<4>();
+    else if (pending == 3) cp_async_wait<3>();
     else if (pending == 2) cp_async_wait<2>();
     else if (pending == 1) cp_async_wait<1>();
     else cp_async_wait<0>();
