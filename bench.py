@@ -839,7 +839,8 @@ def run_profile(args):
     source) at W=4096, M=256 (the Qwen3-like workload's largest M).
     norm8: the decode norm (add + Gemma RMSNorm + MXFP8 + bf16 copy, separate
     residual output) at M=8, H=6144, inputs resident in L2; norm8_inplace:
-    the same with the residual updated in place (whole rows, one CTA each)."""
+    the same with the residual updated in place (whole rows, one CTA each);
+    norm192 / norm192_inplace: the same at M=192."""
     import torch
     dev = torch.device("cuda", 0)
     if args.profile in ("silu128", "silu128_m256"):
@@ -857,16 +858,16 @@ def run_profile(args):
         fn = lib.swiglu_quant
         nbytes = swiglu_bytes(M, I, "block128")
         get = lambda k: arglist[k % ROTATE]
-    elif args.profile in ("norm8", "norm8_inplace"):
+    elif args.profile in ("norm8", "norm8_inplace", "norm192", "norm192_inplace"):
         from swiglu_fp8_activation_gb300 import inputs, library
         import ctypes as C
-        case = inputs.norm_case_gemma_mx(8)
+        case = inputs.norm_case_gemma_mx(192 if args.profile.startswith("norm192") else 8)
         t = inputs.make_norm(case)
         x, r, w = (t[k].to(dev) for k in ("x", "r", "w"))
         q = torch.empty(case.M, case.H, dtype=torch.uint8, device=dev)
         sc = torch.empty(case.M, case.H // 32, dtype=torch.uint8, device=dev)
         nrm = torch.empty(case.M, case.H, dtype=torch.bfloat16, device=dev)
-        ro = r if args.profile == "norm8_inplace" else torch.empty_like(nrm)
+        ro = r if args.profile.endswith("_inplace") else torch.empty_like(nrm)
         lib = library()
         stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
         ptr = lambda a: C.c_void_p(a.data_ptr())
@@ -922,7 +923,7 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle time")
     ap.add_argument("--quick", action="store_true", help="skip the decode and other-config tables")
     ap.add_argument("--profile", choices=("norm", "swiglu", "pertoken", "silu128", "silu128_m256", "norm128_m256",
-                                          "norm8", "norm8_inplace"),
+                                          "norm8", "norm8_inplace", "norm192", "norm192_inplace"),
                     help="time one kernel only (for ncu)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
