@@ -5,7 +5,7 @@
 namespace sgq {
 
 namespace {
-using NormKernel = void (*)(const NormArgs);
+using NormKernel = void (*)(const NormARArgs);
 
 template <int FMT, int LAYOUT, bool RES, bool FULL>
 NormKernel pick_nv(int nv) {
@@ -29,12 +29,12 @@ NormKernel pick_fmt(int fmt, int layout, int nv) {
 }
 }  // namespace
 
-cudaError_t launch_norm_ar(int fmt, const Plan& p, const NormArgs& a, cudaStream_t stream) {
-    const int l = a.so.layout;
-    const bool res = a.r_in != nullptr;
+cudaError_t launch_norm_ar(int fmt, const Plan& p, const NormARArgs& aa, cudaStream_t stream) {
+    const int l = aa.a.so.layout;
+    const bool res = aa.a.r_in != nullptr;
     NormKernel k = res ? (p.full ? pick_fmt<true, true>(fmt, l, p.nv) : pick_fmt<true, false>(fmt, l, p.nv))
                        : (p.full ? pick_fmt<false, true>(fmt, l, p.nv) : pick_fmt<false, false>(fmt, l, p.nv));
-    return launch_pdl(k, p, a, stream, norm_ar_stage_bytes(res, a.nparts, p.nv, p.rpc * p.tpr));
+    return launch_pdl(k, p, aa, stream, norm_ar_stage_bytes(res, aa.ar.n, p.nv, p.rpc * p.tpr));
 }
 
 }  // namespace sgq

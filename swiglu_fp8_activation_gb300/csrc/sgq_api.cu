@@ -332,7 +332,6 @@ int norm_call(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, const vo
     a.eps = eps;
     a.flags = flags;
     a.segc = segc;
-    a.nparts = 0;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     return launched(wide ? sgq::launch_norm_cluster(fmt, dt_of(flags), plan, a, st)
                          : sgq::launch_norm(fmt, dt_of(flags), plan, a, st));
@@ -582,16 +581,24 @@ int allreduce_rmsnorm_add_quant(int fmt, uint32_t flags, int nranks, int64_t M, 
     }
     if (overlap(r_out_span, act, residual_in, act)) return SGQ_ERR_INVALID_ARG;
 
-    // whole rows with the plain norm's plan (so the sum of squares is added
-    // in the same order as rmsnorm_add_quant's), each partial staged
+    // the plain norm's plan and column segments (so the sum of squares is
+    // added in the same order as rmsnorm_add_quant's), each partial staged
     const Device dev = current_device();
+    // Column segments only at the smallest M: each segment's CTA reads every
+    // rank's partial of the whole row, so the reads grow with ranks x
+    // segments (TP4 at M = 1 / 8: 2.55 / 2.51 -> 2.13 / 2.20 us with them;
+    // TP8 at M = 64: 2.98 -> 3.17 us, slower).
+    const int seg = (residual_out && residual_out == residual_in) || so.Ms * nranks > 64
+                        ? 1 : norm_segments(so.Ms, H, dev.sms);
     sgq::Plan plan;
     if (!sgq::plan_rows(so.Ms, (int)H, dev.sms, &plan)) return SGQ_ERR_UNSUPPORTED;
     plan.device = dev.id;
-    plan.full = plan.full && so.Ms == M;
+    plan.full = plan.full && so.Ms == M && seg == 1;
+    plan.seg = seg;
     if (sgq::norm_ar_stage_bytes(residual_in != nullptr, nranks, plan.nv, plan.rpc * plan.tpr) > kMaxDynamicSmem)
         return SGQ_ERR_UNSUPPORTED;
-    sgq::NormArgs a;
+    sgq::NormARArgs aa;
+    sgq::NormArgs& a = aa.a;
     a.x = nullptr;
     a.r_in = static_cast<const uint16_t*>(residual_in);
     a.r_out = static_cast<uint16_t*>(residual_out);
@@ -607,11 +614,11 @@ int allreduce_rmsnorm_add_quant(int fmt, uint32_t flags, int nranks, int64_t M, 
     a.rpc = plan.rpc;
     a.eps = eps;
     a.flags = flags;
-    a.segc = (int)(H / 8);
-    a.nparts = nranks;
+    a.segc = (int)(H / 8 / seg);
+    aa.ar.n = nranks;
     for (int r = 0; r < sgq::kMaxRanks; ++r)
-        a.part[r] = static_cast<const uint16_t*>(partials[r < nranks ? r : 0]);
-    return launched(sgq::launch_norm_ar(fmt, plan, a, static_cast<cudaStream_t>(stream)));
+        aa.ar.p[r] = static_cast<const uint16_t*>(partials[r < nranks ? r : 0]);
+    return launched(sgq::launch_norm_ar(fmt, plan, aa, static_cast<cudaStream_t>(stream)));
 }
 
 int swiglu_quant(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float alpha, float beta,
@@ -745,7 +752,6 @@ int rmsnorm_dual_quant(int fmt, uint32_t flags, int64_t M, float eps, const sgq_
         a.eps = eps;
         a.flags = flags;
         a.segc = (int)(s.H / 8);   // whole rows
-        a.nparts = 0;
     }
     d.grid0 = grid0;
     return launched(sgq::launch_norm_dual(fmt, dt_of(flags), plan, d, static_cast<cudaStream_t>(stream)));

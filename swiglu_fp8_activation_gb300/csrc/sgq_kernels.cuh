@@ -43,8 +43,19 @@ struct NormArgs {
     float eps;
     uint32_t flags;
     int segc;                // output chunks a column segment (SEG) or cluster CTA (CL); H / 8 for whole rows
-    int nparts;              // AR: partial inputs summed into x (x itself unused)
-    const uint16_t* part[kMaxRanks];   // AR: the ranks' partial [M, H] rows
+};
+
+// The all-reduce norm's partial inputs: the tensor-parallel ranks' [M, H]
+// rows, summed into x (NormArgs::x is then unused). A parameter of that
+// kernel alone, so the other norms' launches carry none of it.
+struct ARParts {
+    int n;
+    const uint16_t* p[kMaxRanks];
+};
+
+struct NormARArgs {
+    NormArgs a;
+    ARParts ar;
 };
 
 struct SwigluArgs {
@@ -222,7 +233,7 @@ __host__ __device__ constexpr bool norm_z_in_smem(int fmt) { return fmt == FMT_P
 // segc a multiple of 32, so that a warp's chunks are all in or all out. The
 // host never splits an in-place residual update, which another CTA of the row
 // would read back.
-// AR: x is the all-reduce of a.nparts partial inputs (the tensor-parallel
+// AR: x is the all-reduce of ar->n partial inputs (the tensor-parallel
 // ranks' [M, H] rows): their sum in fp32, in rank order, rounded once to the
 // activation type, as an all-reduce's output would be; each partial is
 // staged in a shared-memory slot of its own beside r and w.
@@ -235,13 +246,14 @@ __host__ __device__ constexpr bool norm_z_in_smem(int fmt) { return fmt == FMT_P
 // in-place residual update is safe here too.
 template <int FMT, int LAYOUT, int NV, bool HAS_RES, bool FULL, int DT, bool SEG = false, bool CL = false,
           bool AR = false>
-__device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
+__device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk, const ARParts* ar = nullptr) {
     extern __shared__ uint4 stage[];
     __shared__ float2 part[32];
     constexpr int NIN = norm_stage_inputs(HAS_RES);
     // shared-memory slots a chunk: x (AR: one for each partial), r, w
-    const int nslot = AR ? a.nparts + NIN - 1 : NIN;
-    const int ir = AR ? a.nparts : 1, iw = nslot - 1;
+    const int nparts = AR ? ar->n : 1;
+    const int nslot = AR ? nparts + NIN - 1 : NIN;
+    const int ir = AR ? nparts : 1, iw = nslot - 1;
     const int tpr = a.tpr;
     const int nt = blockDim.x;
     const int lrow = threadIdx.x / tpr;
@@ -279,8 +291,8 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
         const bool ok = FULL || (row_ok && c < clim);      // else zero-fill, reading nothing
         const int nb = ok ? 16 : 0;
         if (AR) {
-            for (int p = 0; p < a.nparts; ++p)
-                cp_async16(slot(v, p), ok ? (const void*)(a.part[p] + base + (int64_t)c * 8) : (const void*)a.w, nb);
+            for (int p = 0; p < nparts; ++p)
+                cp_async16(slot(v, p), ok ? (const void*)(ar->p[p] + base + (int64_t)c * 8) : (const void*)a.w, nb);
         } else {
             cp_async16(slot(v, 0), ok ? (const void*)(a.x + row * a.ldx + (int64_t)c * 8) : (const void*)a.x, nb);
         }
@@ -315,7 +327,7 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk) {
             cp_async_wait_group_of<NV>(v);
             load8<DT>(ld_smem16(slot(v, 0)), h);
             if (AR) {                        // x = the partials' sum in rank order, rounded to DT
-                for (int p = 1; p < a.nparts; ++p) {
+                for (int p = 1; p < nparts; ++p) {
                     float pf[8];
                     load8<DT>(ld_smem16(slot(v, p)), pf);
 #pragma unroll
@@ -451,10 +463,13 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
 }
 
 // All-reduce + residual add + RMSNorm + quantisation: x is the sum of
-// a.nparts partial inputs (AR above); bf16 rows, no column segments.
+// aa.ar.n partial inputs (AR above); bf16 rows. The bounds-checked kernels
+// may split rows into column segments at small M, as the plain norm does
+// (each segment's CTA sums the partials of the whole row for the sum of
+// squares, and writes its own columns).
 template <int FMT, int LAYOUT, int NV, bool HAS_RES, bool FULL>
-__global__ void __launch_bounds__(kMaxTPR) norm_ar_kernel(const NormArgs a) {
-    norm_rows<FMT, LAYOUT, NV, HAS_RES, FULL, DT_BF16, false, false, true>(a, blockIdx.x);
+__global__ void __launch_bounds__(kMaxTPR) norm_ar_kernel(const NormARArgs aa) {
+    norm_rows<FMT, LAYOUT, NV, HAS_RES, FULL, DT_BF16, !FULL, false, true>(aa.a, blockIdx.x, &aa.ar);
 }
 
 // Bytes of dynamic shared memory the all-reduce norm stages its loads in.

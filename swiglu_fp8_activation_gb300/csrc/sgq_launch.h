@@ -83,8 +83,8 @@ cudaError_t launch_swiglu_silu_full(int fmt, const Plan& p, const SwigluArgs& a,
 cudaError_t launch_swiglu_silu_part(int fmt, const Plan& p, const SwigluArgs& a, cudaStream_t stream);
 cudaError_t launch_quant(int fmt, int dt, const Plan& p, const QuantArgs& a, cudaStream_t stream);
 
-// The norm with the all-reduce of a.nparts partial inputs folded in (bf16).
-cudaError_t launch_norm_ar(int fmt, const Plan& p, const NormArgs& a, cudaStream_t stream);
+// The norm with the all-reduce of aa.ar.n partial inputs folded in (bf16).
+cudaError_t launch_norm_ar(int fmt, const Plan& p, const NormARArgs& aa, cudaStream_t stream);
 
 // Rows wider than one CTA covers, split over a cluster of p.cluster CTAs a
 // row (p.grid = rows * p.cluster, p.rpc = 1, four chunks a thread).
