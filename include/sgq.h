@@ -59,7 +59,9 @@
  *     float32 scale pointer (4 bytes) and an E8M0 scale pointer (1 byte).
  *   - Width rules: MXFP8 needs W % 32 == 0, 1x128 needs W % 128 == 0,
  *     per-token (and the unquantised outputs of rmsnorm_add, swiglu and an
- *     unquantised dual segment) needs W % 8 == 0; W <= SGQ_MAX_WIDTH.
+ *     unquantised dual segment) needs W % 8 == 0; W <= SGQ_MAX_WIDTH
+ *     (SGQ_MAX_DUAL_WIDTH for rmsnorm_dual_quant and
+ *     allreduce_rmsnorm_add_quant).
  *   - Outputs may not overlap inputs or each other, except that residual_out
  *     may equal residual_in exactly (in-place update).
  *   - Launch order: every kernel may begin while the kernel before it on the
@@ -92,7 +94,7 @@ extern "C" {
  * or as column segments where no row-wide value is needed. */
 #define SGQ_MAX_WIDTH 131072
 /* Widest segment of rmsnorm_dual_quant, and widest row of
- * allreduce_rmsnorm_add_quant (one CTA a row). */
+ * allreduce_rmsnorm_add_quant (rows no wider than one CTA covers). */
 #define SGQ_MAX_DUAL_WIDTH 16384
 /* Most partial inputs (tensor-parallel ranks) of allreduce_rmsnorm_add_quant. */
 #define SGQ_MAX_RANKS 8
