@@ -2,7 +2,8 @@
 against the oracle under the same tolerances as the fixed parity tests:
 random formats, flags, activation types, scale layouts and shapes (M from 1
 to a few hundred, widths any multiple of the format's group up to the
-maximum). Cases are drawn once from a fixed seed, so a failure names a
+maximum), then the all-reduce norm over 1 to 8 ranks and rows wider than one
+CTA covers. Cases are drawn once from a fixed seed, so a failure names a
 reproducible configuration."""
 import numpy as np
 import pytest
@@ -147,3 +148,128 @@ def test_random_configuration(c):
         check_bf16("normed_b", rb["normed"], _bits(nb))
         if c["qb"]:
             check_quant(fmt, rb, qb.cpu().numpy(), sb.cpu().numpy(), c["from32"])
+
+
+# --------------------------------------- the all-reduce norm and wide rows
+
+def _wide_width(rng, fmt):
+    g = GROUP[fmt]
+    return int(g * rng.integers(16384 // g + 1, 65536 // g + 1))
+
+
+def _more_cases(n=24, seed=2025):
+    """Seeded configurations of the all-reduce norm (1-8 ranks, every format,
+    residual mode and layout) and of rows wider than one CTA covers (thread
+    block clusters and column segments, every op). Quantisation from fp32
+    only for MXFP8 here, whose power-of-two scales leave no quotient ties:
+    the fixed parity tests cover the ties of fp32-source 1x128 and
+    per-token FP8."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        op = ["allreduce", "wide_norm", "wide_swiglu", "wide_quant"][i % 4]
+        fmt = ["mxfp8", "block128", "per_token"][int(rng.integers(3))]
+        c = {"op": op, "fmt": fmt, "seed": int(rng.integers(1 << 30)),
+             "from32": fmt == "mxfp8" and bool(rng.random() < 0.5), "layout": _layout(rng, fmt)}
+        if op == "allreduce":
+            c.update(W=_width(rng, fmt), n=int(rng.integers(1, 9)), gemma=bool(rng.random() < 0.5),
+                     residual=["none", "separate", "inplace"][int(rng.integers(3))], normed=bool(rng.random() < 0.5))
+            c["M"] = int(rng.integers(1, 65))
+        elif op == "wide_norm":
+            c.update(W=_wide_width(rng, fmt), gemma=bool(rng.random() < 0.5), fp16=bool(rng.random() < 0.3),
+                     residual=["none", "separate", "inplace"][int(rng.integers(3))], normed=bool(rng.random() < 0.5))
+            c["M"] = int(rng.integers(1, 9))
+        elif op == "wide_swiglu":
+            c.update(W=_wide_width(rng, fmt), act=["swiglu_oai", "silu_mul"][int(rng.integers(2))])
+            c["round"] = c["act"] == "silu_mul" and bool(rng.random() < 0.5)
+            c["M"] = int(rng.integers(1, 9))
+        else:
+            c.update(W=_wide_width(rng, fmt), fp16=bool(rng.random() < 0.3), from32=False)
+            c["M"] = int(rng.integers(1, 9))
+        out.append(c)
+    return out
+
+
+MORE_CASES = _more_cases()
+
+
+def _row_scales(fmt, layout, s, M, W):
+    """Row-major scales from a launch's layout (checked against the oracle's rearrangement)."""
+    if layout == "row":
+        return s.cpu().numpy()
+    G = W // (32 if fmt == "mxfp8" else 128)
+    sl = s.cpu().numpy()
+    if layout == "col_major":
+        row = np.ascontiguousarray(sl[:, :M].T)
+    else:
+        flat, Gp = sl.reshape(-1), -(-G // 4) * 4
+        row = np.zeros((M, G), dtype=sl.dtype)
+        for r in range(M):
+            for gi in range(G):
+                rr = r % 128
+                row[r, gi] = flat[((r // 128) * (Gp // 4) + gi // 4) * 512 + (rr % 32) * 16 + (rr // 32) * 4 + gi % 4]
+    np.testing.assert_array_equal(sl, oracle.scale_layout(fmt, row, layout))
+    return row
+
+
+@pytest.mark.parametrize("c", MORE_CASES, ids=_name)
+def test_random_allreduce_and_wide_configuration(c):
+    from swiglu_fp8_activation_gb300 import SgqError, allreduce_rmsnorm_add_quant
+    g = torch.Generator().manual_seed(c["seed"])
+    M, W, fmt, layout = c["M"], c["W"], c["fmt"], c["layout"]
+    if c["op"] in ("allreduce", "wide_norm"):
+        fp16 = c.get("fp16", False)
+        if c["op"] == "allreduce":
+            parts = [_act_tensor(g, M, W, False, 1.0) for _ in range(c["n"])]
+        else:
+            parts = [_act_tensor(g, M, W, fp16)]
+        w = (torch.randn(W, generator=g) * 0.1 + (0.0 if c["gemma"] else 1.0)).to(parts[0].dtype)
+        r = _act_tensor(g, M, W, fp16, 1.0) if c["residual"] != "none" else None
+        rd = r.to(DEV) if r is not None else None
+        ro = None if rd is None else (rd if c["residual"] == "inplace" else torch.empty_like(rd))
+        kw = dict(fmt=fmt, residual_in=rd, residual_out=ro, gemma=c["gemma"], quant_from_fp32=c["from32"],
+                  normed=c["normed"], scale_layout=layout)
+        if c["op"] == "allreduce":
+            pd = [p.to(DEV) for p in parts]
+            try:
+                q, s, n, rout = allreduce_rmsnorm_add_quant(pd, w.to(DEV), **kw)
+            except SgqError as e:
+                # the staging limit: a CTA stages 16 bytes a chunk of every partial and the
+                # residual, at most 2048 chunks; only rows wider than 8192 columns with eight
+                # staged inputs (ranks + residual) reach 227 KB
+                assert e.status == 2 and W > 8192 and c["n"] + (r is not None) >= 8, (e.status, W, c["n"])
+                return
+            summed = pd[0].float()
+            for p in pd[1:]:
+                summed = summed + p.float()     # the kernel's all-reduce: fp32 sum in rank order, then bf16
+            r2 = r.to(DEV) if r is not None else None
+            ro2 = None if r2 is None else (r2 if c["residual"] == "inplace" else torch.empty_like(r2))
+            q2, s2, n2, rout2 = rmsnorm_add_quant(summed.to(torch.bfloat16), w.to(DEV),
+                                                  **{**kw, "residual_in": r2, "residual_out": ro2})
+            torch.cuda.synchronize()
+            assert torch.equal(q, q2) and torch.equal(s, s2)
+            assert (n is None or torch.equal(n, n2)) and (rout is None or torch.equal(rout, rout2))
+            ref = oracle.allreduce_rmsnorm_add_quant(fmt, [_bits(p) for p in parts], _bits(r) if r is not None else None,
+                                                     _bits(w), eps=1e-6, gemma=c["gemma"], from_fp32=c["from32"],
+                                                     normed=c["normed"])
+        else:
+            q, s, n, rout = rmsnorm_add_quant(parts[0].to(DEV), w.to(DEV), **kw)
+            torch.cuda.synchronize()
+            ref = oracle.rmsnorm_add_quant(fmt, _bits(parts[0]), _bits(r) if r is not None else None, _bits(w),
+                                           eps=1e-6, gemma=c["gemma"], from_fp32=c["from32"], normed=c["normed"],
+                                           fp16=fp16)
+        check_norm(fmt, ref, q.cpu().numpy(), _row_scales(fmt, layout, s, M, W), _bits(n) if c["normed"] else None,
+                   _bits(rout) if r is not None else None, from_fp32=c["from32"])
+    elif c["op"] == "wide_swiglu":
+        gu = (torch.randn(M, 2 * W, generator=g) * 3.0).to(torch.bfloat16)
+        q, s = swiglu_quant(gu.to(DEV), fmt=fmt, act=c["act"], quant_from_fp32=c["from32"], round_act_bf16=c["round"],
+                            scale_layout=layout)
+        torch.cuda.synchronize()
+        ref = oracle.swiglu_quant(fmt, c["act"], _bits(gu), from_fp32=c["from32"], round_act_bf16=c["round"])
+        check_swiglu(fmt, ref, q.cpu().numpy(), _row_scales(fmt, layout, s, M, W), from_fp32=c["from32"])
+    else:
+        src = _act_tensor(g, M, W, c["fp16"])
+        q, s = quantize_fp8(src.to(DEV), fmt=fmt, scale_layout=layout)
+        torch.cuda.synchronize()
+        ref = oracle.quantize(fmt, _bits(src), fp16=c["fp16"])
+        check_quant(fmt, ref, q.cpu().numpy(), _row_scales(fmt, layout, s, M, W), from_fp32=False)
