@@ -179,7 +179,8 @@ typedef void* sgq_stream_t;
  *                 scale layout flag of the format (others rejected). With
  *                 SGQ_F_FP16 the bf16 of the formulas above reads fp16.
  *   M, H          rows and hidden width
- *   eps           >= 0, finite
+ *   eps           >= 0, finite; with eps = 0 a row whose h is all zero has no
+ *                 defined result (1/sqrt(0); its outputs are unspecified)
  *   x             [M, H] bf16, read
  *   residual_in   [M, H] bf16, read, or NULL
  *   residual_out  [M, H] bf16, written, or NULL; must be NULL when residual_in
@@ -354,7 +355,7 @@ typedef struct sgq_norm_seg {
  *   fmt           sgq_format_t (both segments)
  *   flags         SGQ_F_GEMMA_WEIGHT | SGQ_F_QUANT_FROM_FP32 | SGQ_F_FP16
  *   M             rows of both segments
- *   eps           >= 0, finite
+ *   eps           >= 0, finite (eps = 0 and an all-zero row: as rmsnorm_add_quant)
  *   seg_a, seg_b  host pointers to the two segments (read during the call
  *                 only); H a multiple of the format's group when the segment
  *                 is quantised, else of 8; H <= SGQ_MAX_DUAL_WIDTH
