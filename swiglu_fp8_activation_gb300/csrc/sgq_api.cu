@@ -68,6 +68,46 @@ std::unordered_map<const void*, int> smem_granted[64];
 
 void note_launch_error(cudaError_t e) { last_launch_error = e; }
 
+namespace {
+struct OccKey {
+    const void* k;
+    int device, threads, smem;
+    bool operator==(const OccKey& o) const {
+        return k == o.k && device == o.device && threads == o.threads && smem == o.smem;
+    }
+};
+struct OccHash {
+    size_t operator()(const OccKey& o) const {
+        return std::hash<const void*>()(o.k) ^ ((size_t)o.device << 48) ^ ((size_t)o.threads << 32) ^ (size_t)o.smem;
+    }
+};
+std::mutex occ_mu;
+std::unordered_map<OccKey, int, OccHash> occ_seen;
+}  // namespace
+
+cudaError_t ctas_per_sm(const void* kernel, int device, int threads, int smem, int* out) {
+    const OccKey key{kernel, device, threads, smem};
+    {
+        std::lock_guard<std::mutex> lock(occ_mu);
+        const auto it = occ_seen.find(key);
+        if (it != occ_seen.end()) {
+            *out = it->second;
+            return cudaSuccess;
+        }
+    }
+    if (smem > 40 * 1024) {
+        const cudaError_t e = ensure_dynamic_smem(kernel, device, smem);
+        if (e != cudaSuccess) return e;
+    }
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, (size_t)smem);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(occ_mu);
+    occ_seen[key] = n;
+    *out = n;
+    return cudaSuccess;
+}
+
 cudaError_t ensure_dynamic_smem(const void* kernel, int device, int bytes) {
     if (device < 0 || device >= 64) return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     std::lock_guard<std::mutex> lock(smem_mu);
@@ -333,6 +373,14 @@ int norm_call(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, const vo
     a.flags = flags;
     a.segc = segc;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // Narrow per-token rows at large M (several rows a CTA, at least two waves
+    // of row blocks, no residual): the persistent kernel, whose outputs are
+    // the row-block kernel's bit for bit (W = 512 at M = 4096: 3.38 -> 2.97 us;
+    // W = 1536 at M = 16384: 21.8 -> 18.7 us; with a residual, or at W = 7168,
+    // it measured no faster).
+    const bool persist = !wide && fmt == SGQ_FMT_FP8_PER_TOKEN && q_out && plan.full && !residual_in &&
+                         plan.rpc >= 2 && so.Ms / plan.rpc >= 2 * (int64_t)sms;
+    if (persist) return launched(sgq::launch_norm_pt_persistent(dt_of(flags), plan, a, st));
     return launched(wide ? sgq::launch_norm_cluster(fmt, dt_of(flags), plan, a, st)
                          : sgq::launch_norm(fmt, dt_of(flags), plan, a, st));
 }

@@ -462,6 +462,121 @@ __global__ void __launch_bounds__(kMaxTPR) norm_quant_kernel(const NormArgs a) {
     norm_rows<FMT, LAYOUT, NV, HAS_RES, FULL, DT, !FULL>(a, blockIdx.x);
 }
 
+// Shared-memory bytes of the persistent per-token norm: the weight's chunks
+// (kept for the CTA's lifetime) and one staging slot a chunk for x.
+__host__ __device__ constexpr int norm_pt_persistent_bytes(int nv, int threads) { return nv * 2 * threads * 16; }
+
+// The per-token fused norm of narrow rows at large M (no residual, several
+// rows a CTA, exact-fit plans, quantised output) as a persistent grid: one
+// wave of CTAs, each taking row blocks blockIdx.x, blockIdx.x + gridDim.x,
+// ... The weight is staged once per CTA; a block's x copies go out as soon
+// as the previous block's first pass has consumed its slots, so they are in
+// flight during that block's reduction, scale and output pass; z stays in
+// registers. Every value is formed by the same operations in the same order
+// as norm_rows computes it for the per-token format, so the outputs are
+// norm_quant_kernel's bit for bit.
+template <int NV, int DT>
+__global__ void __launch_bounds__(kMaxTPR) norm_pt_persistent_kernel(const NormArgs a) {
+    extern __shared__ uint4 stage[];
+    __shared__ float2 part[2][32];           // alternate rounds: no barrier needed between blocks
+    const int tpr = a.tpr;
+    const int nt = blockDim.x;
+    const int lrow = threadIdx.x / tpr;
+    const int t = threadIdx.x - lrow * tpr;
+    const int H = a.H;
+    const int64_t nblk = a.M / a.rpc;
+    auto wslot = [&](int v) { return &stage[v * nt + threadIdx.x]; };
+    auto xslot = [&](int v) { return &stage[(NV + v) * nt + threadIdx.x]; };
+    auto issue = [&](int64_t blk) {          // one commit group per chunk
+        const int64_t row = blk * a.rpc + lrow;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            cp_async16(xslot(v), a.x + row * a.ldx + (int64_t)(t + v * tpr) * 8, 16);
+            cp_async_commit();
+        }
+    };
+
+    // the weight (not written by the grid this launch may overlap) before pdl_wait
+#pragma unroll
+    for (int v = 0; v < NV; ++v) cp_async16_cached(wslot(v), a.w + (int64_t)(t + v * tpr) * 8, 16);
+    cp_async_commit();
+    pdl_wait();
+    if ((int64_t)blockIdx.x < nblk) issue(blockIdx.x);
+    pdl_trigger();
+
+    const bool from32 = (a.flags & F_FROM_FP32) != 0;
+    const float w_add = (a.flags & F_GEMMA) ? 1.0f : -0.0f;
+    const bool normed = a.normed != nullptr;
+    int round = 0;
+    for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x, round ^= 1) {
+        const int64_t row = blk * a.rpc + lrow;
+        const int64_t base = row * (int64_t)H;
+        float z[NV][8];
+        float2 ss2 = make_float2(0.0f, 0.0f);
+        float zmax = 0.0f;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            float h[8], wf[8];
+            cp_async_wait_group_of<NV>(v);
+            load8<DT>(ld_smem16(xslot(v)), h);
+            load8<DT>(ld_smem16(wslot(v)), wf);
+#pragma unroll
+            for (int k = 0; k < 8; k += 2) {
+                const float2 hp = make_float2(h[k], h[k + 1]);
+                const float2 wp = __fadd2_rn(make_float2(wf[k], wf[k + 1]), f2(w_add));
+                ss2 = __ffma2_rn(hp, hp, ss2);
+                const float2 zp = __fmul2_rn(hp, wp);
+                z[v][k] = zp.x;
+                z[v][k + 1] = zp.y;
+                zmax = fmaxf(zmax, fmaxf(fabsf(zp.x), fabsf(zp.y)));
+            }
+        }
+        // this thread's slots are read: the next block's copies go out now
+        if (blk + gridDim.x < nblk) issue(blk + gridDim.x);
+
+        // A one-warp row needs no shared-memory round: row_reduce_sum_max's
+        // butterfly over the warp's partials and 31 zeros gives s + 0 and
+        // max(m, 0), formed here directly (in this kernel alone: the branch
+        // in the shared helper slowed the other kernels).
+        float2 r;
+        if (tpr == 32) {
+            const float sw = warp_sum(ss2.x + ss2.y), mw = warp_max(zmax);
+            r = make_float2(sw + 0.0f, fmaxf(mw, 0.0f));
+        } else {
+            r = row_reduce_sum_max(ss2.x + ss2.y, zmax, part[round], tpr, lrow);
+        }
+        const float inv = __frsqrt_rn(__fdiv_rn(r.x, (float)H) + a.eps);
+        const float ymax = inv * r.y;
+        const float2 pt = per_token_scale(from32 ? ymax : round_io<DT>(ymax));
+        const ScaleRow sr = scale_row<FMT_PT, SCALE_ROW_MAJOR>(a.so, row);
+        auto emit = [&](auto from32_tag) {
+            constexpr bool FROM32 = decltype(from32_tag)::value;
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+                const int c = t + v * tpr;
+                float y[8], src[8];
+#pragma unroll
+                for (int k = 0; k < 8; k += 2) {
+                    const float2 yp = __fmul2_rn(f2(inv), make_float2(z[v][k], z[v][k + 1]));
+                    y[k] = yp.x;
+                    y[k + 1] = yp.y;
+                }
+                const uint4 yb = pack8<DT>(y);
+                st16_if(a.normed + base + (int64_t)c * 8, yb, normed);
+                if (FROM32) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) src[k] = y[k];
+                } else {
+                    load8<DT>(yb, src);
+                }
+                quantize_chunk<FMT_PT, SCALE_ROW_MAJOR>(src, row, c, true, true, H, a.q, sr, pt.x, pt.y);
+            }
+        };
+        if (from32) emit(std::true_type{});
+        else emit(std::false_type{});
+    }
+}
+
 // All-reduce + residual add + RMSNorm + quantisation: x is the sum of
 // aa.ar.n partial inputs (AR above); bf16 rows. The bounds-checked kernels
 // may split rows into column segments at small M, as the plain norm does

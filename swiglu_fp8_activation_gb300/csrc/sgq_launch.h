@@ -33,6 +33,11 @@ bool plan_rows(int64_t M, int W, int sm_count, Plan* p);
 // it needs more than was granted before (a mutex-guarded table lookup else).
 cudaError_t ensure_dynamic_smem(const void* kernel, int device, int bytes);
 
+// CTAs of `threads` threads and `smem` bytes of dynamic shared memory that
+// fit on one multiprocessor at once (the occupancy calculator's answer,
+// recorded per kernel, device and shape, so that it is asked once).
+cudaError_t ctas_per_sm(const void* kernel, int device, int threads, int smem, int* out);
+
 // Launch kernel k on `stream` with programmatic stream serialisation: the
 // grid may begin launching while the preceding kernel on the stream finishes
 // (the kernels wait in pdl_wait() before touching memory the preceding grid
@@ -70,6 +75,9 @@ cudaError_t launch_pdl(void (*k)(const Args), const Plan& p, const Args& a, cuda
 // dt: DT_BF16 or DT_F16, the 16-bit activation type.
 cudaError_t launch_norm(int fmt, int dt, const Plan& p, const NormArgs& a, cudaStream_t stream);
 cudaError_t launch_norm_f16(int fmt, const Plan& p, const NormArgs& a, cudaStream_t stream);
+// The persistent per-token norm (exact-fit plans, quantised output).
+cudaError_t launch_norm_pt_persistent(int dt, const Plan& p, const NormArgs& a, cudaStream_t stream);
+cudaError_t launch_norm_pt_persistent_f16(const Plan& p, const NormArgs& a, cudaStream_t stream);
 // p.grid covers both segments; p.rpc * p.tpr is the common CTA size.
 cudaError_t launch_norm_dual(int fmt, int dt, const Plan& p, const DualArgs& d, cudaStream_t stream);
 

@@ -9,4 +9,9 @@ cudaError_t launch_norm(int fmt, int dt, const Plan& p, const NormArgs& a, cudaS
     return NormPick<DT_BF16>::launch(fmt, p, a, stream);
 }
 
+cudaError_t launch_norm_pt_persistent(int dt, const Plan& p, const NormArgs& a, cudaStream_t stream) {
+    if (dt == DT_F16) return launch_norm_pt_persistent_f16(p, a, stream);
+    return NormPick<DT_BF16>::launch_persistent(p, a, stream);
+}
+
 }  // namespace sgq

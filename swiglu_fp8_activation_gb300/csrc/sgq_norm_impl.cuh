@@ -36,6 +36,30 @@ struct NormPick {
         return pick<FMT_PT, SCALE_ROW_MAJOR, RES, FULL>(nv);
     }
 
+    static Kernel pick_persistent(int nv) {
+        switch (nv) {
+            case 1: return norm_pt_persistent_kernel<1, DT>;
+            case 2: return norm_pt_persistent_kernel<2, DT>;
+            case 3: return norm_pt_persistent_kernel<3, DT>;
+            default: return norm_pt_persistent_kernel<4, DT>;
+        }
+    }
+
+    // The persistent per-token norm: as many CTAs as fit on the device at
+    // once (at most one per row block).
+    static cudaError_t launch_persistent(const Plan& p, const NormArgs& a, cudaStream_t stream) {
+        Kernel k = pick_persistent(p.nv);
+        const int threads = p.rpc * p.tpr;
+        const int smem = norm_pt_persistent_bytes(p.nv, threads);
+        int per_sm = 0;
+        const cudaError_t e = ctas_per_sm(reinterpret_cast<const void*>(k), p.device, threads, smem, &per_sm);
+        if (e != cudaSuccess) return e;
+        Plan q = p;
+        const int64_t nblk = a.M / p.rpc, wave = (int64_t)(per_sm > 0 ? per_sm : 1) * p.sms;
+        q.grid = nblk < wave ? nblk : wave;
+        return launch_pdl(k, q, a, stream, smem);
+    }
+
     static cudaError_t launch(int fmt, const Plan& p, const NormArgs& a, cudaStream_t stream) {
         const int l = a.so.layout;
         Kernel k = a.r_in ? (p.full ? pick_fmt<true, true>(fmt, l, p.nv) : pick_fmt<true, false>(fmt, l, p.nv))
