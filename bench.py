@@ -862,7 +862,8 @@ def run_profile(args):
     """One kernel only (for ncu): `--warmup` untimed then `--steps` timed
     launches. norm / swiglu: the M=8192 prefill workload (inputs > L2,
     rotated). pertoken: RMSNorm + per-token FP8 at W=7168, M=4096 (three
-    rotating input sets, 176 MB together). silu128: SiLU-and-mul + 1x128
+    rotating input sets, 176 MB together); pertoken512 the same at W=512
+    (the persistent kernel). silu128: SiLU-and-mul + 1x128
     (bf16 roundings) at I=12288, M=2048 (three sets, 302 MB together);
     silu128_m256 the same at M=256 and norm128_m256 RMSNorm + 1x128 (fp32
     source) at W=4096, M=256 (the Qwen3-like workload's largest M).
@@ -904,10 +905,11 @@ def run_profile(args):
         fn = lib.rmsnorm_add_quant
         nbytes = norm_bytes(case.M, case.H)
         get = lambda k: args1
-    elif args.profile in ("pertoken", "norm128_m256"):
+    elif args.profile in ("pertoken", "pertoken512", "norm128_m256"):
         from swiglu_fp8_activation_gb300 import inputs, library
-        pt = args.profile == "pertoken"
-        case = inputs.norm_case_per_token(4096, 7168) if pt else inputs.norm_case_block128(256)
+        pt = args.profile.startswith("pertoken")
+        W = 512 if args.profile == "pertoken512" else 7168
+        case = inputs.norm_case_per_token(4096, W) if pt else inputs.norm_case_block128(256)
         t = inputs.make_norm(case)
         sets = [(t["x"].to(dev), t["w"].to(dev)) for _ in range(ROTATE)]
         q = torch.empty(case.M, case.H, dtype=torch.uint8, device=dev)
@@ -951,7 +953,7 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle time")
     ap.add_argument("--quick", action="store_true", help="skip the decode and other-config tables")
-    ap.add_argument("--profile", choices=("norm", "swiglu", "pertoken", "silu128", "silu128_m256", "norm128_m256",
+    ap.add_argument("--profile", choices=("norm", "swiglu", "pertoken", "pertoken512", "silu128", "silu128_m256", "norm128_m256",
                                           "norm8", "norm8_inplace", "norm192", "norm192_inplace"),
                     help="time one kernel only (for ncu)")
     args = ap.parse_args(argv)
