@@ -346,7 +346,12 @@ typedef struct sgq_norm_seg {
  *   q_out, scale_out = quantise(src)        (if q_out is not NULL)
  *
  * exactly as rmsnorm_add_quant computes a row without residual, so each
- * segment's outputs equal a rmsnorm_add_quant call on its rows. The inputs
+ * segment's outputs equal a rmsnorm_add_quant call on its rows, bit for bit
+ * (each segment keeps that call's threads per row). The one exception: width
+ * pairs whose single-norm threads per row have a least common multiple above
+ * 512 (for instance 7168 and 2240 at small M) run both segments at one
+ * width's threads per row, and then match a single call within the parity
+ * tolerances. The inputs
  * may be column ranges of one tensor (x = base + column offset, ld = the
  * tensor's row length), and may overlap each other; the outputs may overlap
  * nothing. Scales are row-major (no layout flags).

@@ -510,40 +510,44 @@ int swiglu_call(int fmt, int act, uint32_t flags, int64_t M, int64_t I, float al
 
 int gcd(int a, int b) { return b == 0 ? a : gcd(b, a % b); }
 
-// Plan of the two-segment norm: one chunk count per thread (NV) for both
-// segments, each segment's threads per row (a multiple of 32), and a common
-// CTA size T that both divide, so every CTA holds whole rows of its segment.
-// T is the least common multiple of the two, grown towards kTargetCTA at
-// large M; when that exceeds kMaxTPR both segments take the wider one's
-// threads per row. NV order and the small-M rule follow plan_rows.
+// Plan of the two-segment norm. Each segment keeps the threads per row of
+// its own single-norm plan (plan_rows for M and its width), and the launch
+// takes the larger of the two plans' chunks a thread (NV): the extra chunks of
+// the other segment lie past its row end and add exact zeros, so every thread
+// sums the same chunks in the same order as a rmsnorm_add_quant call on that
+// segment, and each segment's outputs equal that call's bit for bit. The CTA
+// size T is the least common multiple of the two threads per row (so every
+// CTA holds whole rows of its segment), grown towards kTargetCTA at large M.
+// Where that multiple exceeds kMaxTPR, both segments take the wider one's
+// threads per row, and the outputs then match a single call within the
+// tolerances only (its sum of squares is added in another order).
 bool plan_dual(int64_t M, int Ha, int Hb, int sms, sgq::Plan* p, int tpr[2], int rpc[2], int64_t* grid0) {
-    const int n[2] = {Ha / 8, Hb / 8};
-    const bool small = sms > 0 && M * (int64_t)(n[0] + n[1]) <= (int64_t)sms * 1024;
-    for (int i = 0; i < sgq::kMaxNV; ++i) {
-        const int nv = small ? 1 + i : sgq::kMaxNV - i;
-        int t[2];
+    sgq::Plan single[2];
+    if (!sgq::plan_rows(M, Ha, sms, &single[0]) || !sgq::plan_rows(M, Hb, sms, &single[1])) return false;
+    const int nv = single[0].nv > single[1].nv ? single[0].nv : single[1].nv;
+    int t[2] = {single[0].tpr, single[1].tpr};
+    int T = t[0] / gcd(t[0], t[1]) * t[1];
+    if (T > sgq::kMaxTPR) {
+        const int n[2] = {Ha / 8, Hb / 8};
         for (int s = 0; s < 2; ++s) t[s] = ((n[s] + nv - 1) / nv + 31) / 32 * 32;
-        if (t[0] > sgq::kMaxTPR || t[1] > sgq::kMaxTPR) continue;
-        int T = t[0] / gcd(t[0], t[1]) * t[1];
-        if (T > sgq::kMaxTPR) {                     // both take the wider segment's threads per row
-            T = t[0] > t[1] ? t[0] : t[1];
-            t[0] = t[1] = T;
-        }
-        if (!small && T < sgq::kTargetCTA) T *= sgq::kTargetCTA / T;
-        for (int s = 0; s < 2; ++s) {
-            tpr[s] = t[s];
-            rpc[s] = T / t[s];
-        }
-        *grid0 = (M + rpc[0] - 1) / rpc[0];
-        p->nv = nv;
-        p->tpr = T;
-        p->rpc = 1;
-        p->grid = *grid0 + (M + rpc[1] - 1) / rpc[1];
-        p->full = false;
-        p->sms = sms;
-        return p->grid <= 0x7FFFFFFF;
+        T = t[0] > t[1] ? t[0] : t[1];
+        if (T > sgq::kMaxTPR) return false;
+        t[0] = t[1] = T;
     }
-    return false;
+    const bool small = sms > 0 && M * (int64_t)(Ha / 8 + Hb / 8) <= (int64_t)sms * 1024;
+    if (!small && T < sgq::kTargetCTA) T *= sgq::kTargetCTA / T;
+    for (int s = 0; s < 2; ++s) {
+        tpr[s] = t[s];
+        rpc[s] = T / t[s];
+    }
+    *grid0 = (M + rpc[0] - 1) / rpc[0];
+    p->nv = nv;
+    p->tpr = T;
+    p->rpc = 1;
+    p->grid = *grid0 + (M + rpc[1] - 1) / rpc[1];
+    p->full = false;
+    p->sms = sms;
+    return p->grid <= 0x7FFFFFFF;
 }
 
 }  // namespace

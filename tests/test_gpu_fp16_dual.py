@@ -130,3 +130,30 @@ def test_dual_norm_leaves_the_input_tail_alone_and_writes_only_its_outputs():
     rmsnorm_dual_quant(d[:, :Ha], wa.to(DEV), d[:, Ha:Ha + Hb], wb.to(DEV))
     torch.cuda.synchronize()
     assert torch.equal(d, before)
+
+
+# (fmt, M, Ha, Hb, gemma, from_fp32, dtype): each segment's outputs must equal
+# a single rmsnorm_add_quant call on its rows bit for bit (the two-segment
+# plan keeps each segment's single-norm threads per row). The M values cross
+# the single norms' small-M plan boundaries of the latent widths (1536 / 512).
+BITWISE = [("per_token", M, 1536, 512, False, False, torch.bfloat16) for M in (1, 64, 700, 1024, 2048, 4096)]
+BITWISE += [("mxfp8", 300, 2048, 1024, True, False, torch.bfloat16),
+            ("block128", 1500, 4096, 512, False, True, torch.float16),
+            ("per_token", 2500, 7168, 512, False, True, torch.bfloat16)]
+
+
+@pytest.mark.parametrize("c", BITWISE, ids=lambda c: "-".join(str(v) for v in c[:6]) + ("-f16" if c[6] == torch.float16 else ""))
+def test_dual_norm_equals_single_calls_bitwise(c):
+    fmt, M, Ha, Hb, gemma, from32, dtype = c
+    buf, wa, wb = _dual_case(M, Ha, Hb, dtype, seed=M + Ha + Hb)
+    d = buf.to(DEV)
+    xa, xb = d[:, :Ha], d[:, Ha:Ha + Hb]
+    wa, wb = wa.to(DEV), wb.to(DEV)
+    (qa, sa, na), (qb, sb, nb) = rmsnorm_dual_quant(xa, wa, xb, wb, fmt=fmt, gemma=gemma, quant_from_fp32=from32,
+                                                   quant_a=True, quant_b=True, normed_a=True, normed_b=True)
+    kw = dict(fmt=fmt, gemma=gemma, quant_from_fp32=from32, normed=True)
+    q1, s1, n1, _ = rmsnorm_add_quant(xa.contiguous(), wa, **kw)
+    q2, s2, n2, _ = rmsnorm_add_quant(xb.contiguous(), wb, **kw)
+    torch.cuda.synchronize()
+    for got, want in ((qa, q1), (sa, s1), (na, n1), (qb, q2), (sb, s2), (nb, n2)):
+        assert torch.equal(got, want)
