@@ -135,6 +135,35 @@ def test_activation_then_quant_equals_fused_bitwise(fmt, act, round_bf16, M):
     assert torch.equal(q_f, q_u) and torch.equal(s_f, s_u)
 
 
+# The prefill workload's shapes and rows wider than one CTA covers (a thread
+# block cluster a row for the norms and per-token SwiGLU, column segments for
+# MX / 1x128 SwiGLU): the unfused chain must still equal the fused op.
+@pytest.mark.parametrize("fmt,M,H", [("mxfp8", 8192, 6144), ("mxfp8", 3, 32768), ("block128", 5, 24576),
+                                     ("per_token", 4, 24576)])
+def test_norm_then_quant_equals_fused_bitwise_large_and_wide(fmt, M, H):
+    t = inputs.norm_inputs(M, H, seed=M + H, x_std=1.0, r_std=1.0, w_mean=0.0, w_std=0.1)
+    xd, rd, wd = t["x"].to(DEV), t["r"].to(DEV), t["w"].to(DEV)
+    q_f, s_f, n_f, r_f = rmsnorm_add_quant(xd, wd, fmt=fmt, residual_in=rd, residual_out=torch.empty_like(rd),
+                                           gemma=True, quant_from_fp32=False, normed=True)
+    n_u, r_u = rmsnorm_add(xd, wd, residual_in=rd, residual_out=torch.empty_like(rd), gemma=True)
+    q_u, s_u = quantize_fp8(n_u, fmt=fmt)
+    torch.cuda.synchronize()
+    assert torch.equal(n_f, n_u) and torch.equal(r_f, r_u)
+    assert torch.equal(q_f, q_u) and torch.equal(s_f, s_u)
+
+
+@pytest.mark.parametrize("fmt,act,round_bf16,M,I", [("mxfp8", "swiglu_oai", False, 8192, 3072),
+                                                    ("block128", "silu_mul", True, 4, 24576),
+                                                    ("per_token", "silu_mul", False, 4, 24576)])
+def test_activation_then_quant_equals_fused_bitwise_large_and_wide(fmt, act, round_bf16, M, I):
+    gu = inputs.swiglu_inputs(M, I, seed=M + I, std=2.0).to(DEV)
+    q_f, s_f = swiglu_quant(gu, fmt=fmt, act=act, quant_from_fp32=False, round_act_bf16=round_bf16, alpha=ALPHA)
+    a = swiglu(gu, act=act, round_act_bf16=round_bf16, alpha=ALPHA)
+    q_u, s_u = quantize_fp8(a, fmt=fmt)
+    torch.cuda.synchronize()
+    assert torch.equal(q_f, q_u) and torch.equal(s_f, s_u)
+
+
 def _golden_rates():
     rows = []
     with open(os.path.join(GOLDEN, "swiglu_oai_mxfp8_fp32_vs_bf16.txt")) as f:
