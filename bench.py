@@ -836,7 +836,15 @@ def run_ours(args, world, rank, local):
                               "norm_frac": round(nb / (norm_alone_us * 1e-6) / 1e9 / peak, 4),
                               "swiglu_us": round(swiglu_alone_us, 2),
                               "swiglu_frac": round(swiglu_bytes(M_PREFILL, I_PREFILL) / (swiglu_alone_us * 1e-6)
-                                                   / 1e9 / peak, 4)}},
+                                                   / 1e9 / peak, 4)},
+                    # SwiGLU's added cost inside the step: the step's time less the norm's time back to
+                    # back (each norm launch there also writes back its predecessor's dirty lines, as the
+                    # SwiGLU kernel does for the norm inside the step)
+                    "in_step_marginal": {
+                        "swiglu_us": round(ms_step * 1e3 - norm_alone_us, 2),
+                        "swiglu_frac": round(swiglu_bytes(M_PREFILL, I_PREFILL)
+                                             / max((ms_step * 1e3 - norm_alone_us) * 1e-6, 1e-12) / 1e9 / peak, 4),
+                        "note": "step time (no events) minus the norm's back-to-back time, same run"}},
         "host_us_per_eager_call_M8": {"rmsnorm_add_quant": host_us, "ctypes_floor": ctypes_us},
         "decode_us_per_launch": decode,
         "other_configs": others,
