@@ -13,6 +13,7 @@ tests/test_oracle_*.py.
 from __future__ import annotations
 
 import ctypes as C
+import os
 
 import numpy as np
 
@@ -28,9 +29,11 @@ _lib = None
 
 
 def lib() -> C.CDLL:
+    """The oracle library: built beside its source, or the prebuilt library
+    named by SGQ_ORACLE_LIBRARY (the mutation tests' planted-mistake builds)."""
     global _lib
     if _lib is None:
-        L = C.CDLL(build_oracle())
+        L = C.CDLL(os.environ.get("SGQ_ORACLE_LIBRARY") or build_oracle())
         L.ora_bf16_decode.restype = C.c_double
         L.ora_bf16_decode.argtypes = [C.c_uint16]
         L.ora_bf16_round.restype = C.c_uint16

@@ -14,16 +14,22 @@ SRC = os.path.join(HERE, "sgq_oracle.c")
 LIB = os.path.join(HERE, "libsgq_oracle.so")
 
 
+def compile_oracle(src: str, out: str) -> str:
+    """Compile the oracle source `src` into the shared library `out` (the
+    mutation tests build planted-mistake copies with the same flags)."""
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-Wall", "-Wextra", "-Werror", "-ffp-contract=off",
+           "-fno-fast-math", "-shared", "-fPIC", "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
 def build_oracle(force: bool = False) -> str:
     """Build libsgq_oracle.so if it is missing or older than its source; return its path."""
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= os.path.getmtime(SRC):
         return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-Wall", "-Wextra", "-Werror", "-ffp-contract=off",
-           "-fno-fast-math", "-shared", "-fPIC", "-o", tmp, SRC, "-lm"]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    return compile_oracle(SRC, LIB)
 
 
 if __name__ == "__main__":
