@@ -16,7 +16,8 @@ from oracle.build import SRC, compile_oracle
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 OUT = os.path.join(ROOT, "_build", "oracle_mutants")
 PINS = ["tests/test_oracle_codecs.py", "tests/test_oracle_norm.py", "tests/test_oracle_swiglu.py",
-        "tests/test_oracle_fp16.py", "tests/test_oracle_allreduce.py", "tests/test_oracle_layouts.py"]
+        "tests/test_oracle_fp16.py", "tests/test_oracle_allreduce.py", "tests/test_oracle_layouts.py",
+        "tests/test_oracle_flags.py"]
 
 # (name, text in the oracle source, its replacement)
 MUTANTS = [
@@ -48,6 +49,12 @@ MUTANTS = [
     ("fp16_bias", "else v = ldexp(1024.0 + (double)f, e - 25);", "else v = ldexp(1024.0 + (double)f, e - 24);"),
     ("allreduce_last_rank", "for (int r = 0; r < n; ++r) s += io_decode(f16, parts[r][j]);",
      "for (int r = 0; r < n; ++r) s = io_decode(f16, parts[r][j]);"),
+    # the ambiguity flags the parity checker relies on
+    ("pow2_flag_always", "    if (amax == 0.0) return 0;\n    int e2;\n    double f = frexp(amax, &e2);     /* f in [0.5, 1) */",
+     "    if (amax == 0.0) return 0;\n    if (rel > 0.0) return 1;\n    int e2;\n    double f = frexp(amax, &e2);     /* f in [0.5, 1) */"),
+    ("tie_window_wide", "near_e4m3_boundary(tj, ldexp(1.0, -22))", "near_e4m3_boundary(tj, ldexp(1.0, -12))"),
+    ("source_flag_dropped", "src_amb[j] = (unsigned char)(from_fp32 ? 0 : near_io_boundary(f16, pre[j], rel));",
+     "src_amb[j] = (unsigned char)(0 * near_io_boundary(f16, pre[j], rel));"),
 ]
 
 
