@@ -47,7 +47,9 @@
  *     State kept between calls: the calling thread's last launch error (see
  *     sgq_launch_error), each device's multiprocessor count (queried on the
  *     first call on that device), the shared-memory opt-in each kernel was
- *     given on each device, and the planning count of sgq_set_sm_budget.
+ *     given on each device, the occupancy calculator's answer for each
+ *     persistent launch shape (asked on its first launch), and the planning
+ *     count of sgq_set_sm_budget.
  *   - All tensors are contiguous and row-major (the dual norm's inputs may
  *     have a row stride). 16-bit activations are bfloat16, or IEEE fp16 with
  *     SGQ_F_FP16 where an entry point accepts it. Quantised values are OCP
