@@ -90,3 +90,25 @@ def test_persistent_per_token_norm(c):
                                    normed=normed, fp16=f16)
     check_norm("per_token", ref, q.cpu().numpy(), s.cpu().numpy(), _bits(n) if normed else None, None,
                from_fp32=f32)
+
+
+def test_first_persistent_launch_inside_graph_capture():
+    # fp16 rows of 768 (3 chunks a thread, 32 threads a row): a kernel and
+    # shape no other test launches, so its first launch (which asks the
+    # occupancy calculator) happens while the stream is being captured
+    M, W = 4096, 768
+    assert _persistent(M, W, _sms())
+    t = inputs.norm_inputs(M, W, seed=768, x_std=1.0, r_std=None, w_mean=1.0, w_std=0.1)
+    x, w = t["x"].to(torch.float16).to(DEV), t["w"].to(torch.float16).to(DEV)
+    q = torch.empty(M, W, dtype=torch.uint8, device=DEV)
+    s = torch.empty(M, 1, dtype=torch.float32, device=DEV)
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        rmsnorm_add_quant(x, w, fmt="per_token", gemma=False, q_out=q, scale_out=s)
+    g.replay()
+    q2, s2, _, _ = rmsnorm_add_quant(x, w, fmt="per_token", gemma=False)
+    torch.cuda.synchronize()
+    assert torch.equal(q, q2) and torch.equal(s, s2)
+    ref = oracle.quantize("per_token", _bits(rmsnorm_add(x, w, gemma=False)[0]), fp16=True)
+    np.testing.assert_array_equal(q.cpu().numpy(), ref["q"])
