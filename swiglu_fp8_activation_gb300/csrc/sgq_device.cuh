@@ -502,15 +502,22 @@ __device__ __forceinline__ float row_reduce(float v, float* part, int tpr, int l
 
 // Sum of `a` and max of `b` (b >= 0) over the `tpr` threads of one row, in
 // one shared-memory round (one __syncthreads); same rules as row_reduce.
+// The max over a warp in one instruction (exact, as any order of maxima is).
+__device__ __forceinline__ float warp_max_redux(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 __device__ __forceinline__ float2 row_reduce_sum_max(float a, float b, float2* part, int tpr, int lrow) {
     a = warp_sum(a);
-    b = warp_max(b);
+    b = warp_max_redux(b);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (lane == 0) part[warp] = make_float2(a, b);
     __syncthreads();
     const int nw = tpr >> 5;
     const float2 r = lane < nw ? part[lrow * nw + lane] : make_float2(0.0f, 0.0f);
-    return make_float2(warp_sum(r.x), warp_max(r.y));
+    return make_float2(warp_sum(r.x), warp_max_redux(r.y));
 }
 
 // ------------------------------------------------------------------ scales

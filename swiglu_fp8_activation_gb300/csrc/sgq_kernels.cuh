@@ -256,7 +256,8 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk, const 
     const int ir = AR ? nparts : 1, iw = nslot - 1;
     const int tpr = a.tpr;
     const int nt = blockDim.x;
-    const int lrow = threadIdx.x / tpr;
+    // one row a CTA (the per-token format's wide rows): no division
+    const int lrow = (FMT == FMT_PT && a.rpc == 1) ? 0 : threadIdx.x / tpr;
     const int t = threadIdx.x - lrow * tpr;
     const int64_t row = blk * a.rpc + lrow;
     const bool row_ok = FULL || row < a.M;
