@@ -314,12 +314,14 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk, const 
     float z[NV][8];
     float2 ss2 = make_float2(0.0f, 0.0f);
     float zmax = 0.0f;
-    // w' = w + 1 (Gemma) or w + (-0), which is w exactly, signed zeros
-    // included. (A chunk loop specialised on the weight form, with no
-    // addition for a plain weight, measured 10% slower at small M: the
-    // doubled code.)
+    // The weight term w' = w + 1 (Gemma) or w + (-0), which is w exactly,
+    // signed zeros included: an addition of w_add in the general form
+    // (WMODE 0); the per-token kernels take the weight form as a constant
+    // (WMODE 1: + 1, WMODE 2: no addition), the same values. (For every
+    // format, the doubled code measured 10% slower at small M.)
     const float w_add = (a.flags & F_GEMMA) ? 1.0f : -0.0f;
-    {
+    auto pass1 = [&](auto wmode_tag) {
+        constexpr int WMODE = decltype(wmode_tag)::value;
 #pragma unroll
         for (int v = 0; v < NV; ++v) {
             const int c = c0 + t + v * tpr;
@@ -367,7 +369,9 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk, const 
 #pragma unroll
             for (int k = 0; k < 8; k += 2) {
                 const float2 hp = make_float2(h[k], h[k + 1]);
-                const float2 wp = __fadd2_rn(make_float2(wf[k], wf[k + 1]), f2(w_add));
+                float2 wp = make_float2(wf[k], wf[k + 1]);
+                if constexpr (WMODE == 0) wp = __fadd2_rn(wp, f2(w_add));
+                else if constexpr (WMODE == 1) wp = __fadd2_rn(wp, f2(1.0f));
                 ss2 = __ffma2_rn(hp, hp, ss2);
                 const float2 zp = __fmul2_rn(hp, wp);
                 z[v][k] = zp.x;
@@ -379,6 +383,12 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk, const 
                 *reinterpret_cast<float4*>(slot(v, iw)) = make_float4(z[v][4], z[v][5], z[v][6], z[v][7]);
             }
         }
+    };
+    if constexpr (FMT == FMT_PT) {
+        if (a.flags & F_GEMMA) pass1(std::integral_constant<int, 1>{});
+        else pass1(std::integral_constant<int, 2>{});
+    } else {
+        pass1(std::integral_constant<int, 0>{});
     }
     float ss = ss2.x + ss2.y;
 
