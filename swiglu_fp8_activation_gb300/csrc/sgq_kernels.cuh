@@ -214,14 +214,6 @@ __host__ __device__ constexpr int norm_stage_bytes(bool has_res, int nv, int thr
     return nv * norm_stage_inputs(has_res) * threads * 16;
 }
 
-// Where the norm keeps z = h * w' between the row reduction and the output
-// pass: in registers (NV x 8 floats a thread across the reduction's barrier),
-// or written back over the thread's own x and weight slots in shared memory,
-// which frees those registers for more resident CTAs. The per-token format,
-// whose register count limited it to four 224-thread CTAs an SM, takes the
-// shared-memory form.
-__host__ __device__ constexpr bool norm_z_in_smem(int fmt) { return fmt == FMT_PT; }
-
 // The rows of CTA `blk` of one norm launch (blockDim.x = a.rpc * a.tpr).
 // FULL: every thread's chunks lie inside the row and every row inside M (the
 // plan divides both exactly), so no bounds are checked. DT is the 16-bit
@@ -310,7 +302,6 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk, const 
     //    sum (c & ~31 is the same in every lane of a warp, and segc is a
     //    multiple of 32); their z is never used, except by the per-token max.
     const bool from32 = (a.flags & F_FROM_FP32) != 0;
-    constexpr bool ZS = norm_z_in_smem(FMT);
     float z[NV][8];
     float2 ss2 = make_float2(0.0f, 0.0f);
     float zmax = 0.0f;
@@ -378,10 +369,6 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk, const 
                 z[v][k + 1] = zp.y;
                 if (FMT == FMT_PT) zmax = fmaxf(zmax, fmaxf(fabsf(zp.x), fabsf(zp.y)));
             }
-            if (ZS) {   // over this thread's own x and weight slots of chunk v, both read above
-                *reinterpret_cast<float4*>(slot(v, 0)) = make_float4(z[v][0], z[v][1], z[v][2], z[v][3]);
-                *reinterpret_cast<float4*>(slot(v, iw)) = make_float4(z[v][4], z[v][5], z[v][6], z[v][7]);
-            }
         }
     };
     if constexpr (FMT == FMT_PT) {
@@ -433,19 +420,10 @@ __device__ __forceinline__ void norm_rows(const NormArgs& a, int64_t blk, const 
             // the row end) skip the chunk; c & ~31 is the same in every lane
             if (SEG && ((c & ~31) < cb || (c & ~31) >= cend)) continue;
             const bool ok = FULL || (row_ok && c < clim);
-            float y[8], src[8], zc[8];
-            if (ZS) {
-                const float4 lo = *reinterpret_cast<const float4*>(slot(v, 0));
-                const float4 hi = *reinterpret_cast<const float4*>(slot(v, iw));
-                zc[0] = lo.x, zc[1] = lo.y, zc[2] = lo.z, zc[3] = lo.w;
-                zc[4] = hi.x, zc[5] = hi.y, zc[6] = hi.z, zc[7] = hi.w;
-            } else {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) zc[k] = z[v][k];
-            }
+            float y[8], src[8];
 #pragma unroll
             for (int k = 0; k < 8; k += 2) {                   // z = 0 past the row end (zero-filled copies)
-                const float2 yp = __fmul2_rn(f2(inv), make_float2(zc[k], zc[k + 1]));
+                const float2 yp = __fmul2_rn(f2(inv), make_float2(z[v][k], z[v][k + 1]));
                 y[k] = yp.x;
                 y[k + 1] = yp.y;
             }
@@ -551,7 +529,7 @@ __global__ void __launch_bounds__(kMaxTPR) norm_pt_persistent_kernel(const NormA
         // in the shared helper slowed the other kernels).
         float2 r;
         if (tpr == 32) {
-            const float sw = warp_sum(ss2.x + ss2.y), mw = warp_max(zmax);
+            const float sw = warp_sum(ss2.x + ss2.y), mw = warp_max_redux(zmax);
             r = make_float2(sw + 0.0f, fmaxf(mw, 0.0f));
         } else {
             r = row_reduce_sum_max(ss2.x + ss2.y, zmax, part[round], tpr, lrow);
