@@ -228,6 +228,20 @@ bool plan_launch(int64_t M, int W, const sgq::ScaleOut& so, const Device& dev, s
     return true;
 }
 
+// The norms' plan: threads per row and chunks a thread from the real rows M,
+// since they fix the order in which a row's sum of squares is added (so a
+// scale layout's padding rows change no output value, and the fused norm
+// stays equal to rmsnorm_add + quantize_fp8 in every layout); the grid then
+// also covers the layout's padding rows [M, Ms).
+bool plan_norm(int64_t M, int64_t Ms, int H, int sms, sgq::Plan* p) {
+    if (!sgq::plan_rows(M, H, sms, p)) return false;
+    if (Ms > M) {
+        p->grid = (Ms + p->rpc - 1) / p->rpc;
+        p->full = false;
+    }
+    return p->grid <= 0x7FFFFFFF;
+}
+
 // Dynamic shared memory one CTA may use (227 KB on sm_100-class parts).
 constexpr int kMaxDynamicSmem = 227 * 1024;
 
@@ -349,7 +363,7 @@ int norm_call(int fmt, uint32_t flags, int64_t M, int64_t H, float eps, const vo
         if (!plan_cluster(so.Ms, (int)(H / 8), dev, &plan, &segc)) return SGQ_ERR_UNSUPPORTED;
     } else {
         const int seg = residual_out && residual_out == residual_in ? 1 : norm_segments(so.Ms, H, sms);
-        if (!sgq::plan_rows(so.Ms, (int)H, sms, &plan)) return SGQ_ERR_UNSUPPORTED;
+        if (!plan_norm(M, so.Ms, (int)H, sms, &plan)) return SGQ_ERR_UNSUPPORTED;
         plan.device = dev.id;
         plan.seg = seg;
         plan.full = plan.full && so.Ms == M && seg == 1;   // the exact-fit kernels write whole rows
@@ -643,7 +657,7 @@ int allreduce_rmsnorm_add_quant(int fmt, uint32_t flags, int nranks, int64_t M, 
     const int seg = (residual_out && residual_out == residual_in) || so.Ms * nranks > 64
                         ? 1 : norm_segments(so.Ms, H, dev.sms);
     sgq::Plan plan;
-    if (!sgq::plan_rows(so.Ms, (int)H, dev.sms, &plan)) return SGQ_ERR_UNSUPPORTED;
+    if (!plan_norm(M, so.Ms, (int)H, dev.sms, &plan)) return SGQ_ERR_UNSUPPORTED;
     plan.device = dev.id;
     plan.full = plan.full && so.Ms == M && seg == 1;
     plan.seg = seg;

@@ -445,18 +445,23 @@ __device__ __forceinline__ bool bf16x2_any_lt(uint32_t a, uint32_t b) {
 // q0 + rem*r rounded once is the correctly rounded quotient (Markstein's
 // correction step: P. Markstein, "Computation of elementary functions on the
 // IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990). Results
-// below the normal range may differ from IEEE division by an ulp.
+// below the normal range may differ from IEEE division by an ulp. The
+// remainder's FMA rounds down: being exact, its value is the same in any
+// rounding direction, but for a = +-0 the sum +0 + -0 it forms is then -0,
+// so that the correction keeps the sign of a zero quotient (-0 / b = -0, as
+// in IEEE division; rounding to nearest would give +0).
 __device__ __forceinline__ float div_rn(float a, float b, float r) {
     const float q0 = a * r;
-    const float rem = fmaf(-q0, b, a);
+    const float rem = __fmaf_rd(-q0, b, a);
     return fmaf(rem, r, q0);
 }
 
 // Two quotients at once, as div_rn, given nb = -b and r = RN(1/b) for the
-// same b (one FP8 group's scale): q0 = a*r; rem = a - b*q0 (exact); q0 + rem*r.
+// same b (one FP8 group's scale): q0 = a*r; rem = a - b*q0 (exact, rounded
+// down for the sign of zero); q0 + rem*r.
 __device__ __forceinline__ float2 div2_rn(float2 a, float2 nb, float2 r) {
     const float2 q0 = __fmul2_rn(a, r);
-    const float2 rem = __ffma2_rn(q0, nb, a);
+    const float2 rem = __ffma2_rd(q0, nb, a);
     return __ffma2_rn(rem, r, q0);
 }
 

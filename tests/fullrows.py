@@ -1,8 +1,8 @@
 """Parity over every row of a launch: the oracle and the checker run on row
 blocks, one block per task, on all host threads (the C oracle and numpy's
-loops run outside the interpreter lock). The 1e-4 code-mismatch budget is
-applied to the totals over all blocks; every other tolerance applies in each
-block. Used by the GPU parity tests for launches too large for one oracle
+loops run outside the interpreter lock). The code-mismatch budgets (1e-4
+away from exact ties, 1e-3 at them) are applied to the totals over all
+blocks; every other tolerance applies in each block. Used by the GPU parity tests for launches too large for one oracle
 call."""
 from __future__ import annotations
 
@@ -10,7 +10,7 @@ import concurrent.futures as cf
 import os
 
 import oracle
-from oracle.parity import MAX_CODE_MISMATCH_FRACTION, check_norm, check_swiglu
+from oracle.parity import budget_verdict, check_norm, check_swiglu
 
 BLOCK = 256
 
@@ -37,9 +37,8 @@ def _merge(parts: list) -> dict:
 
 def _finish(parts: list) -> dict:
     st = _merge(parts)
-    assert st["code_mismatch_frac"] <= MAX_CODE_MISMATCH_FRACTION, \
-        (f"E4M3 mismatch fraction {st['code_mismatch_frac']:.2e} > 1e-4 "
-         f"({st['code_mismatch']} of {st['n_plain']}, {st['tie_mismatch']} at ties)")
+    ok, msg = budget_verdict(st.get("code_mismatch", 0), st.get("tie_mismatch", 0), st.get("n_plain", 0))
+    assert ok, msg
     return st
 
 

@@ -10,8 +10,8 @@
 * div_rn() and div2_rn() (one reciprocal per group + Markstein's FMA
   correction) against CUDA's correctly rounded __fdiv_rn, bit for bit, for
   the FP8 quotients the kernels form (|a| <= b * 448 * (1 + 2^-20), b
-  normal), the FP8 scale amax / 448, quotients by integer widths and random
-  pairs.
+  normal), the FP8 scale amax / 448, quotients by integer widths, random
+  pairs and signed zero numerators.
 """
 import ctypes as C
 import os
@@ -124,3 +124,15 @@ def test_div_rn_and_packed_form_match_ieee_division(devlib):
         normal = (np.abs(qi) >= 2.0 ** -126) & np.isfinite(qi)     # overflowing pairs never occur in the kernels
         np.testing.assert_array_equal(qf.view(np.uint32)[normal], qi.view(np.uint32)[normal])
         np.testing.assert_array_equal(qp.view(np.uint32)[normal], qi.view(np.uint32)[normal])
+    # zero numerators keep their sign (-0 / b = -0), bit for bit (an FP8 code
+    # of a -0 source is 0x80)
+    az = np.zeros(1024, np.float32)
+    az[1::2] = np.float32(-0.0)
+    bz = np.abs(rng.standard_normal(1024) * 2.0 ** rng.integers(-60, 60, 1024)).astype(np.float32) + np.float32(1.0)
+    at, bt = torch.from_numpy(az).cuda(), torch.from_numpy(bz).cuda()
+    qf, qp, qi = torch.empty_like(at), torch.empty_like(at), torch.empty_like(at)
+    assert devlib.run_div(_p(at), _p(bt), _p(qf), _p(qp), _p(qi), 1024) == 0
+    qi = qi.cpu().numpy()
+    assert (np.signbit(qi) == np.signbit(az)).all()
+    np.testing.assert_array_equal(qf.cpu().numpy().view(np.uint32), qi.view(np.uint32))
+    np.testing.assert_array_equal(qp.cpu().numpy().view(np.uint32), qi.view(np.uint32))

@@ -3,7 +3,7 @@ against the oracle under the same tolerances as the fixed parity tests:
 random formats, flags, activation types, scale layouts and shapes (M from 1
 to a few hundred, widths any multiple of the format's group up to the
 maximum), then the all-reduce norm over 1 to 8 ranks and rows wider than one
-CTA covers. Cases are drawn once from a fixed seed, so a failure names a
+CTA covers. Cases are drawn once from fixed seeds, so a failure names a
 reproducible configuration."""
 import numpy as np
 import pytest
@@ -65,7 +65,9 @@ def _cases(n=48, seed=2024):
     return out
 
 
-CASES = _cases()
+# a second draw of twice as many cases (it found the -0 code, the layout-dependent plan and the
+# tie counts of fp32-source FP8 norms that the first draw had missed)
+CASES = _cases() + _cases(n=96, seed=7919)
 
 
 def _name(c):
@@ -190,7 +192,7 @@ def _more_cases(n=24, seed=2025):
     return out
 
 
-MORE_CASES = _more_cases()
+MORE_CASES = _more_cases() + _more_cases(n=48, seed=104729)
 
 
 def _row_scales(fmt, layout, s, M, W):

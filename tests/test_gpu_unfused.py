@@ -197,3 +197,21 @@ def test_page_statistic_fused_vs_unfused_chain_on_gpu():
 
         assert np.abs(deq(q_f, s_f) - a).sum() <= np.abs(deq(q_u, s_u) - a).sum()
     assert diff_blocks <= 0.005 * total_blocks
+
+
+@pytest.mark.parametrize("fmt", ["mxfp8", "block128", "per_token"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_signed_zeros_keep_their_code(fmt, dtype):
+    # a -0 source element quantises to the code of -0 (0x80) and +0 to 0x00 in every format, bit for
+    # bit with the oracle (the FP8 quotient -0 / s is -0)
+    M, W = 6, 1024
+    g = torch.Generator().manual_seed(17)
+    src = (torch.randn(M, W, generator=g) * 2.0).to(dtype)
+    src[:, 0::7] = 0.0
+    src[:, 3::7] = -0.0
+    q, s = quantize_fp8(src.to(DEV), fmt=fmt)
+    torch.cuda.synchronize()
+    bits = src.contiguous().view(torch.int16).numpy().view(np.uint16)
+    ref = oracle.quantize(fmt, bits, fp16=dtype == torch.float16)
+    np.testing.assert_array_equal(q.cpu().numpy(), ref["q"])
+    assert (q.cpu().numpy()[:, 3::7] == 0x80).all() and (q.cpu().numpy()[:, 0::7] == 0x00).all()
