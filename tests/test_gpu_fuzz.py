@@ -29,8 +29,8 @@ def _width(rng, fmt, lo=1):
     return int(g * rng.integers(lo, 16384 // g + 1))
 
 
-def _rows(rng, W):
-    return int(rng.integers(1, max(2, min(300, MAX_ELEMS // W)) + 1))
+def _rows(rng, W, max_rows=300, max_elems=MAX_ELEMS):
+    return int(rng.integers(1, max(2, min(max_rows, max_elems // W)) + 1))
 
 
 def _layout(rng, fmt):
@@ -41,7 +41,7 @@ def _layout(rng, fmt):
     return "row"
 
 
-def _cases(n=48, seed=2024):
+def _cases(n=48, seed=2024, max_rows=300, max_elems=MAX_ELEMS):
     rng = np.random.default_rng(seed)
     out = []
     for i in range(n):
@@ -60,7 +60,7 @@ def _cases(n=48, seed=2024):
         else:
             c.update(W=_width(rng, fmt), Wb=_width(rng, fmt), fp16=bool(rng.random() < 0.3), gemma=bool(rng.random() < 0.5),
                      qb=bool(rng.random() < 0.5))
-        c["M"] = _rows(rng, max(c["W"], c.get("Wb", 0)))
+        c["M"] = _rows(rng, max(c["W"], c.get("Wb", 0)), max_rows, max_elems)
         out.append(c)
     return out
 
@@ -68,6 +68,10 @@ def _cases(n=48, seed=2024):
 # a second draw of twice as many cases (it found the -0 code, the layout-dependent plan and the
 # tie counts of fp32-source FP8 norms that the first draw had missed)
 CASES = _cases() + _cases(n=96, seed=7919)
+
+
+# and cases of up to 9000 rows and 4M elements a launch (the exact-fit and many-rows-a-CTA plans)
+CASES += _cases(n=40, seed=4242, max_rows=9000, max_elems=1 << 22)
 
 
 def _name(c):

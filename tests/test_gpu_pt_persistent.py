@@ -112,3 +112,32 @@ def test_first_persistent_launch_inside_graph_capture():
     assert torch.equal(q, q2) and torch.equal(s, s2)
     ref = oracle.quantize("per_token", _bits(rmsnorm_add(x, w, gemma=False)[0]), fp16=True)
     np.testing.assert_array_equal(q.cpu().numpy(), ref["q"])
+
+
+_rng = np.random.default_rng(99)
+# seeded narrow per-token shapes at large M: width a multiple of 8 up to 2048, 2400-12000 rows,
+# fp16 or bf16, either quant source, either weight form
+RANDOM = [(int(8 * _rng.integers(1, 257)), int(_rng.integers(2400, 12000)), bool(_rng.random() < 0.3),
+           bool(_rng.random() < 0.5), bool(_rng.random() < 0.5)) for _ in range(24)]
+
+
+@pytest.mark.parametrize("c", RANDOM, ids=lambda c: "W{}-M{}-f16{}-f32{}-gemma{}".format(*c))
+def test_random_large_m_per_token_shapes(c):
+    W, M, f16, f32, gemma = c
+    dt = torch.float16 if f16 else torch.bfloat16
+    t = inputs.norm_inputs(M, W, seed=W + M, x_std=1.0, r_std=None, w_mean=0.0 if gemma else 1.0, w_std=0.1)
+    x, w = t["x"].to(dt), t["w"].to(dt)
+    q, s, n, _ = rmsnorm_add_quant(x.to(DEV), w.to(DEV), fmt="per_token", gemma=gemma, quant_from_fp32=f32,
+                                   normed=True)
+    nb, _ = rmsnorm_add(x.to(DEV), w.to(DEV), gemma=gemma)
+    torch.cuda.synchronize()
+    assert torch.equal(n, nb)
+    if not f32:
+        q2, s2 = quantize_fp8(nb, fmt="per_token")
+        torch.cuda.synchronize()
+        assert torch.equal(q, q2) and torch.equal(s, s2)
+    rows = np.unique(np.r_[0, np.random.default_rng(W + M).integers(0, M, 64), M - 1])
+    ref = oracle.rmsnorm_add_quant("per_token", _bits(x)[rows], None, _bits(w), eps=1e-6, gemma=gemma, from_fp32=f32,
+                                   normed=True, fp16=f16)
+    check_norm("per_token", ref, q.cpu().numpy()[rows], s.cpu().numpy()[rows], _bits(n)[rows], None, from_fp32=f32,
+               budget=False)
