@@ -11,7 +11,10 @@ The three steps of the unfused chains they replace are exported too, one
 launch each, to run and time beside them: `rmsnorm_add` (norm to bf16),
 `swiglu` (activation to bf16) and `quantize_fp8` (FP8 quant of bf16 rows).
 `rmsnorm_dual_quant` norms two row sets (the q and kv latent norms) in one
-launch. The norms and the quant also take fp16 activations.
+launch, and `allreduce_rmsnorm_add_quant` folds a tensor-parallel all-reduce
+(the ranks' partial rows summed in rank order) into the fused norm; the `tp`
+module holds its two-shot row partition and gather. The norms and the quant
+also take fp16 activations.
 
 Formats: MXFP8 (E4M3 + one E8M0 scale per 1x32 block), 1x128 block FP8 with
 fp32 scales, and per-token FP8 with an [M,1] fp32 scale.
