@@ -35,7 +35,7 @@ MAX_TIE_MISMATCH_FRACTION = 1e-3     # code mismatches at the oracle's exact tie
 FP32_SCALE_REL = 2.0 ** -20
 
 
-def budget_verdict(n_mism: int, n_tie: int, n_plain: int) -> tuple:
+def budget_result(n_mism: int, n_tie: int, n_plain: int) -> tuple:
     """(ok, message) of the code-mismatch budget: n_mism mismatches over
     n_plain compared elements, n_tie of them at exact ties."""
     other = n_mism - n_tie
@@ -94,7 +94,7 @@ def check_quant(fmt: str, ref: dict, q: np.ndarray, scale: np.ndarray, from_fp32
     budget=False leaves out the mismatch-fraction tests (every other test
     still applies), for callers that check the fractions over several row
     blocks at once from the returned counts `code_mismatch`, `tie_mismatch`
-    and `n_plain` (budget_verdict)."""
+    and `n_plain` (budget_result)."""
     q = np.asarray(q)
     scale = np.asarray(scale)
     M, W = ref["q"].shape
@@ -139,7 +139,7 @@ def check_quant(fmt: str, ref: dict, q: np.ndarray, scale: np.ndarray, from_fp32
     frac = float(mism.sum()) / max(n_plain, 1)
     stats["tie_mismatch"] = int((mism & tie).sum())
     if budget:
-        ok, msg = budget_verdict(int(mism.sum()), stats["tie_mismatch"], n_plain)
+        ok, msg = budget_result(int(mism.sum()), stats["tie_mismatch"], n_plain)
         assert ok, msg
     if excused.any():
         dq_ref = _dequant(fmt, ref["q"], rs, gs)

@@ -10,7 +10,7 @@ import concurrent.futures as cf
 import os
 
 import oracle
-from oracle.parity import budget_verdict, check_norm, check_swiglu
+from oracle.parity import budget_result, check_norm, check_swiglu
 
 BLOCK = 256
 
@@ -37,7 +37,7 @@ def _merge(parts: list) -> dict:
 
 def _finish(parts: list) -> dict:
     st = _merge(parts)
-    ok, msg = budget_verdict(st.get("code_mismatch", 0), st.get("tie_mismatch", 0), st.get("n_plain", 0))
+    ok, msg = budget_result(st.get("code_mismatch", 0), st.get("tie_mismatch", 0), st.get("n_plain", 0))
     assert ok, msg
     return st
 
